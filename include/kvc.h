@@ -1,0 +1,267 @@
+/*
+ * kvc.h -- C ABI of libkvc: online token-eviction compaction of a paged KV
+ * cache on one GB300 (sm_103a).
+ *
+ * The five calls below are, in order, the data-parallel hot path:
+ *
+ *   kvc_score        proxy-query attention-mass score of every cached key
+ *   kvc_select_topm  top-m positions per (layer, KV head, sequence)
+ *   kvc_plan_compact conflict-free slot plan (tail target region)
+ *   kvc_compact      one parallel copy of the retained entries
+ *   kvc_free_pages   emptied blocks back to the allocator
+ *
+ * Sources (web pages on online KV-cache compaction):
+ *   [TE]  "Practical Online KV Cache Compaction for LLM Agents: An Empirical
+ *         Study" (tutorial page), section on the design space: proxy queries
+ *         Q (q x d) give attention weights alpha_ij over the context to be
+ *         compacted; s_j(Q,K) = ((1/q) sum_i alpha_ij^2)^(1/2); the top-m
+ *         positions keep their raw Key/Value, the rest are dropped; keep
+ *         ratio 0.2; delayed (next-turn) queries as proxies.
+ *   [ACT] "ActKV 解剖" (zhichai.net analysis of ActKV), paragraph on the third
+ *         component: attention recovered as exp(logits - LSE) without the
+ *         full attention matrix; a conflict-free slot plan whose target is
+ *         the last X logical blocks, retained entries outside it paired
+ *         one-to-one with holes inside it, one parallel copy, emptied blocks
+ *         returned to the scheduler, no extra KV buffer; budget paragraph:
+ *         512 entries, x1.75 per growth step, cap 30 000.
+ *   [SE]  "AI智能体记忆越用越长，推理引擎为何跟不上" (SparseEngine article):
+ *         the application names a history range and a retain ratio
+ *         (controllable prefix-cache pruning); Chain Cache keeps the logical
+ *         prefix apart from physical storage.
+ *
+ * Conventions
+ *   Ownership: the caller owns every buffer; the library allocates no device
+ *     or pinned memory and keeps no state across calls except the device
+ *     status word (kvc_read_device_status) and cached TMA descriptors.
+ *   Pointers: device pointers unless marked "host".  k_pool, v_pool, q and
+ *     workspaces must be 16-byte aligned.
+ *   Streams: every call is asynchronous on `stream` (0 = legacy default
+ *     stream) and performs no implicit synchronisation.  Calls of one
+ *     compaction must be issued in order on the same stream.
+ *   Errors: arguments are validated on the host before any launch; a bad
+ *     argument returns a negative kvc_status and launches nothing.  The text
+ *     of the last error of the calling thread is kvc_last_error().  Errors a
+ *     kernel detects (bounded wait expired, free stack overflow, a block-table
+ *     entry out of range) set bits of the device status word instead of
+ *     trapping.
+ *   Cache layout (all layers share one block table and one page id space):
+ *     k_pool, v_pool  bf16  [L][num_pages][H][P][d]  (H = KV heads)
+ *     tags            int32 [L][num_pages][H][P]     logical position of the
+ *                     entry in the slot, -1 = empty/dead ([SE] Chain Cache)
+ *     block_table     int32 [B][max_blocks], nblocks int32 [B]
+ *   Slot coordinates: slot s of sequence b lives in page
+ *     block_table[b][s / P] at offset s % P.  A segment is a slot range
+ *     [seg_start, seg_end) of one sequence: seg_start % P == 0 and
+ *     (seg_end % P == 0 or seg_end == seq_len[b]).
+ *   Supported: d in {64, 128}; P a power of two in [8, 64]; 1 <= R <= 4096;
+ *     L*num_pages*H*P < 2^31.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kvc_status;
+#define KVC_OK 0
+#define KVC_ERR_INVALID_ARG (-1)       /* null pointer, bad size or alignment   */
+#define KVC_ERR_UNALIGNED_SEGMENT (-2) /* segment not on block boundaries       */
+#define KVC_ERR_BUDGET (-3)            /* m < 0                                 */
+#define KVC_ERR_WORKSPACE (-4)         /* workspace or plan buffer too small    */
+#define KVC_ERR_UNSUPPORTED (-5)       /* d, P or R outside the supported set   */
+#define KVC_ERR_CUDA (-6)              /* CUDA runtime/driver error             */
+#define KVC_ERR_DEVICE_CHECK (-7)      /* device status word has a bit set      */
+
+/* Device status word bits (kvc_read_device_status). */
+#define KVC_DEV_WAIT_TIMEOUT 1u /* a bounded pipeline wait gave up           */
+#define KVC_DEV_FREE_STACK 2u   /* free stack would overflow its capacity   */
+#define KVC_DEV_BAD_PAGE 4u     /* a block-table entry was outside the pool */
+#define KVC_DEV_BAD_KEEP 8u     /* a keep position was outside its segment   */
+
+/* Opaque CUDA stream handle (same object as cudaStream_t). */
+typedef struct CUstream_st *kvc_stream_t;
+
+/* The paged cache.  All pointers are device pointers. */
+typedef struct kvc_cache {
+    void *k_pool;         /* bf16 [L][num_pages][H][P][d]              */
+    void *v_pool;         /* bf16 [L][num_pages][H][P][d]              */
+    int32_t *tags;        /* int32 [L][num_pages][H][P]                */
+    int32_t *block_table; /* int32 [batch][max_blocks]                 */
+    int32_t *nblocks;     /* int32 [batch]: mapped blocks per sequence */
+    int32_t num_layers;   /* L */
+    int32_t num_pages;
+    int32_t num_kv_heads; /* H */
+    int32_t page_size;    /* P */
+    int32_t head_dim;     /* d */
+    int32_t max_blocks;
+    int32_t batch;        /* B */
+} kvc_cache;
+
+/* One segment per sequence, all host memory ([SE]: the application names the
+ * range to prune).  seq_len[b] = slots in use by sequence b (its fill).  A
+ * sequence with seg_start == seg_end takes no part in the call. */
+typedef struct kvc_segments {
+    const int32_t *seg_start; /* host [batch] */
+    const int32_t *seg_end;   /* host [batch] */
+    const int32_t *seq_len;   /* host [batch] */
+    int32_t batch;
+} kvc_segments;
+
+/* Free-page stack of the page allocator (device memory).  Pop =
+ * free_ids[--free_top], push = free_ids[free_top++]. */
+typedef struct kvc_allocator {
+    int32_t *free_ids; /* int32 [capacity] */
+    int32_t *free_top; /* int32 [1]        */
+    int32_t capacity;
+} kvc_allocator;
+
+/* Output of kvc_plan_compact, input of kvc_compact / kvc_free_pages.  The
+ * caller allocates every buffer with the element counts of
+ * kvc_plan_buffer_sizes.  A "physical slot" is page * P + offset.
+ *   moves      int32 [L][H][Mtot][2]  (src, dst) physical slots; unit
+ *              (l, h, b) owns entries [(l*H + h)*Mtot + moff_b, + m_b)
+ *   move_count int32 [L][H][B]        valid moves of each unit
+ *   dead       int32 [L][H][B][P]     holes left empty (tag becomes -1)
+ *   dead_count int32 [L][H][B]
+ *   freed      int32 [Ftot]           page ids to release, sequence order
+ *   new_rows   int32 [B][max_blocks]  block-table rows after the release
+ * Mtot = sum_b min(m_b, n_b); Ftot = sum_b (ceil(n_b/P) - ceil(m_b/P)). */
+typedef struct kvc_plan {
+    int32_t *moves;
+    int32_t *move_count;
+    int32_t *dead;
+    int32_t *dead_count;
+    int32_t *freed;
+    int32_t *new_rows;
+    int64_t moves_len; /* elements available in each buffer (checked) */
+    int64_t units_len; /* move_count / dead_count length             */
+    int64_t dead_len;
+    int64_t freed_len;
+    int64_t new_rows_len;
+} kvc_plan;
+
+typedef struct kvc_plan_sizes {
+    int64_t moves_len;    /* int32 elements: 2 * L * H * Mtot */
+    int64_t units_len;    /* L * H * B                         */
+    int64_t dead_len;     /* L * H * B * P                     */
+    int64_t freed_len;    /* Ftot                              */
+    int64_t new_rows_len; /* B * max_blocks                    */
+    int64_t Mtot;
+    int64_t Ntot;
+} kvc_plan_sizes;
+
+/* ----------------------------------------------------------------- budget */
+
+/* m = min(n, ceil(ratio * n)) -- keep ratio of [TE] (0.2 drops 80%), and
+ * [SE]'s application-specified retain ratio.  The product is taken in
+ * double with a 1e-9*n downward guard so that e.g. 0.07*100 gives 7.
+ * Returns 0 for n <= 0 and clamps to [0, n]. */
+int64_t kvc_budget_from_ratio(int64_t n, double ratio);
+
+/* ActKV's ratchet budget after k growth steps ([ACT] budget paragraph):
+ * min(30000, floor(512 * 1.75^k)).  k < 0 returns -1. */
+int64_t kvc_budget_actkv(int32_t k);
+
+/* ------------------------------------------------------------- hot path */
+
+/* Bytes of workspace kvc_score needs for these segments and R proxy rows.
+ * Returns KVC_OK and writes *bytes, or an argument error. */
+kvc_status kvc_score_workspace_size(const kvc_cache *cache, const kvc_segments *segs, int32_t R,
+                                    size_t *bytes);
+
+/* Scores every key of every segment ([TE] score, [ACT] LSE recovery):
+ *   L_ij  = scale * q_i . k_j  over the n keys of the segment
+ *   LSE_i = log sum_j exp(L_ij)           (softmax over the segment)
+ *   s_j   = sqrt((1/R) sum_i exp(2 (L_ij - LSE_i)))
+ * q      bf16 [B][L][H][R][d], device: the R = q*g proxy rows of the g query
+ *        heads that share KV head h (all rows of the group form Q).
+ * scores out fp32 [L][H][Ntot]; sequence b at offset sum_{b'<b} n_b'.
+ * lse    out fp32 [B][L][H][R] (natural log) or NULL.
+ * ws     device workspace of kvc_score_workspace_size bytes.
+ * Two tensor-core passes (bf16 operands, fp32 accumulation): the first
+ * builds LSE with an online max/sum, the second recomputes the logits and
+ * accumulates alpha^2.  Keys are used as stored (no positional rotation).
+ * scale must be finite and > 0. */
+kvc_status kvc_score(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
+                     int32_t R, float scale, float *scores, float *lse, void *ws, size_t ws_bytes,
+                     kvc_stream_t stream);
+
+/* Bytes of workspace kvc_select_topm needs (may be 0). */
+kvc_status kvc_select_workspace_size(const kvc_cache *cache, const kvc_segments *segs,
+                                     const int32_t *m, size_t *bytes);
+
+/* Keeps the top-m positions of every (layer, head, sequence) ([TE]):
+ * m[b] (host, >= 0, clamped to n_b) positions with the highest score, equal
+ * scores going to the lower position (decided on the fp32 scores), written
+ * in ascending position order, segment-relative.
+ * scores fp32 [L][H][Ntot] as written by kvc_score.
+ * keep   out int32 [L][H][Mtot]; sequence b at offset sum_{b'<b} min(m_b', n_b'). */
+kvc_status kvc_select_topm(const kvc_cache *cache, const kvc_segments *segs, const float *scores,
+                           const int32_t *m, int32_t *keep, void *ws, size_t ws_bytes,
+                           kvc_stream_t stream);
+
+/* Element counts of the plan buffers for these segments and budgets. */
+kvc_status kvc_plan_buffer_sizes(const kvc_cache *cache, const kvc_segments *segs,
+                                 const int32_t *m, kvc_plan_sizes *out);
+
+/* The conflict-free slot plan of [ACT], per (layer, head, sequence):
+ * nb = ceil(n/P), X = ceil(m/P); the target region T is the last X blocks
+ * of the segment; the k-th retained position before T (ascending) is paired
+ * with the k-th hole of T (ascending slot; a hole is a slot of T holding no
+ * retained entry, including slots past the segment end in its last block);
+ * leftover holes are dead.  The first nb - X blocks are to be freed.
+ * Reads the cache (block table) and keep; mutates nothing but the plan. */
+kvc_status kvc_plan_compact(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                            const int32_t *keep, const kvc_plan *plan, kvc_stream_t stream);
+
+/* Executes the plan as one parallel copy ([ACT]): K row, V row and tag of
+ * every move; tag -1 on every dead hole.  Sources lie before T and
+ * destinations inside it, so no entry is both.  Raw K/V bytes are copied
+ * unmodified ([TE]).  Mutates k_pool, v_pool, tags. */
+kvc_status kvc_compact(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                       const kvc_plan *plan, kvc_stream_t stream);
+
+/* Returns the emptied blocks to the allocator ([ACT]): pushes plan->freed
+ * (sequence order, ascending block order) onto the free stack, installs the
+ * new block-table rows (later blocks shift down, vacated entries become -1)
+ * and lowers nblocks[b] by ceil(n_b/P) - ceil(m_b/P).  Logical positions are
+ * untouched: they travel in the tags ([SE] Chain Cache).  Must follow
+ * kvc_plan_compact on the same stream; a stack overflow sets
+ * KVC_DEV_FREE_STACK and pushes nothing. */
+kvc_status kvc_free_pages(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                          const kvc_allocator *alloc, const kvc_plan *plan, kvc_stream_t stream);
+
+/* -------------------------------------------------------------- helpers */
+
+const char *kvc_status_string(kvc_status status);
+
+/* Text of the last error returned on the calling thread ("" if none). */
+const char *kvc_last_error(void);
+
+/* Copies the device status word of the current device to *out (host) and,
+ * if clear != 0, resets it.  Synchronises `stream`. */
+kvc_status kvc_read_device_status(uint32_t *out, int32_t clear, kvc_stream_t stream);
+
+/* Host-side consistency check of a cache's bookkeeping (host copies):
+ * block-table entries of mapped blocks in [0, num_pages) and unique across
+ * all sequences, unmapped entries -1, nblocks[b] <= max_blocks and
+ * ceil(seq_len[b]/P) <= nblocks[b], free-stack entries in range, unique and
+ * disjoint from mapped pages.  seq_len may be NULL.  Returns KVC_OK or
+ * KVC_ERR_INVALID_ARG with the reason in kvc_last_error(). */
+kvc_status kvc_validate_cache_host(const int32_t *block_table, const int32_t *nblocks,
+                                   const int32_t *seq_len, int32_t batch, int32_t max_blocks,
+                                   int32_t num_pages, int32_t page_size, const int32_t *free_ids,
+                                   int32_t free_top);
+
+/* Library version string. */
+const char *kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,681 @@
+// api.cu -- the C ABI of libkvc (declared in include/kvc.h).
+//
+// Host side only: argument validation (before any launch), launch metadata
+// (every grid and offset is derived from the host-known segment lengths and
+// budgets, so the hot path needs no device->host read), TMA descriptors for
+// the paged K pool and the proxy queries, and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "kvc.h"
+
+namespace kvc {
+
+__device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvc_status fail(kvc_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+kvc_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(KVC_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+kvc_status ok() {
+  g_last_error.clear();
+  return KVC_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+kvc_status device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(KVC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& di = cache[dev];
+  if (di.status == nullptr) {
+    e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    di.status = static_cast<unsigned*>(p);
+  }
+  *out = di;
+  return KVC_OK;
+}
+
+// ------------------------------------------------------------- validation
+
+enum Need : unsigned {
+  kNeedK = 1, kNeedV = 2, kNeedTags = 4, kNeedBT = 8, kNeedNB = 16,
+};
+
+kvc_status check_cache(const kvc_cache* c, unsigned need) {
+  if (c == nullptr) return fail(KVC_ERR_INVALID_ARG, "cache is NULL");
+  if (c->num_layers <= 0 || c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 ||
+      c->head_dim <= 0 || c->max_blocks <= 0 || c->batch <= 0)
+    return fail(KVC_ERR_INVALID_ARG, "cache dimensions must be positive");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+  const int P = c->page_size;
+  if (P < 8 || P > 64 || (P & (P - 1)) != 0)
+    return fail(KVC_ERR_UNSUPPORTED, "page_size %d (supported: 8, 16, 32, 64)", P);
+  const int64_t rows = (int64_t)c->num_layers * c->num_pages * c->num_kv_heads * P;
+  if (rows >= (int64_t(1) << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "L*num_pages*H*P = %lld exceeds 2^31", (long long)rows);
+  if ((need & kNeedK) && (c->k_pool == nullptr || !aligned16(c->k_pool)))
+    return fail(KVC_ERR_INVALID_ARG, "k_pool is NULL or not 16-byte aligned");
+  if ((need & kNeedV) && (c->v_pool == nullptr || !aligned16(c->v_pool)))
+    return fail(KVC_ERR_INVALID_ARG, "v_pool is NULL or not 16-byte aligned");
+  if ((need & kNeedTags) && c->tags == nullptr) return fail(KVC_ERR_INVALID_ARG, "tags is NULL");
+  if ((need & kNeedBT) && c->block_table == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "block_table is NULL");
+  if ((need & kNeedNB) && c->nblocks == nullptr) return fail(KVC_ERR_INVALID_ARG, "nblocks is NULL");
+  return KVC_OK;
+}
+
+// One active sequence (n > 0) of a call.
+struct Seq {
+  int32_t b, s0, n, m, nb, X;
+};
+
+struct Plan {
+  std::vector<Seq> seqs;  // active sequences, ascending b
+  int64_t Ntot = 0, Mtot = 0, Ftot = 0;
+  std::vector<int64_t> off, moff, foff;  // per active sequence
+};
+
+kvc_status build_plan(const kvc_cache* c, const kvc_segments* s, const int32_t* m, Plan* out) {
+  if (s == nullptr || s->seg_start == nullptr || s->seg_end == nullptr || s->seq_len == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "segments or one of its arrays is NULL");
+  if (s->batch != c->batch)
+    return fail(KVC_ERR_INVALID_ARG, "segments batch %d != cache batch %d", s->batch, c->batch);
+  const int P = c->page_size;
+  Plan p;
+  for (int b = 0; b < s->batch; ++b) {
+    const int32_t s0 = s->seg_start[b], s1 = s->seg_end[b], len = s->seq_len[b];
+    if (len < 0 || ceil_div(len, P) > c->max_blocks)
+      return fail(KVC_ERR_INVALID_ARG, "seq_len[%d] = %d does not fit max_blocks", b, len);
+    if (s0 < 0 || s1 < s0 || s1 > len)
+      return fail(KVC_ERR_INVALID_ARG, "segment %d = [%d, %d) outside [0, %d]", b, s0, s1, len);
+    if (s0 % P != 0 || (s1 % P != 0 && s1 != len))
+      return fail(KVC_ERR_UNALIGNED_SEGMENT,
+                  "segment %d = [%d, %d) must start on a block boundary and end on one or at the "
+                  "sequence end (%d)",
+                  b, s0, s1, len);
+    int32_t mb = 0;
+    if (m != nullptr) {
+      if (m[b] < 0) return fail(KVC_ERR_BUDGET, "m[%d] = %d < 0", b, m[b]);
+      mb = std::min(m[b], s1 - s0);
+    }
+    const int32_t n = s1 - s0;
+    if (n == 0) continue;
+    Seq q{b, s0, n, mb, (int32_t)ceil_div(n, P), (int32_t)ceil_div(mb, P)};
+    p.seqs.push_back(q);
+    p.off.push_back(p.Ntot);
+    p.moff.push_back(p.Mtot);
+    p.foff.push_back(p.Ftot);
+    p.Ntot += n;
+    p.Mtot += mb;
+    p.Ftot += q.nb - q.X;
+  }
+  // rows before an active sequence's offsets in the ragged [L][H][Ntot] layout
+  if (p.Ntot >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "sum of segment lengths >= 2^31");
+  // offsets of inactive sequences are not needed: they own no entries
+  *out = std::move(p);
+  return KVC_OK;
+}
+
+LaunchMeta base_meta(const kvc_cache* c, const Plan& p) {
+  LaunchMeta lm;
+  std::memset(&lm, 0, sizeof lm);
+  lm.L = c->num_layers;
+  lm.H = c->num_kv_heads;
+  lm.P = c->page_size;
+  lm.d = c->head_dim;
+  lm.num_pages = c->num_pages;
+  lm.max_blocks = c->max_blocks;
+  lm.B = c->batch;
+  lm.Ntot = p.Ntot;
+  lm.Mtot = p.Mtot;
+  lm.Ftot = p.Ftot;
+  return lm;
+}
+
+void fill_seq(SeqMeta* sm, const Plan& p, size_t i) {
+  const Seq& q = p.seqs[i];
+  sm->b = q.b;
+  sm->s0 = q.s0;
+  sm->n = q.n;
+  sm->m = q.m;
+  sm->nb = q.nb;
+  sm->X = q.X;
+  sm->split = 1;
+  sm->off = p.off[i];
+  sm->moff = p.moff[i];
+  sm->foff = p.foff[i];
+}
+
+// Splits the active sequences into launch chunks of at most kMaxSeqPerLaunch.
+std::vector<std::pair<size_t, size_t>> chunks_of(const Plan& p) {
+  std::vector<std::pair<size_t, size_t>> ch;
+  for (size_t i = 0; i < p.seqs.size(); i += kMaxSeqPerLaunch)
+    ch.emplace_back(i, std::min(p.seqs.size(), i + (size_t)kMaxSeqPerLaunch));
+  return ch;
+}
+
+// ------------------------------------------------------------- scoring
+
+struct ScoreGeom {
+  int R, R_pad, W, nchunks, rowtiles;
+};
+
+ScoreGeom score_geom(int R) {
+  ScoreGeom g;
+  g.R = R;
+  const int R32 = (int)ceil_div(R, 32) * 32;
+  g.nchunks = (int)ceil_div(R32, 256);
+  g.W = (int)ceil_div(ceil_div(R, g.nchunks), 32) * 32;
+  g.R_pad = g.W * g.nchunks;
+  g.rowtiles = (int)ceil_div(R, 128);
+  return g;
+}
+
+int pass1_split(int n) {
+  const int T = (int)ceil_div(n, 128);
+  return std::max(1, std::min(T, (int)ceil_div(T, 16)));
+}
+
+struct ScorePlan {
+  std::vector<LaunchMeta> p1, comb, p2;
+  size_t part_bytes = 0, obias_bytes = 0;
+};
+
+void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, float scale, ScorePlan* sp) {
+  const int64_t LH = (int64_t)c->num_layers * c->num_kv_heads;
+  int64_t max_p1 = 0;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta a = base_meta(c, p), k = base_meta(c, p), z = base_meta(c, p);
+    for (LaunchMeta* lm : {&a, &k, &z}) {
+      lm->nseq = (int)(hi - lo);
+      lm->R = g.R;
+      lm->R_pad = g.R_pad;
+      lm->W = g.W;
+      lm->nchunks = g.nchunks;
+      lm->rowtiles = g.rowtiles;
+      lm->scale = scale;
+    }
+    int64_t i1 = 0, ic = 0, i2 = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      const size_t j = i - lo;
+      for (LaunchMeta* lm : {&a, &k, &z}) fill_seq(&lm->seq[j], p, i);
+      const int split = pass1_split(p.seqs[i].n);
+      const int T = (int)ceil_div(p.seqs[i].n, 128);
+      a.seq[j].split = k.seq[j].split = z.seq[j].split = split;
+      a.seq[j].item0 = i1;
+      k.seq[j].item0 = ic;
+      k.seq[j].item1 = i1;
+      z.seq[j].item0 = i2;
+      i1 += LH * split * g.rowtiles;
+      ic += LH * g.R_pad;
+      i2 += LH * T;
+    }
+    a.items = i1;
+    k.items = ic;
+    z.items = i2;
+    max_p1 = std::max(max_p1, i1);
+    sp->p1.push_back(a);
+    sp->comb.push_back(k);
+    sp->p2.push_back(z);
+  }
+  sp->part_bytes = (size_t)max_p1 * 128 * sizeof(float2);
+  sp->obias_bytes = (size_t)c->batch * LH * g.R_pad * sizeof(float);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][d] with a {64, box_rows} box and 128-byte swizzle.
+kvc_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
+
+const char* kvc_last_error(void) { return g_last_error.c_str(); }
+
+const char* kvc_status_string(kvc_status st) {
+  switch (st) {
+    case KVC_OK: return "KVC_OK";
+    case KVC_ERR_INVALID_ARG: return "KVC_ERR_INVALID_ARG";
+    case KVC_ERR_UNALIGNED_SEGMENT: return "KVC_ERR_UNALIGNED_SEGMENT";
+    case KVC_ERR_BUDGET: return "KVC_ERR_BUDGET";
+    case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
+    case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
+    case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
+    case KVC_ERR_DEVICE_CHECK: return "KVC_ERR_DEVICE_CHECK";
+    default: return "KVC_ERR_UNKNOWN";
+  }
+}
+
+int64_t kvc_budget_from_ratio(int64_t n, double ratio) {
+  if (n <= 0 || !std::isfinite(ratio)) return 0;
+  const double x = ratio * (double)n - 1e-9 * (double)n;
+  int64_t m = (int64_t)std::ceil(x);
+  return std::max<int64_t>(0, std::min<int64_t>(m, n));
+}
+
+int64_t kvc_budget_actkv(int32_t k) {
+  if (k < 0) return -1;
+  // 512 * (7/4)^k = 7^k * 2^(9 - 2k), floored, capped at 30000
+  int64_t num = 512;
+  int64_t den = 1;
+  for (int i = 0; i < k; ++i) {
+    if (num / den >= 30000) return 30000;
+    num *= 7;
+    den *= 4;
+  }
+  return std::min<int64_t>(30000, num / den);
+}
+
+kvc_status kvc_score_workspace_size(const kvc_cache* cache, const kvc_segments* segs, int32_t R,
+                                    size_t* bytes) {
+  kvc_status st = check_cache(cache, 0);
+  if (st != KVC_OK) return st;
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  if (R < 1 || R > 4096) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..4096)", R);
+  Plan p;
+  if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
+  ScorePlan sp;
+  build_score_plan(cache, p, score_geom(R), 1.0f, &sp);
+  *bytes = align256(sp.part_bytes) + align256(sp.obias_bytes);
+  return ok();
+}
+
+kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
+                     float scale, float* scores, float* lse, void* ws, size_t ws_bytes,
+                     kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedK | kNeedBT);
+  if (st != KVC_OK) return st;
+  if (R < 1 || R > 4096) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..4096)", R);
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(KVC_ERR_INVALID_ARG, "scale must be finite and > 0");
+  Plan p;
+  if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  if (q == nullptr || !aligned16(q)) return fail(KVC_ERR_INVALID_ARG, "q is NULL or not 16-byte aligned");
+  if (scores == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores is NULL");
+  const ScoreGeom g = score_geom(R);
+  ScorePlan sp;
+  build_score_plan(cache, p, g, scale, &sp);
+  const size_t need = align256(sp.part_bytes) + align256(sp.obias_bytes);
+  if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+
+  const int64_t krows = (int64_t)cache->num_layers * cache->num_pages * cache->num_kv_heads * cache->page_size;
+  const int64_t qrows = (int64_t)cache->batch * cache->num_layers * cache->num_kv_heads * R;
+  if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
+  CUtensorMap tmK, tmQ1, tmQ2;
+  if ((st = make_tmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
+  if ((st = make_tmap(&tmQ1, q, qrows, cache->head_dim, 128)) != KVC_OK) return st;
+  if ((st = make_tmap(&tmQ2, q, qrows, cache->head_dim, g.W)) != KVC_OK) return st;
+
+  ScoreLaunch sl;
+  sl.d = cache->head_dim;
+  sl.num_sms = di.num_sms;
+  sl.chunks = sp.p1.size();
+  sl.pass1 = sp.p1.data();
+  sl.combine = sp.comb.data();
+  sl.pass2 = sp.p2.data();
+  sl.tmK = &tmK;
+  sl.tmQ1 = &tmQ1;
+  sl.tmQ2 = &tmQ2;
+  sl.block_table = cache->block_table;
+  sl.part = static_cast<float2*>(ws);
+  sl.obias = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes));
+  sl.lse_out = lse;
+  sl.scores = scores;
+  sl.status = di.status;
+  const cudaError_t e = launch_score(sl, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_score launch");
+  return ok();
+}
+
+kvc_status kvc_select_workspace_size(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                                     size_t* bytes) {
+  kvc_status st = check_cache(cache, 0);
+  if (st != KVC_OK) return st;
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  *bytes = 0;
+  return ok();
+}
+
+kvc_status kvc_select_topm(const kvc_cache* cache, const kvc_segments* segs, const float* scores,
+                           const int32_t* m, int32_t* keep, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  kvc_status st = check_cache(cache, 0);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if (p.seqs.empty() || p.Mtot == 0) return ok();
+  if (scores == nullptr || keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores or keep is NULL");
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  std::vector<LaunchMeta> metas;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta lm = base_meta(cache, p);
+    lm.nseq = (int)(hi - lo);
+    int64_t it = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      fill_seq(&lm.seq[i - lo], p, i);
+      lm.seq[i - lo].item0 = it;
+      it += LH;
+    }
+    lm.items = it;
+    metas.push_back(lm);
+  }
+  SelectLaunch sl;
+  sl.num_sms = di.num_sms;
+  sl.chunks = metas.size();
+  sl.meta = metas.data();
+  sl.scores = scores;
+  sl.keep = keep;
+  sl.status = di.status;
+  const cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_select_topm launch");
+  return ok();
+}
+
+kvc_status kvc_plan_buffer_sizes(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                                 kvc_plan_sizes* out) {
+  kvc_status st = check_cache(cache, 0);
+  if (st != KVC_OK) return st;
+  if (m == nullptr || out == nullptr) return fail(KVC_ERR_INVALID_ARG, "m or out is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  out->moves_len = 2 * LH * p.Mtot;
+  out->units_len = LH * cache->batch;
+  out->dead_len = LH * cache->batch * cache->page_size;
+  out->freed_len = p.Ftot;
+  out->new_rows_len = (int64_t)cache->batch * cache->max_blocks;
+  out->Mtot = p.Mtot;
+  out->Ntot = p.Ntot;
+  return ok();
+}
+
+namespace {
+
+kvc_status check_plan(const kvc_cache* cache, const Plan& p, const kvc_plan* plan) {
+  if (plan == nullptr) return fail(KVC_ERR_INVALID_ARG, "plan is NULL");
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  struct { const int32_t* ptr; int64_t have, need; const char* name; } bufs[] = {
+      {plan->moves, plan->moves_len, 2 * LH * p.Mtot, "moves"},
+      {plan->move_count, plan->units_len, LH * cache->batch, "move_count"},
+      {plan->dead, plan->dead_len, LH * cache->batch * cache->page_size, "dead"},
+      {plan->dead_count, plan->units_len, LH * cache->batch, "dead_count"},
+      {plan->freed, plan->freed_len, p.Ftot, "freed"},
+      {plan->new_rows, plan->new_rows_len, (int64_t)cache->batch * cache->max_blocks, "new_rows"},
+  };
+  for (const auto& b : bufs) {
+    if (b.need > 0 && (b.ptr == nullptr || b.have < b.need))
+      return fail(KVC_ERR_WORKSPACE, "plan buffer %s needs %lld elements (have %lld)", b.name,
+                  (long long)b.need, (long long)b.have);
+  }
+  return KVC_OK;
+}
+
+void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta>* plan_m,
+                   std::vector<LaunchMeta>* rows_m, std::vector<LaunchMeta>* copy_m,
+                   std::vector<LaunchMeta>* free_m) {
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  const int P = cache->page_size;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta a = base_meta(cache, p), r = base_meta(cache, p), c = base_meta(cache, p),
+               f = base_meta(cache, p);
+    const int nseq = (int)(hi - lo);
+    a.nseq = r.nseq = c.nseq = f.nseq = nseq;
+    int64_t ia = 0, ic = 0, fc = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      const size_t j = i - lo;
+      for (LaunchMeta* lm : {&a, &r, &c, &f}) fill_seq(&lm->seq[j], p, i);
+      const Seq& q = p.seqs[i];
+      a.seq[j].item0 = ia;
+      ia += LH * std::max<int64_t>(1, ceil_div((int64_t)q.X * P, 256));
+      c.seq[j].item0 = ic;  // chunk-local prefix of m
+      ic += q.m;
+      fc += q.nb - q.X;
+    }
+    a.items = ia;
+    c.items = LH * ic;
+    f.Ftot = fc;
+    plan_m->push_back(a);
+    rows_m->push_back(r);
+    copy_m->push_back(c);
+    free_m->push_back(f);
+  }
+}
+
+}  // namespace
+
+kvc_status kvc_plan_compact(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                            const int32_t* keep, const kvc_plan* plan, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if ((st = check_plan(cache, p, plan)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  if (p.Mtot > 0 && keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  std::vector<LaunchMeta> pm, rm, cm, fm;
+  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  CompactLaunch cl;
+  cl.num_sms = di.num_sms;
+  cl.chunks = pm.size();
+  cl.plan_meta = pm.data();
+  cl.rows_meta = rm.data();
+  cl.block_table = cache->block_table;
+  cl.nblocks = cache->nblocks;
+  cl.keep = keep;
+  cl.moves = plan->moves;
+  cl.move_count = plan->move_count;
+  cl.dead = plan->dead;
+  cl.dead_count = plan->dead_count;
+  cl.freed = plan->freed;
+  cl.new_rows = plan->new_rows;
+  cl.status = di.status;
+  const cudaError_t e = launch_plan(cl, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_plan_compact launch");
+  return ok();
+}
+
+kvc_status kvc_compact(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                       const kvc_plan* plan, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedTags);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if ((st = check_plan(cache, p, plan)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  std::vector<LaunchMeta> pm, rm, cm, fm;
+  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  CompactLaunch cl;
+  cl.num_sms = di.num_sms;
+  cl.chunks = cm.size();
+  cl.copy_meta = cm.data();
+  cl.k_pool = cache->k_pool;
+  cl.v_pool = cache->v_pool;
+  cl.tags = cache->tags;
+  cl.moves = plan->moves;
+  cl.move_count = plan->move_count;
+  cl.dead = plan->dead;
+  cl.dead_count = plan->dead_count;
+  cl.status = di.status;
+  const cudaError_t e = launch_compact(cl, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_compact launch");
+  return ok();
+}
+
+kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                          const kvc_allocator* alloc, const kvc_plan* plan, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  if (alloc == nullptr || alloc->free_ids == nullptr || alloc->free_top == nullptr || alloc->capacity < 0)
+    return fail(KVC_ERR_INVALID_ARG, "allocator is NULL or incomplete");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if ((st = check_plan(cache, p, plan)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  std::vector<LaunchMeta> pm, rm, cm, fm;
+  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  CompactLaunch cl;
+  cl.num_sms = di.num_sms;
+  cl.chunks = fm.size();
+  cl.free_meta = fm.data();
+  cl.block_table_mut = cache->block_table;
+  cl.nblocks = cache->nblocks;
+  cl.new_rows = plan->new_rows;
+  cl.freed = plan->freed;
+  cl.free_ids = alloc->free_ids;
+  cl.free_top = alloc->free_top;
+  cl.capacity = alloc->capacity;
+  cl.status = di.status;
+  const cudaError_t e = launch_free(cl, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_free_pages launch");
+  return ok();
+}
+
+kvc_status kvc_read_device_status(uint32_t* out, int32_t clear, kvc_stream_t stream) {
+  if (out == nullptr) return fail(KVC_ERR_INVALID_ARG, "out is NULL");
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(status)");
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(status)");
+  }
+  *out = v;
+  return ok();
+}
+
+kvc_status kvc_validate_cache_host(const int32_t* block_table, const int32_t* nblocks, const int32_t* seq_len,
+                                   int32_t batch, int32_t max_blocks, int32_t num_pages, int32_t page_size,
+                                   const int32_t* free_ids, int32_t free_top) {
+  if (block_table == nullptr || nblocks == nullptr || batch <= 0 || max_blocks <= 0 || num_pages <= 0 ||
+      page_size <= 0)
+    return fail(KVC_ERR_INVALID_ARG, "bad arguments");
+  std::vector<int32_t> owner(num_pages, -1);  // -1 free/unknown, b = mapped by b, -2 on the free stack
+  for (int b = 0; b < batch; ++b) {
+    const int nb = nblocks[b];
+    if (nb < 0 || nb > max_blocks) return fail(KVC_ERR_INVALID_ARG, "nblocks[%d] = %d out of range", b, nb);
+    if (seq_len != nullptr && (seq_len[b] < 0 || ceil_div(seq_len[b], page_size) > nb))
+      return fail(KVC_ERR_INVALID_ARG, "seq_len[%d] = %d needs more than %d blocks", b, seq_len[b], nb);
+    for (int j = 0; j < max_blocks; ++j) {
+      const int32_t pg = block_table[(int64_t)b * max_blocks + j];
+      if (j >= nb) {
+        if (pg != -1) return fail(KVC_ERR_INVALID_ARG, "block_table[%d][%d] = %d past nblocks is not -1", b, j, pg);
+        continue;
+      }
+      if (pg < 0 || pg >= num_pages)
+        return fail(KVC_ERR_INVALID_ARG, "block_table[%d][%d] = %d outside the pool", b, j, pg);
+      if (owner[pg] != -1)
+        return fail(KVC_ERR_INVALID_ARG, "page %d mapped twice (sequence %d block %d)", pg, b, j);
+      owner[pg] = b;
+    }
+  }
+  if (free_ids != nullptr) {
+    if (free_top < 0 || free_top > num_pages) return fail(KVC_ERR_INVALID_ARG, "free_top = %d out of range", free_top);
+    for (int i = 0; i < free_top; ++i) {
+      const int32_t pg = free_ids[i];
+      if (pg < 0 || pg >= num_pages) return fail(KVC_ERR_INVALID_ARG, "free_ids[%d] = %d outside the pool", i, pg);
+      if (owner[pg] >= 0) return fail(KVC_ERR_INVALID_ARG, "page %d is both mapped and free", pg);
+      if (owner[pg] == -2) return fail(KVC_ERR_INVALID_ARG, "page %d is free twice", pg);
+      owner[pg] = -2;
+    }
+  }
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// internal.h -- host-side launch descriptions passed from the C-ABI front end
+// (api.cu) to the kernel launchers (score.cu, select.cu, compact.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "common.cuh"
+
+namespace kvc {
+
+struct ScoreLaunch {
+  int d = 0;
+  int num_sms = 0;
+  size_t chunks = 0;
+  const LaunchMeta* pass1 = nullptr;   // [chunks]
+  const LaunchMeta* combine = nullptr; // [chunks]
+  const LaunchMeta* pass2 = nullptr;   // [chunks]
+  const CUtensorMap* tmK = nullptr;    // K pool, box {64, P}
+  const CUtensorMap* tmQ1 = nullptr;   // Q, box {64, 128}
+  const CUtensorMap* tmQ2 = nullptr;   // Q, box {64, W}
+  const int32_t* block_table = nullptr;
+  float2* part = nullptr;              // pass-1 partials (workspace)
+  float* obias = nullptr;              // per-row pass-2 offsets (workspace)
+  float* lse_out = nullptr;
+  float* scores = nullptr;
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_score(const ScoreLaunch& sl, cudaStream_t stream);
+
+struct SelectLaunch {
+  int num_sms = 0;
+  size_t chunks = 0;
+  const LaunchMeta* meta = nullptr;    // [chunks]; one item per (seq, l, h)
+  const float* scores = nullptr;
+  int32_t* keep = nullptr;
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_select(const SelectLaunch& sl, cudaStream_t stream);
+
+struct CompactLaunch {
+  int num_sms = 0;
+  size_t chunks = 0;
+  const LaunchMeta* plan_meta = nullptr;  // [chunks]; items: (seq, l, h, hole block)
+  const LaunchMeta* rows_meta = nullptr;  // [chunks]; items: (seq, block-table block)
+  const LaunchMeta* copy_meta = nullptr;  // [chunks]; items: (l, h, seq, move)
+  const LaunchMeta* free_meta = nullptr;  // [chunks]
+  const int32_t* block_table = nullptr;
+  int32_t* block_table_mut = nullptr;
+  int32_t* nblocks = nullptr;
+  const int32_t* keep = nullptr;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  int32_t* tags = nullptr;
+  int32_t* moves = nullptr;
+  int32_t* move_count = nullptr;
+  int32_t* dead = nullptr;
+  int32_t* dead_count = nullptr;
+  int32_t* freed = nullptr;
+  int32_t* new_rows = nullptr;
+  int32_t* free_ids = nullptr;
+  int32_t* free_top = nullptr;
+  int32_t capacity = 0;
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream);
+cudaError_t launch_compact(const CompactLaunch& cl, cudaStream_t stream);
+cudaError_t launch_free(const CompactLaunch& cl, cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,162 @@
+// select.cu -- top-m position selection per (layer, KV head, sequence).
+//
+// Token eviction keeps the m positions with the highest score s_j and drops
+// the rest ("Practical Online KV Cache Compaction for LLM Agents", design-space
+// section).  Equal scores go to the lower position; the kept positions are
+// written in ascending order (the order the slot plan consumes them).
+//
+// One 1024-thread CTA per unit.  Scores are >= 0, so their fp32 bit patterns
+// order like the values.  Three radix passes over the bits (11, 11, 10 from
+// the top) find the exact bit pattern T of the m-th largest score and how many
+// elements equal to T are kept (k_eq).  A final pass keeps every element > T
+// and the first k_eq elements == T, and writes each kept position at its rank
+// (warp ballots + a block scan of the warp counts).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kSelThreads = 1024;
+constexpr int kBins = 2048;
+
+__global__ void __launch_bounds__(kSelThreads, 1)
+    select_topm_kernel(const __grid_constant__ LaunchMeta meta, const float* __restrict__ scores,
+                       int32_t* __restrict__ keep) {
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t warp_gt[32], warp_eq[32];
+  __shared__ uint32_t sh_digit, sh_k;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t item = blockIdx.x;
+  const int si = find_seq(meta, item);
+  const SeqMeta& s = meta.seq[si];
+  const int64_t local = item - s.item0;
+  const int h = (int)(local % meta.H);
+  const int l = (int)(local / meta.H);
+  const int n = s.n, m = s.m;
+  const uint32_t* key =
+      reinterpret_cast<const uint32_t*>(scores + ((int64_t)l * meta.H + h) * meta.Ntot + s.off);
+  int32_t* out = keep + ((int64_t)l * meta.H + h) * meta.Mtot + s.moff;
+  if (m <= 0) return;
+  if (m >= n) {
+    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+    return;
+  }
+
+  // ---- radix select of the m-th largest bit pattern
+  uint32_t prefix = 0, pmask = 0, k = (uint32_t)m;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass];
+    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    const int nbins = 1 << widths[pass];
+    for (int i = tid; i < kBins; i += kSelThreads) hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kSelThreads) {  // warp-uniform trip count
+      const int i = base + tid;
+      uint32_t d = 0xFFFFFFFFu;  // "no digit"
+      if (i < n) {
+        const uint32_t u = __ldg(key + i);
+        if ((u & pmask) == prefix) d = (u >> sh) & dmask;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane 0 owns the highest bins; find the digit where the count from the top reaches k
+      const int per = nbins / 32;
+      const int hi = nbins - 1 - lane * per;  // this lane covers digits (hi - per, hi]
+      uint32_t sum = 0;
+      for (int j = 0; j < per; ++j) sum += hist[hi - j];
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t excl = incl - sum;
+      if (excl < k && incl >= k) {
+        uint32_t acc = excl;
+        for (int j = 0; j < per; ++j) {
+          const uint32_t c = hist[hi - j];
+          if (acc + c >= k) {
+            sh_digit = (uint32_t)(hi - j);
+            sh_k = k - acc;
+            break;
+          }
+          acc += c;
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sh_digit << sh;
+    pmask |= dmask << sh;
+    k = sh_k;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;   // bit pattern of the m-th largest score
+  const uint32_t k_eq = k;     // elements equal to T that are kept (lowest positions first)
+
+  // ---- order-preserving compaction
+  uint32_t base_gt = 0, base_eq = 0;
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int start = 0; start < n; start += kSelThreads) {
+    const int i = start + tid;
+    const uint32_t u = (i < n) ? __ldg(key + i) : 0u;
+    const bool gt = (i < n) && (u > T);
+    const bool eq = (i < n) && (u == T);
+    const unsigned bg = __ballot_sync(0xffffffffu, gt);
+    const unsigned be = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      warp_gt[warp] = __popc(bg);
+      warp_eq[warp] = __popc(be);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t g = warp_gt[lane], e = warp_eq[lane];
+      uint32_t ig = g, ie = e;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t tg = __shfl_up_sync(0xffffffffu, ig, o);
+        const uint32_t te = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) { ig += tg; ie += te; }
+      }
+      warp_gt[lane] = ig - g;  // exclusive prefix over warps
+      warp_eq[lane] = ie - e;
+      if (lane == 31) { sh_digit = ig; sh_k = ie; }  // tile totals
+    }
+    __syncthreads();
+    const uint32_t gt_before = base_gt + warp_gt[warp] + __popc(bg & lt_mask);
+    const uint32_t eq_before = base_eq + warp_eq[warp] + __popc(be & lt_mask);
+    const uint32_t rank = gt_before + min(eq_before, k_eq);
+    if ((gt || (eq && eq_before < k_eq)) && rank < (uint32_t)m) out[rank] = i;
+    base_gt += sh_digit;
+    base_eq += sh_k;
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_select(const SelectLaunch& sl, cudaStream_t stream) {
+  for (size_t c = 0; c < sl.chunks; ++c) {
+    const LaunchMeta& m = sl.meta[c];
+    if (m.items <= 0) continue;
+    select_topm_kernel<<<(unsigned)m.items, kSelThreads, 0, stream>>>(m, sl.scores, sl.keep);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace kvc

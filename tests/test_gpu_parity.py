@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs.  Scores, LSE and keep sets follow the rules in tests/parity.py; compaction is checked
+bit-exact given a selection that comes from the oracle or from the seeded generator (never from
+the CUDA path)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_kv_cache_gb300 as kvc
+import workloads
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from online_kv_cache_gb300 import build
+    build.build()
+    kvc.kvc_read_device_status(clear=True)
+
+
+def full_check(case, label, check_lse=True):
+    """Score + select against the oracle on every unit, then compaction bit-exact given the
+    oracle's keep sets.  Returns (max score error, in-band selection differences)."""
+    m_orc = PT.oracle_budgets(case)
+    m_lib = PT.lib_budgets(case)
+    assert m_orc == m_lib, "budget helpers disagree"
+    pristine = PT.host_state(case)
+    snap = case.snapshot()
+    s_orc, lse_orc = PT.oracle_scores(case)
+    keep_orc = oracle.select_cache(s_orc, case.seg_start, case.seg_end, m_orc)
+
+    cp = PT.compactor(case, m_lib)
+    cp.score(case.q, case.spec.scale, True)
+    cp.select()
+    torch.cuda.synchronize()
+    s_gpu = cp.scores.cpu().numpy()[:, :, :cp.Ntot]
+    k_gpu = cp.keep.cpu().numpy()[:, :, :cp.Mtot]
+    worst = PT.check_scores(s_gpu, s_orc, label)
+    if check_lse:
+        lse_gpu = cp.lse.cpu().numpy()
+        for b in range(case.spec.B):
+            if case.seg_end[b] > case.seg_start[b]:
+                PT.check_lse(lse_gpu[b], lse_orc[b], f"{label} lse b={b}")
+    diffs = 0
+    L, H = case.spec.L, case.spec.H
+    noff, moff = PT.unit_offsets(case, m_orc)
+    for l in range(L):
+        for h in range(H):
+            for b in range(case.spec.B):
+                diffs += PT.check_keep(k_gpu[l, h, moff[b]:moff[b + 1]], keep_orc[l, h, moff[b]:moff[b + 1]],
+                                       s_orc[l, h, noff[b]:noff[b + 1]], int(moff[b + 1] - moff[b]),
+                                       f"{label} l={l} h={h} b={b}")
+    # compaction given the oracle's selection
+    keep_dev = torch.from_numpy(np.ascontiguousarray(keep_orc)).to(DEV)
+    cp.plan_compact(keep_dev if keep_orc.size else None)
+    cp.compact()
+    cp.free_pages()
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    PT.assert_state_equal(PT.host_state(case), PT.oracle_compaction(pristine, case, m_orc, keep_orc),
+                          label)
+    # the chain on the GPU's own selection, when it equals the oracle's, gives the same bytes
+    if diffs == 0:
+        case.restore(snap)
+        PT.run_chain(case, m_lib)
+        torch.cuda.synchronize()
+        PT.device_status_clean()
+        PT.assert_state_equal(PT.host_state(case),
+                              PT.oracle_compaction(PT.host_state_from(snap), case, m_orc, keep_orc),
+                              label + " (own selection)")
+    return worst, diffs
+
+
+def test_tiny_workload():
+    case = workloads.build(workloads.spec("tiny"), 0, DEV)
+    planted = case.planted[0].cpu().numpy()  # [L][H][4] segment positions
+    m = PT.lib_budgets(case)
+    assert m == [103]
+    cp = PT.compactor(case, m)
+    cp.score(case.q, case.spec.scale)
+    cp.select()
+    torch.cuda.synchronize()
+    keep = cp.keep.cpu().numpy()
+    for h in range(case.spec.H):
+        assert set(planted[0, h].tolist()) <= set(keep[0, h].tolist()), "planted keys must survive"
+    case2 = workloads.build(workloads.spec("tiny"), 0, DEV)
+    worst, diffs = full_check(case2, "tiny")
+    assert diffs == 0
+
+
+MICRO = [
+    # d, P, G, q, lengths, budget
+    (64, 16, 2, 8, (512,), ("ratio", 0.2)),
+    (128, 16, 8, 16, (1, 15, 16, 17, 32, 129), ("ratio", 0.2)),
+    (128, 8, 4, 1, (7, 8, 9, 300), ("ratio", 0.5)),
+    (64, 32, 1, 1, (4097,), ("ratio", 0.2)),
+    (128, 64, 4, 25, (200, 1000), ("ratio", 0.1)),
+    (128, 16, 8, 64, (2048, 777), ("ratio", 0.2)),          # R = 512: two pass-2 chunks
+    (64, 16, 4, 75, (640,), ("ratio", 0.3)),                # R = 300: padded rows
+    (128, 32, 16, 256, (1536,), ("ratio", 0.2)),            # R = 4096
+    (128, 16, 8, 16, (5000, 3000, 9000), ("actkv", (0, 1, 2))),
+]
+
+
+@pytest.mark.parametrize("d,P,G,q,lengths,budget", MICRO)
+def test_micro_shapes(d, P, G, q, lengths, budget):
+    sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, budget=budget,
+                          shuffle_pages=True)
+    case = workloads.build(sp, 1, DEV)
+    full_check(case, f"micro d={d} P={P} R={sp.R} n={lengths}")
+
+
+@pytest.mark.parametrize("mode", ["zero", "one", "n-1", "all"])
+def test_edge_budgets(mode):
+    sp = workloads.custom(L=1, H=2, G=4, d=128, P=16, q=8, lengths=(100, 47, 16), shuffle_pages=True)
+    case = workloads.build(sp, 2, DEV)
+    n = PT.seg_lengths(case)
+    m = {"zero": [0] * 3, "one": [1] * 3, "n-1": [x - 1 for x in n], "all": n}[mode]
+    pristine = PT.host_state(case)
+    s_orc, _ = PT.oracle_scores(case)
+    keep_orc = oracle.select_cache(s_orc, case.seg_start, case.seg_end, m)
+    cp = PT.compactor(case, m)
+    cp.score(case.q, sp.scale)
+    cp.select()
+    torch.cuda.synchronize()
+    k_gpu = cp.keep.cpu().numpy()[:, :, :cp.Mtot]
+    noff, moff = PT.unit_offsets(case, m)
+    for l in range(sp.L):
+        for h in range(sp.H):
+            for b in range(sp.B):
+                PT.check_keep(k_gpu[l, h, moff[b]:moff[b + 1]], keep_orc[l, h, moff[b]:moff[b + 1]],
+                              s_orc[l, h, noff[b]:noff[b + 1]], int(moff[b + 1] - moff[b]), mode)
+    keep_dev = torch.from_numpy(np.ascontiguousarray(keep_orc)).to(DEV) if keep_orc.size else None
+    cp.plan_compact(keep_dev)
+    cp.compact()
+    cp.free_pages()
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    PT.assert_state_equal(PT.host_state(case), PT.oracle_compaction(pristine, case, m, keep_orc), mode)
+
+
+def test_segments_inside_sequences():
+    """Segments that start past slot 0 and end before the sequence end; a sequence with no
+    segment; a segment ending at a ragged sequence end."""
+    sp = workloads.custom(L=2, H=2, G=4, d=128, P=16, q=8, lengths=(1000, 333, 520),
+                          shuffle_pages=True)
+    case = workloads.build(sp, 3, DEV, with_q=False)
+    case.seg_start = [160, 0, 96]
+    case.seg_end = [800, 0, 520]
+    workloads.make_q(case, 3)
+    full_check(case, "inner segments")
+
+
+def test_given_selection_random_keeps():
+    """Compaction alone, bit-exact, for seeded random keep sets (any selection)."""
+    sp = workloads.custom(L=3, H=2, G=2, d=64, P=8, q=2, lengths=(257, 64, 1023, 8),
+                          shuffle_pages=True)
+    case = workloads.build(sp, 4, DEV)
+    for trial, ratio in enumerate((0.0, 0.05, 0.2, 0.6, 1.0)):
+        m = [oracle.budget_ratio(x, ratio) for x in PT.seg_lengths(case)]
+        snap = case.snapshot()
+        pristine = PT.host_state(case)
+        keep = workloads.random_keep(case, m, 100 + trial)
+        cp = PT.compactor(case, m)
+        cp.plan_compact(keep.contiguous() if keep.numel() else None)
+        cp.compact()
+        cp.free_pages()
+        torch.cuda.synchronize()
+        PT.device_status_clean()
+        PT.assert_state_equal(PT.host_state(case),
+                              PT.oracle_compaction(pristine, case, m, keep.cpu().numpy()),
+                              f"random keep ratio={ratio}")
+        case.restore(snap)
+
+
+def test_logical_view_after_compaction():
+    """T's live slots gathered by ascending tag reproduce the oracle's order-preserving view."""
+    sp = workloads.custom(L=2, H=2, G=4, d=128, P=16, q=8, lengths=(700, 260), shuffle_pages=True)
+    case = workloads.build(sp, 5, DEV)
+    m = PT.lib_budgets(case)
+    pristine = PT.host_state(case)
+    cp = PT.run_chain(case, m)
+    torch.cuda.synchronize()
+    keep = cp.keep.cpu().numpy()[:, :, :cp.Mtot]
+    after = PT.host_state(case)
+    moff = np.concatenate([[0], np.cumsum(m)])
+    P = sp.P
+    for l in range(sp.L):
+        for h in range(sp.H):
+            for b in range(sp.B):
+                kb = keep[l, h, moff[b]:moff[b + 1]]
+                Kc, Vc, pos = oracle.logical_view(pristine["k"], pristine["v"], pristine["tags"], l, h,
+                                                  pristine["bt"][b], case.seg_start[b], kb)
+                n = case.seg_end[b] - case.seg_start[b]
+                nb, X = -(-n // P), -(-len(kb) // P)
+                row = after["bt"][b]
+                slots = [(row[blk] , off) for blk in range(X) for off in range(P)]  # new rows: T first
+                live = [(after["tags"][l, pg, h, off], after["k"][l, pg, h, off], after["v"][l, pg, h, off])
+                        for pg, off in slots if after["tags"][l, pg, h, off] >= 0]
+                live.sort(key=lambda e: e[0])
+                assert [e[0] for e in live] == list(pos)
+                assert np.array_equal(np.array([e[1] for e in live]).reshape(Kc.shape), Kc)
+                assert np.array_equal(np.array([e[2] for e in live]).reshape(Vc.shape), Vc)

@@ -432,3 +432,24 @@ class MultiTurn:
         self.turn_start_slot[t] -= shift
         self.case.seq_len[0] -= shift
         self.case.seg_start[0] = self.case.seg_end[0] = 0
+
+
+def random_keep(case: Case, m: Sequence[int], seed: int) -> torch.Tensor:
+    """A seeded keep set per unit, independent of any score: for every (layer, head, sequence)
+    min(m_b, n_b) distinct segment positions in ascending order, laid out [L][H][Mtot]."""
+    sp = case.spec
+    dev = case.k_pool.device
+    g = _gen(dev, seed, 7)
+    n = [e - s for s, e in zip(case.seg_start, case.seg_end)]
+    mm = [min(int(a), b) for a, b in zip(m, n)]
+    Mtot = sum(mm)
+    keep = torch.empty((sp.L, sp.H, max(1, Mtot)), dtype=torch.int32, device=dev)
+    for l in range(sp.L):
+        for h in range(sp.H):
+            off = 0
+            for b in range(len(n)):
+                if mm[b] > 0:
+                    pick = torch.randperm(n[b], generator=g, device=dev)[:mm[b]]
+                    keep[l, h, off:off + mm[b]] = torch.sort(pick).values.to(torch.int32)
+                off += mm[b]
+    return keep[:, :, :Mtot]
