@@ -190,6 +190,28 @@ kvc_status kvc_score(const kvc_cache *cache, const kvc_segments *segs, const uin
                      int32_t R, float scale, float *scores, float *lse, void *ws, size_t ws_bytes,
                      kvc_stream_t stream);
 
+/* The two passes of kvc_score as separate calls (same arguments, same
+ * workspace; kvc_score == kvc_score_lse followed by kvc_score_alpha).
+ *
+ * kvc_score_lse: pass 1 only -- the per-row LSE over the segment ([ACT]:
+ * log-sum-exp of the logits), kept in the workspace for kvc_score_alpha and
+ * written to `lse` (fp32 [B][L][H][R], natural log) when it is not NULL.
+ *
+ * kvc_score_alpha: pass 2 only -- recomputes the logits and accumulates
+ * alpha^2 into `scores`.  With lse == NULL it uses the LSE that the last
+ * kvc_score_lse call left in `ws` (same cache, segments, R and scale).  With
+ * a caller-supplied lse (fp32 [B][L][H][R], natural log) it normalises by
+ * that instead -- e.g. the log-sum-exp a paged-attention kernel produced for
+ * the same queries over the whole context ([ACT]: the LSE is a by-product of
+ * paged attention), which skips pass 1 entirely. */
+kvc_status kvc_score_lse(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
+                         int32_t R, float scale, float *lse, void *ws, size_t ws_bytes,
+                         kvc_stream_t stream);
+
+kvc_status kvc_score_alpha(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
+                           int32_t R, float scale, const float *lse, float *scores, void *ws,
+                           size_t ws_bytes, kvc_stream_t stream);
+
 /* Bytes of workspace kvc_select_topm needs (may be 0). */
 kvc_status kvc_select_workspace_size(const kvc_cache *cache, const kvc_segments *segs,
                                      const int32_t *m, size_t *bytes);
@@ -256,6 +278,10 @@ kvc_status kvc_validate_cache_host(const int32_t *block_table, const int32_t *nb
                                    const int32_t *seq_len, int32_t batch, int32_t max_blocks,
                                    int32_t num_pages, int32_t page_size, const int32_t *free_ids,
                                    int32_t free_top);
+
+/* Number of kernels the library has launched in this process (all devices)
+ * since the last reset; reset != 0 returns the count and zeroes it. */
+uint64_t kvc_launch_count(int32_t reset);
 
 /* Library version string. */
 const char *kvc_version(void);

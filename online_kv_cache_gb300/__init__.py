@@ -43,7 +43,8 @@ EXPORTED = (
     "kvc_budget_from_ratio", "kvc_budget_actkv", "kvc_score_workspace_size", "kvc_score",
     "kvc_select_workspace_size", "kvc_select_topm", "kvc_plan_buffer_sizes", "kvc_plan_compact",
     "kvc_compact", "kvc_free_pages", "kvc_status_string", "kvc_last_error",
-    "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version",
+    "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
+    "kvc_score_alpha", "kvc_launch_count",
 )
 
 
@@ -129,6 +130,9 @@ def lib():
             "kvc_read_device_status": (I32, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
             "kvc_validate_cache_host": (I32, [P, P, P, I32, I32, I32, I32, P, I32]),
             "kvc_version": (ctypes.c_char_p, []),
+            "kvc_score_lse": (I32, [C, SG, P, I32, F, P, P, S, P]),
+            "kvc_score_alpha": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
+            "kvc_launch_count": (ctypes.c_uint64, [I32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -244,6 +248,25 @@ def kvc_score(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale: floa
                            float(scale), _dev_ptr(scores, "scores", torch.float32),
                            _dev_ptr(lse, "lse", torch.float32), _dev_ptr(ws, "ws"),
                            ws.numel() * ws.element_size(), _stream(stream)), "kvc_score")
+
+
+def kvc_score_lse(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale: float,
+                  lse: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    _check(lib().kvc_score_lse(cache.ref, segs.ref, _dev_ptr(q, "q", torch.bfloat16), int(R),
+                               float(scale), _dev_ptr(lse, "lse", torch.float32), _dev_ptr(ws, "ws"),
+                               ws.numel() * ws.element_size(), _stream(stream)), "kvc_score_lse")
+
+
+def kvc_score_alpha(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale: float,
+                    lse: Optional[torch.Tensor], scores: torch.Tensor, ws: torch.Tensor, stream=None):
+    _check(lib().kvc_score_alpha(cache.ref, segs.ref, _dev_ptr(q, "q", torch.bfloat16), int(R),
+                                 float(scale), _dev_ptr(lse, "lse", torch.float32),
+                                 _dev_ptr(scores, "scores", torch.float32), _dev_ptr(ws, "ws"),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "kvc_score_alpha")
+
+
+def kvc_launch_count(reset: bool = False) -> int:
+    return int(lib().kvc_launch_count(1 if reset else 0))
 
 
 def kvc_select_workspace_size(cache: Cache, segs: Segments, m) -> int:
@@ -377,6 +400,15 @@ class Compactor:
     def score(self, q: torch.Tensor, scale: float, want_lse: bool = True, stream=None):
         kvc_score(self.cache, self.segs, q, self.R, scale, self.scores,
                   self.lse if want_lse else None, self.ws_view, stream)
+
+    def score_lse(self, q: torch.Tensor, scale: float, want_lse: bool = False, stream=None):
+        kvc_score_lse(self.cache, self.segs, q, self.R, scale, self.lse if want_lse else None,
+                      self.ws_view, stream)
+
+    def score_alpha(self, q: torch.Tensor, scale: float, lse: Optional[torch.Tensor] = None,
+                    stream=None):
+        kvc_score_alpha(self.cache, self.segs, q, self.R, scale, lse, self.scores, self.ws_view,
+                        stream)
 
     def select(self, stream=None):
         kvc_select_topm(self.cache, self.segs, self.scores, self.m, self.keep, None, stream)

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -356,9 +357,16 @@ kvc_status kvc_score_workspace_size(const kvc_cache* cache, const kvc_segments* 
   return ok();
 }
 
-kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
-                     float scale, float* scores, float* lse, void* ws, size_t ws_bytes,
-                     kvc_stream_t stream) {
+}  // extern "C"
+
+namespace kvc {
+namespace {
+
+// Validation, descriptors and launches shared by kvc_score, kvc_score_lse and kvc_score_alpha.
+kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cache,
+                        const kvc_segments* segs, const uint16_t* q, int32_t R, float scale,
+                        const float* lse_in, float* lse_out, float* scores, void* ws, size_t ws_bytes,
+                        kvc_stream_t stream) {
   kvc_status st = check_cache(cache, kNeedK | kNeedBT);
   if (st != KVC_OK) return st;
   if (R < 1 || R > 4096) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..4096)", R);
@@ -367,7 +375,8 @@ kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uin
   if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
   if (p.seqs.empty()) return ok();
   if (q == nullptr || !aligned16(q)) return fail(KVC_ERR_INVALID_ARG, "q is NULL or not 16-byte aligned");
-  if (scores == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores is NULL");
+  if ((phases & kPhaseAlpha) && scores == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores is NULL");
+  if ((phases & kPhaseLseIn) && lse_in == nullptr) return fail(KVC_ERR_INVALID_ARG, "lse is NULL");
   const ScoreGeom g = score_geom(R);
   ScorePlan sp;
   build_score_plan(cache, p, g, scale, &sp);
@@ -386,6 +395,8 @@ kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uin
   if ((st = make_tmap(&tmQ2, q, qrows, cache->head_dim, g.W)) != KVC_OK) return st;
 
   ScoreLaunch sl;
+  sl.phases = phases;
+  sl.lse_in = lse_in;
   sl.d = cache->head_dim;
   sl.num_sms = di.num_sms;
   sl.chunks = sp.p1.size();
@@ -398,12 +409,47 @@ kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uin
   sl.block_table = cache->block_table;
   sl.part = static_cast<float2*>(ws);
   sl.obias = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes));
-  sl.lse_out = lse;
+  sl.lse_out = lse_out;
   sl.scores = scores;
   sl.status = di.status;
   const cudaError_t e = launch_score(sl, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "kvc_score launch");
+  if (e != cudaSuccess) return cuda_fail(e, where);
   return ok();
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
+                     float scale, float* scores, float* lse, void* ws, size_t ws_bytes,
+                     kvc_stream_t stream) {
+  return score_common("kvc_score", kPhaseLse | kPhaseAlpha, cache, segs, q, R, scale, nullptr, lse,
+                      scores, ws, ws_bytes, stream);
+}
+
+kvc_status kvc_score_lse(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
+                         float scale, float* lse, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  return score_common("kvc_score_lse", kPhaseLse, cache, segs, q, R, scale, nullptr, lse, nullptr, ws,
+                      ws_bytes, stream);
+}
+
+kvc_status kvc_score_alpha(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
+                           float scale, const float* lse, float* scores, void* ws, size_t ws_bytes,
+                           kvc_stream_t stream) {
+  const unsigned phases = kPhaseAlpha | (lse != nullptr ? kPhaseLseIn : 0u);
+  return score_common("kvc_score_alpha", phases, cache, segs, q, R, scale, lse, nullptr, scores, ws,
+                      ws_bytes, stream);
+}
+
+uint64_t kvc_launch_count(int32_t reset) {
+  return reset ? g_launches.exchange(0) : g_launches.load();
 }
 
 kvc_status kvc_select_workspace_size(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,

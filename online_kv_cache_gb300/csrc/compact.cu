@@ -249,6 +249,7 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
           m, cl.block_table, cl.keep, cl.moves, cl.move_count, cl.dead, cl.dead_count, cl.status);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
+      count_launch();
     }
     const LaunchMeta& r = cl.rows_meta[c];
     if (r.nseq > 0) {
@@ -256,6 +257,7 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
                                                                  cl.freed, cl.new_rows, cl.status);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
+      count_launch();
     }
   }
   return cudaSuccess;
@@ -279,6 +281,7 @@ cudaError_t launch_compact(const CompactLaunch& cl, cudaStream_t stream) {
           static_cast<uint8_t*>(cl.v_pool), cl.tags);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launch();
   }
   return cudaSuccess;
 }
@@ -292,6 +295,7 @@ cudaError_t launch_free(const CompactLaunch& cl, cudaStream_t stream) {
                                                             cl.capacity, cl.status);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launch();
   }
   return cudaSuccess;
 }

@@ -13,7 +13,18 @@
 
 namespace kvc {
 
+// Counts kernel launches issued by the library (read by kvc_launch_count).
+void count_launch();
+
+enum ScorePhase : unsigned {
+  kPhaseLse = 1,      // pass 1 + combine: per-row LSE -> pass-2 offsets (and lse_out)
+  kPhaseLseIn = 2,    // pass-2 offsets from a caller-supplied LSE
+  kPhaseAlpha = 4,    // pass 2: scores
+};
+
 struct ScoreLaunch {
+  unsigned phases = kPhaseLse | kPhaseAlpha;
+  const float* lse_in = nullptr;       // [B][L][H][R] natural-log LSE (kPhaseLseIn)
   int d = 0;
   int num_sms = 0;
   size_t chunks = 0;

@@ -343,6 +343,25 @@ __global__ void lse_combine_kernel(const __grid_constant__ LaunchMeta meta,
   }
 }
 
+// Pass-2 offsets from a caller-supplied natural-log LSE (for instance the
+// log-sum-exp the attention kernel produced for the same proxy queries).
+__global__ void obias_from_lse_kernel(const __grid_constant__ LaunchMeta meta,
+                                      const float* __restrict__ lse_in, float* __restrict__ obias) {
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < meta.items;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int si = find_seq(meta, g);
+    const SeqMeta& s = meta.seq[si];
+    int64_t local = g - s.item0;
+    const int i = (int)(local % meta.R_pad);
+    local /= meta.R_pad;
+    const int h = (int)(local % meta.H);
+    const int l = (int)(local / meta.H);
+    const int64_t u = ((int64_t)s.b * meta.L + l) * meta.H + h;
+    obias[u * meta.R_pad + i] =
+        (i < meta.R) ? 2.0f * kLog2e * lse_in[u * meta.R + i] - kBias : INFINITY;
+  }
+}
+
 // ============================================================== pass 2
 
 struct P2Item {
@@ -548,25 +567,41 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   for (size_t c = 0; c < sl.chunks; ++c) {
-    const LaunchMeta& m1 = sl.pass1[c];
-    if (m1.items > 0) {
-      const int grid = (int)std::min<int64_t>(m1.items, sl.num_sms);
-      lse_pass_kernel<D><<<grid, kThreads, C::kP1Smem, stream>>>(*sl.tmK, *sl.tmQ1, m1, sl.block_table,
-                                                                 sl.part, sl.status);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (sl.phases & kPhaseLse) {
+      const LaunchMeta& m1 = sl.pass1[c];
+      if (m1.items > 0) {
+        const int grid = (int)std::min<int64_t>(m1.items, sl.num_sms);
+        lse_pass_kernel<D><<<grid, kThreads, C::kP1Smem, stream>>>(*sl.tmK, *sl.tmQ1, m1, sl.block_table,
+                                                                   sl.part, sl.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+      }
+      const LaunchMeta& mc = sl.combine[c];
+      if (mc.items > 0) {
+        const int grid = (int)std::min<int64_t>((mc.items + 255) / 256, (int64_t)sl.num_sms * 8);
+        lse_combine_kernel<<<grid, 256, 0, stream>>>(mc, sl.part, sl.obias, sl.lse_out);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+      }
     }
-    const LaunchMeta& mc = sl.combine[c];
-    if (mc.items > 0) {
-      const int grid = (int)std::min<int64_t>((mc.items + 255) / 256, (int64_t)sl.num_sms * 8);
-      lse_combine_kernel<<<grid, 256, 0, stream>>>(mc, sl.part, sl.obias, sl.lse_out);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (sl.phases & kPhaseLseIn) {
+      const LaunchMeta& mc = sl.combine[c];
+      if (mc.items > 0) {
+        const int grid = (int)std::min<int64_t>((mc.items + 255) / 256, (int64_t)sl.num_sms * 8);
+        obias_from_lse_kernel<<<grid, 256, 0, stream>>>(mc, sl.lse_in, sl.obias);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+      }
     }
-    const LaunchMeta& m2 = sl.pass2[c];
-    if (m2.items > 0) {
-      const int grid = (int)std::min<int64_t>(m2.items, sl.num_sms);
-      alpha_pass_kernel<D><<<grid, kThreads, C::kP2Smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,
-                                                                   sl.obias, sl.scores, sl.status);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (sl.phases & kPhaseAlpha) {
+      const LaunchMeta& m2 = sl.pass2[c];
+      if (m2.items > 0) {
+        const int grid = (int)std::min<int64_t>(m2.items, sl.num_sms);
+        alpha_pass_kernel<D><<<grid, kThreads, C::kP2Smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,
+                                                                     sl.obias, sl.scores, sl.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+      }
     }
   }
   return cudaSuccess;

@@ -155,6 +155,7 @@ cudaError_t launch_select(const SelectLaunch& sl, cudaStream_t stream) {
     select_topm_kernel<<<(unsigned)m.items, kSelThreads, 0, stream>>>(m, sl.scores, sl.keep);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launch();
   }
   return cudaSuccess;
 }
