@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (small profiling cases)")
     return ap.parse_args()
 
 
@@ -281,6 +283,9 @@ def our_arm(args):
     import workloads
 
     sp = workloads.spec(args.workload, args.seed)
+    if args.layers:
+        import dataclasses
+        sp = dataclasses.replace(sp, L=args.layers)
     case = workloads.build(sp, args.seed + rank, dev)
     m = budgets_lib(case)
     cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks,

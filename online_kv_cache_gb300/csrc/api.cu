@@ -79,6 +79,19 @@ kvc_status device_info(DeviceInfo* out) {
   return KVC_OK;
 }
 
+// Like device_info, but without a usable device reports the GB300's 152 SMs (the
+// work split, and so the workspace size, depends on the SM count).
+kvc_status device_info_or_default(DeviceInfo* out) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+    cudaGetLastError();
+    out->num_sms = 152;
+    out->status = nullptr;
+    return KVC_OK;
+  }
+  return device_info(out);
+}
+
 // ------------------------------------------------------------- validation
 
 enum Need : unsigned {
@@ -203,9 +216,11 @@ std::vector<std::pair<size_t, size_t>> chunks_of(const Plan& p) {
 
 struct ScoreGeom {
   int R, R_pad, W, nchunks, rowtiles;
+  int gsub1, ngroups1, qbytes1, kst1;  // pass 1: row tiles per group, groups, smem
+  int gsub2, ngroups2, qbytes2, kst2;  // pass 2: chunks per group, groups, smem
 };
 
-ScoreGeom score_geom(int R) {
+ScoreGeom score_geom(int R, int d) {
   ScoreGeom g;
   g.R = R;
   const int R32 = (int)ceil_div(R, 32) * 32;
@@ -213,21 +228,37 @@ ScoreGeom score_geom(int R) {
   g.W = (int)ceil_div(ceil_div(R, g.nchunks), 32) * 32;
   g.R_pad = g.W * g.nchunks;
   g.rowtiles = (int)ceil_div(R, 128);
+  const int tile_bytes = 128 * d * 2;
+  const int fixed = score_smem_bytes(0, 0, d);
+  g.gsub1 = std::min(4, g.rowtiles);
+  g.ngroups1 = (int)ceil_div(g.rowtiles, g.gsub1);
+  g.qbytes1 = g.gsub1 * 128 * d * 2;
+  g.kst1 = std::min(8, (kScoreSmemLimit - fixed - g.qbytes1) / tile_bytes);
+  g.gsub2 = std::min(g.nchunks, std::max(1, 512 / g.W));
+  g.ngroups2 = (int)ceil_div(g.nchunks, g.gsub2);
+  g.qbytes2 = g.gsub2 * g.W * d * 2;
+  g.kst2 = std::min(8, (kScoreSmemLimit - fixed - g.qbytes2) / tile_bytes);
   return g;
 }
 
-int pass1_split(int n) {
-  const int T = (int)ceil_div(n, 128);
-  return std::max(1, std::min(T, (int)ceil_div(T, 16)));
+// Key tiles per work item: enough items for ~8 per SM, 2..32 tiles each.
+int tiles_per_item(const kvc_cache* c, const Plan& p, int ngroups, int num_sms) {
+  int64_t jobs = 0;
+  for (const Seq& q : p.seqs) jobs += (int64_t)c->num_layers * c->num_kv_heads * ngroups * ceil_div(q.n, 128);
+  const int64_t t = jobs / std::max<int64_t>(1, 8 * (int64_t)num_sms);
+  return (int)std::max<int64_t>(2, std::min<int64_t>(32, t));
 }
 
 struct ScorePlan {
   std::vector<LaunchMeta> p1, comb, p2;
-  size_t part_bytes = 0, obias_bytes = 0;
+  size_t part_bytes = 0, obias_bytes = 0, part2_bytes = 0;
 };
 
-void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, float scale, ScorePlan* sp) {
+void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, float scale, int num_sms,
+                      ScorePlan* sp) {
   const int64_t LH = (int64_t)c->num_layers * c->num_kv_heads;
+  const int tpi1 = tiles_per_item(c, p, g.ngroups1, num_sms);
+  const int tpi2 = tiles_per_item(c, p, g.ngroups2, num_sms);
   int64_t max_p1 = 0;
   for (auto [lo, hi] : chunks_of(p)) {
     LaunchMeta a = base_meta(c, p), k = base_meta(c, p), z = base_meta(c, p);
@@ -240,20 +271,31 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
       lm->rowtiles = g.rowtiles;
       lm->scale = scale;
     }
+    a.ngroups = g.ngroups1;
+    a.gsub = g.gsub1;
+    a.qbytes = g.qbytes1;
+    a.kst = g.kst1;
+    z.ngroups = g.ngroups2;
+    z.gsub = g.gsub2;
+    z.qbytes = g.qbytes2;
+    z.kst = g.kst2;
     int64_t i1 = 0, ic = 0, i2 = 0;
     for (size_t i = lo; i < hi; ++i) {
       const size_t j = i - lo;
       for (LaunchMeta* lm : {&a, &k, &z}) fill_seq(&lm->seq[j], p, i);
-      const int split = pass1_split(p.seqs[i].n);
       const int T = (int)ceil_div(p.seqs[i].n, 128);
-      a.seq[j].split = k.seq[j].split = z.seq[j].split = split;
+      const int split1 = (int)std::min<int64_t>(T, ceil_div(T, tpi1));
+      const int split2 = (int)std::min<int64_t>(T, ceil_div(T, tpi2));
+      a.seq[j].split = split1;
+      k.seq[j].split = split1;
+      z.seq[j].split = split2;
       a.seq[j].item0 = i1;
       k.seq[j].item0 = ic;
       k.seq[j].item1 = i1;
       z.seq[j].item0 = i2;
-      i1 += LH * split * g.rowtiles;
+      i1 += LH * g.ngroups1 * split1;
       ic += LH * g.R_pad;
-      i2 += LH * T;
+      i2 += LH * g.ngroups2 * split2;
     }
     a.items = i1;
     k.items = ic;
@@ -263,8 +305,9 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
     sp->comb.push_back(k);
     sp->p2.push_back(z);
   }
-  sp->part_bytes = (size_t)max_p1 * 128 * sizeof(float2);
+  sp->part_bytes = (size_t)max_p1 * 2 * 4 * 128 * sizeof(float2);
   sp->obias_bytes = (size_t)c->batch * LH * g.R_pad * sizeof(float);
+  sp->part2_bytes = g.ngroups2 > 1 ? (size_t)g.ngroups2 * LH * p.Ntot * sizeof(float) : 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -351,9 +394,11 @@ kvc_status kvc_score_workspace_size(const kvc_cache* cache, const kvc_segments* 
   if (R < 1 || R > 4096) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..4096)", R);
   Plan p;
   if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
+  DeviceInfo di;
+  if ((st = device_info_or_default(&di)) != KVC_OK) return st;
   ScorePlan sp;
-  build_score_plan(cache, p, score_geom(R), 1.0f, &sp);
-  *bytes = align256(sp.part_bytes) + align256(sp.obias_bytes);
+  build_score_plan(cache, p, score_geom(R, cache->head_dim), 1.0f, di.num_sms, &sp);
+  *bytes = align256(sp.part_bytes) + align256(sp.obias_bytes) + align256(sp.part2_bytes);
   return ok();
 }
 
@@ -377,13 +422,14 @@ kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cac
   if (q == nullptr || !aligned16(q)) return fail(KVC_ERR_INVALID_ARG, "q is NULL or not 16-byte aligned");
   if ((phases & kPhaseAlpha) && scores == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores is NULL");
   if ((phases & kPhaseLseIn) && lse_in == nullptr) return fail(KVC_ERR_INVALID_ARG, "lse is NULL");
-  const ScoreGeom g = score_geom(R);
+  DeviceInfo di;
+  if ((st = device_info_or_default(&di)) != KVC_OK) return st;
+  const ScoreGeom g = score_geom(R, cache->head_dim);
   ScorePlan sp;
-  build_score_plan(cache, p, g, scale, &sp);
-  const size_t need = align256(sp.part_bytes) + align256(sp.obias_bytes);
+  build_score_plan(cache, p, g, scale, di.num_sms, &sp);
+  const size_t need = align256(sp.part_bytes) + align256(sp.obias_bytes) + align256(sp.part2_bytes);
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
-  DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
 
   const int64_t krows = (int64_t)cache->num_layers * cache->num_pages * cache->num_kv_heads * cache->page_size;
@@ -409,6 +455,8 @@ kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cac
   sl.block_table = cache->block_table;
   sl.part = static_cast<float2*>(ws);
   sl.obias = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes));
+  sl.part2 = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes) +
+                                      align256(sp.obias_bytes));
   sl.lse_out = lse_out;
   sl.scores = scores;
   sl.status = di.status;

@@ -39,7 +39,10 @@ struct LaunchMeta {
   int32_t rowtiles; // ceil(R / 128) (score pass 1)
   int32_t W;        // Q rows per pass-2 chunk (multiple of 32, <= 256)
   int32_t nchunks;  // R_pad / W
-  int32_t pad;
+  int32_t ngroups;  // row groups of a scoring pass (each resident in shared memory)
+  int32_t gsub;     // jobs per K tile of a full group (row tiles or chunks)
+  int32_t kst;      // K-tile ring stages of a scoring pass
+  int32_t qbytes;   // shared-memory bytes of one resident row group
   float scale;      // logit scale
   float pad2;
   int64_t Ntot, Mtot, Ftot;

@@ -22,6 +22,13 @@ enum ScorePhase : unsigned {
   kPhaseAlpha = 4,    // pass 2: scores
 };
 
+// Dynamic shared memory of a scoring pass: 1024 B alignment slack, the resident
+// row group of Q, `kst` K tiles of 128 keys, and the barrier block.
+constexpr int kScoreSmemLimit = 232448;  // 227 KB per block on sm_103a
+__host__ __device__ constexpr int score_smem_bytes(int qbytes, int kst, int d) {
+  return 1024 + qbytes + kst * 128 * d * 2 + 256;
+}
+
 struct ScoreLaunch {
   unsigned phases = kPhaseLse | kPhaseAlpha;
   const float* lse_in = nullptr;       // [B][L][H][R] natural-log LSE (kPhaseLseIn)
@@ -36,6 +43,7 @@ struct ScoreLaunch {
   const CUtensorMap* tmQ2 = nullptr;   // Q, box {64, W}
   const int32_t* block_table = nullptr;
   float2* part = nullptr;              // pass-1 partials (workspace)
+  float* part2 = nullptr;              // pass-2 per-row-group partial sums (workspace)
   float* obias = nullptr;              // per-row pass-2 offsets (workspace)
   float* lse_out = nullptr;
   float* scores = nullptr;
