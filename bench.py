@@ -363,7 +363,8 @@ def our_arm(args):
     # dominant kernel: the longer scoring pass (each is one persistent kernel; the LSE stage also
     # runs a small combine kernel)
     dom = max(("score_lse", "score_alpha"), key=lambda s: per_stage[s])
-    dom_kernel = "alpha_pass_kernel" if dom == "score_alpha" else "lse_pass_kernel"
+    dom_kernel = ("score_pass_kernel<128,2> (alpha pass)" if dom == "score_alpha"
+                  else "score_pass_kernel<128,1> (LSE pass)")
     t_dom = per_stage[dom] * 1e-3
     achieved = F_alg / t_dom / 1e12
     roofline = {"bound": "tensor", "kernel": dom_kernel, "achieved": achieved,

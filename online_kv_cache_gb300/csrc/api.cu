@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -90,6 +91,18 @@ kvc_status device_info_or_default(DeviceInfo* out) {
     return KVC_OK;
   }
   return device_info(out);
+}
+
+// Persistent-grid size of the scoring passes: one CTA per SM, or fewer when
+// the KVC_GRID_LIMIT environment variable asks for it (a test knob that makes
+// every CTA walk many work items).
+int grid_limit(int num_sms) {
+  const char* e = std::getenv("KVC_GRID_LIMIT");
+  if (e != nullptr) {
+    const int v = std::atoi(e);
+    if (v > 0) return std::min(v, num_sms);
+  }
+  return num_sms;
 }
 
 // ------------------------------------------------------------- validation
@@ -241,12 +254,29 @@ ScoreGeom score_geom(int R, int d) {
   return g;
 }
 
-// Key tiles per work item: enough items for ~8 per SM, 2..32 tiles each.
+// Key tiles per work item.  Items are dealt round-robin to one persistent CTA
+// per SM, so the pass ends when the busiest CTA does: choose the item size that
+// minimises (items per CTA, rounded up) x (tiles per item) + a per-item cost.
 int tiles_per_item(const kvc_cache* c, const Plan& p, int ngroups, int num_sms) {
-  int64_t jobs = 0;
-  for (const Seq& q : p.seqs) jobs += (int64_t)c->num_layers * c->num_kv_heads * ngroups * ceil_div(q.n, 128);
-  const int64_t t = jobs / std::max<int64_t>(1, 8 * (int64_t)num_sms);
-  return (int)std::max<int64_t>(2, std::min<int64_t>(32, t));
+  const int64_t LHg = (int64_t)c->num_layers * c->num_kv_heads * ngroups;
+  double best = 1e300;
+  int best_tpi = 2;
+  for (int tpi = 2; tpi <= 48; ++tpi) {
+    int64_t items = 0, max_tiles = 0;
+    for (const Seq& q : p.seqs) {
+      const int64_t T = ceil_div(q.n, 128);
+      const int64_t split = std::min<int64_t>(T, ceil_div(T, tpi));
+      items += LHg * split;
+      max_tiles = std::max<int64_t>(max_tiles, ceil_div(T, split));
+    }
+    const double per_cta = (double)ceil_div(items, num_sms);
+    const double cost = per_cta * ((double)max_tiles + 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_tpi = tpi;
+    }
+  }
+  return best_tpi;
 }
 
 struct ScorePlan {
@@ -445,6 +475,7 @@ kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cac
   sl.lse_in = lse_in;
   sl.d = cache->head_dim;
   sl.num_sms = di.num_sms;
+  sl.grid_limit = grid_limit(di.num_sms);
   sl.chunks = sp.p1.size();
   sl.pass1 = sp.p1.data();
   sl.combine = sp.comb.data();

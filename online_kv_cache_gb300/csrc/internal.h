@@ -22,11 +22,12 @@ enum ScorePhase : unsigned {
   kPhaseAlpha = 4,    // pass 2: scores
 };
 
-// Dynamic shared memory of a scoring pass: 1024 B alignment slack, the resident
-// row group of Q, `kst` K tiles of 128 keys, and the barrier block.
+// Dynamic shared memory of a scoring pass: the barrier block, up to 1024 B of
+// alignment padding, the resident row group of Q and `kst` K tiles of 128 keys.
 constexpr int kScoreSmemLimit = 232448;  // 227 KB per block on sm_103a
+constexpr int kScoreSmemHead = 1536;     // barriers, TMEM address, reduction buffer
 __host__ __device__ constexpr int score_smem_bytes(int qbytes, int kst, int d) {
-  return 1024 + qbytes + kst * 128 * d * 2 + 256;
+  return kScoreSmemHead + 1024 + qbytes + kst * 128 * d * 2;
 }
 
 struct ScoreLaunch {
@@ -34,6 +35,7 @@ struct ScoreLaunch {
   const float* lse_in = nullptr;       // [B][L][H][R] natural-log LSE (kPhaseLseIn)
   int d = 0;
   int num_sms = 0;
+  int grid_limit = 0;                  // persistent CTAs per pass (<= num_sms)
   size_t chunks = 0;
   const LaunchMeta* pass1 = nullptr;   // [chunks]
   const LaunchMeta* combine = nullptr; // [chunks]

@@ -114,10 +114,13 @@ __device__ __forceinline__ int32_t page_row(const LaunchMeta& meta, const int32_
 
 // ============================================================== skeleton
 
-// PASS 1: A = Q row tile (M = 128 rows), B = K tile (N = 128 keys); TMEM: two
-//         slots of 128 columns per warpgroup.
-// PASS 2: A = K tile (M = 128 keys), B = Q chunk (N = W rows); TMEM: one slot of
-//         256 columns per warpgroup.
+// PASS 1: A = Q row tile (M = 128 rows), B = K tile (N = 128 keys).
+// PASS 2: A = K tile (M = 128 keys), B = Q chunk (N = W rows).
+// Jobs run tile by tile: for each K tile, one job per row tile / chunk of the
+// group; job number jc (counted over the CTA's whole run) goes to warpgroup
+// jc & 1, which uses its own TMEM slots (two of 128 columns in pass 1, one of
+// 256 in pass 2).  Only one K tile is in use at a time, so a ring of kst tiles
+// keeps kst - 1 tiles in flight.
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     score_pass_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -127,27 +130,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   constexpr int NBW = (PASS == 1) ? 2 : 1;        // TMEM slots per warpgroup
   constexpr int SLOT_COLS = (PASS == 1) ? 128 : 256;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // [barriers, TMEM address, abort flag, reduction buffer][pad to 1024][Q group][K ring]
   const int kst = meta.kst;
-  uint8_t* sQ = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  uint8_t* sQ = align1024(smem_raw + kScoreSmemHead);
   uint8_t* sK = sQ + meta.qbytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sK + kst * C::kTileBytes);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
+  uint64_t* q_full = bars;               // [4] one per row tile / chunk of the group
+  uint64_t* q_empty = bars + 4;          // [4]
+  uint64_t* k_full = bars + 8;           // [kMaxKStages]
   uint64_t* k_empty = k_full + kMaxKStages;
-  uint64_t* t_full = k_empty + kMaxKStages;
+  uint64_t* t_full = k_empty + kMaxKStages;  // [4] TMEM slots
   uint64_t* t_empty = t_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parity][128] (pass 2)
 
   const int total_sub = (PASS == 1) ? meta.rowtiles : meta.nchunks;
   const int sub_rows = (PASS == 1) ? kTile : meta.W;  // Q rows per job
+  const uint32_t sub_bytes = (uint32_t)(C::KB * sub_rows * 128);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int i = 0; i < 4; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     for (int i = 0; i < kMaxKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < 4; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 128); }
     *abort_flag = 0;
@@ -166,126 +170,129 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer (whole warp)
-    uint32_t qit = 0, kit = 0;
+    // Load order per item: its first min(kst-1, tiles) K tiles, then its Q group
+    // (sub-tile by sub-tile as the previous item releases them), then the rest.
+    uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0};
     bool ok = true;
-    int64_t item = blockIdx.x;
-    if (item < meta.items) {
-      Item it = decode_item(meta, item, total_sub);
-      int t = it.t0;
-      int32_t prow = page_row(meta, block_table, it.u, t, lane, status);
-      const int ppt = kTile / meta.P;
-      while (ok) {
-        if (t == it.t0) {  // new item: its row group of Q
-          if (lane == 0) ok = mbar_wait(q_empty, (qit & 1) ^ 1, abort_flag, status);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+    int64_t k_item = blockIdx.x, q_item = blockIdx.x;
+    Item kit_ = k_item < meta.items ? decode_item(meta, k_item, total_sub) : Item{};
+    int kt = kit_.t0;
+    int32_t prow = k_item < meta.items ? page_row(meta, block_table, kit_.u, kt, lane, status) : -1;
+    const int ppt = kTile / meta.P;
+    while (ok && (k_item < meta.items || q_item < meta.items)) {
+      const int pre = min(kst - 1, kit_.t1 - kit_.t0);
+      // Q of item q_item goes after that item's first `pre` K tiles (or at once
+      // when the K cursor has already passed them)
+      const bool do_q = q_item < meta.items &&
+                        (q_item < k_item || k_item >= meta.items ||
+                         (q_item == k_item && kt >= kit_.t0 + pre));
+      if (do_q) {
+        const Item qi = decode_item(meta, q_item, total_sub);
+        const int qrow = ((qi.u.b * meta.L + qi.u.l) * meta.H + qi.u.h) * meta.R +
+                         qi.u.g * meta.gsub * sub_rows;
+        for (int j = 0; j < qi.J && ok; ++j) {
           if (lane == 0) {
-            const int qrow = ((it.u.b * meta.L + it.u.l) * meta.H + it.u.h) * meta.R +
-                             it.u.g * meta.gsub * sub_rows;
-            mbar_arrive_expect_tx(q_full, (uint32_t)(it.J * C::KB * sub_rows * 128));
-            for (int j = 0; j < it.J; ++j)
+            ok = mbar_wait(&q_empty[j], (q_use[j] & 1) ^ 1, abort_flag, status);
+            if (ok) {
+              mbar_arrive_expect_tx(&q_full[j], sub_bytes);
 #pragma unroll
               for (int kb = 0; kb < C::KB; ++kb)
-                tma_load_2d(sQ + (j * C::KB + kb) * sub_rows * 128, &tmQ, q_full, kb * 64,
+                tma_load_2d(sQ + (j * C::KB + kb) * sub_rows * 128, &tmQ, &q_full[j], kb * 64,
                             qrow + j * sub_rows);
+            }
           }
-          ++qit;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++q_use[j];
         }
-        // the next tile to load, and its page rows (consumed next iteration)
-        Item nit = it;
-        int nt = t + 1;
-        int64_t nitem = item;
-        bool more = true;
-        if (nt >= it.t1) {
-          nitem = item + gridDim.x;
-          more = nitem < meta.items;
-          if (more) {
-            nit = decode_item(meta, nitem, total_sub);
-            nt = nit.t0;
-          }
-        }
-        const int32_t prow_next = more ? page_row(meta, block_table, nit.u, nt, lane, status) : -1;
-        // tile t into the ring
-        const int ks = kit % kst;
-        if (lane == 0) ok = mbar_wait(&k_empty[ks], ((kit / kst) & 1) ^ 1, abort_flag, status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        const unsigned valid = __ballot_sync(0xffffffffu, prow >= 0);
-        if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], __popc(valid) * C::KB * meta.P * 128);
-        uint8_t* dst = sK + ks * C::kTileBytes;
-        for (int p = 0; p < ppt; ++p) {
-          const int32_t row = __shfl_sync(0xffffffffu, prow, p);
-          if (lane == 0 && row >= 0) {
-#pragma unroll
-            for (int kb = 0; kb < C::KB; ++kb)
-              tma_load_2d(dst + kb * C::kKbBytes + p * meta.P * 128, &tmK, &k_full[ks], kb * 64, row);
-          }
-        }
-        ++kit;
-        if (!more) break;
-        item = nitem;
-        it = nit;
-        t = nt;
-        prow = prow_next;
+        q_item += gridDim.x;
+        continue;
       }
+      // the K tile after this one, and its page rows (consumed next iteration)
+      Item nit = kit_;
+      int nt = kt + 1;
+      int64_t nitem = k_item;
+      if (nt >= kit_.t1) {
+        nitem = k_item + gridDim.x;
+        if (nitem < meta.items) {
+          nit = decode_item(meta, nitem, total_sub);
+          nt = nit.t0;
+        }
+      }
+      const int32_t prow_next = nitem < meta.items ? page_row(meta, block_table, nit.u, nt, lane, status) : -1;
+      const int ks = kcount % kst;
+      if (lane == 0) ok = mbar_wait(&k_empty[ks], ((kcount / kst) & 1) ^ 1, abort_flag, status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const unsigned valid = __ballot_sync(0xffffffffu, prow >= 0);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], __popc(valid) * C::KB * meta.P * 128);
+      uint8_t* dst = sK + ks * C::kTileBytes;
+      for (int p = 0; p < ppt; ++p) {
+        const int32_t row = __shfl_sync(0xffffffffu, prow, p);
+        if (lane == 0 && row >= 0) {
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(dst + kb * C::kKbBytes + p * meta.P * 128, &tmK, &k_full[ks], kb * 64, row);
+        }
+      }
+      ++kcount;
+      k_item = nitem;
+      kit_ = nit;
+      kt = nt;
+      prow = prow_next;
     }
     if (!ok && lane == 0) {  // let issued copies land before the CTA exits
-      for (uint32_t j = (kit > (uint32_t)kst ? kit - kst : 0); j < kit; ++j)
+      for (uint32_t j = (kcount > (uint32_t)kst ? kcount - kst : 0); j < kcount; ++j)
         mbar_wait(&k_full[j % kst], (j / kst) & 1, nullptr, status);
-      if (qit > 0) mbar_wait(q_full, (qit - 1) & 1, nullptr, status);
+      for (int j = 0; j < 4; ++j)
+        if (q_use[j] > 0) mbar_wait(&q_full[j], (q_use[j] - 1) & 1, nullptr, status);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = (PASS == 1) ? idesc_bf16_f32(kTile, kTile) : idesc_bf16_f32(kTile, meta.W);
-      uint32_t qit = 0, kit = 0, cnt[2] = {0, 0}, last_slot = 0, last_use = 0;
+      uint32_t kcount = 0, jc = 0, cnt[2] = {0, 0}, q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
       bool issued = false, ok = true;
+      const uint32_t q_base = smem_u32(sQ);
       for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
         const Item it = decode_item(meta, item, total_sub);
-        if (!(ok = mbar_wait(q_full, qit & 1, abort_flag, status))) break;
-        const uint32_t q_base = smem_u32(sQ);
-        for (int p = it.t0; p < it.t1 && ok; p += 2) {
-          const int npair = min(2, it.t1 - p);
-          uint32_t k_base[2] = {0u, 0u};
-          for (int w = 0; w < npair; ++w) {
-            const uint32_t ki = kit + w;
-            if (!(ok = mbar_wait(&k_full[ki % kst], (ki / kst) & 1, abort_flag, status))) break;
-            k_base[w] = smem_u32(sK + (ki % kst) * C::kTileBytes);
-          }
-          if (!ok) break;
-          for (int j = 0; j < it.J && ok; ++j) {
-            const uint32_t sub_base = q_base + j * C::KB * sub_rows * 128;
-            for (int w = 0; w < npair; ++w) {
-              const uint32_t slot = w * NBW + (cnt[w] % NBW);
-              const uint32_t use = cnt[w] / NBW;
-              if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status))) break;
-              tc_fence_after_sync();
-              const uint32_t d_tmem = tmem + slot * SLOT_COLS;
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k) {
-                const uint32_t koff_k = (k >> 2) * C::kKbBytes + (k & 3) * 32;
-                const uint32_t koff_q = (k >> 2) * (uint32_t)(sub_rows * 128) + (k & 3) * 32;
-                if (PASS == 1)
-                  mma_bf16(d_tmem, sdesc_k_sw128(sub_base + koff_q), sdesc_k_sw128(k_base[w] + koff_k),
-                           idesc, k > 0);
-                else
-                  mma_bf16(d_tmem, sdesc_k_sw128(k_base[w] + koff_k), sdesc_k_sw128(sub_base + koff_q),
-                           idesc, k > 0);
-              }
-              mma_commit(&t_full[slot]);
-              issued = true;
-              last_slot = slot;
-              last_use = use;
-              ++cnt[w];
-            }
-          }
-          if (!ok) break;
-          for (int w = 0; w < npair; ++w) mma_commit(&k_empty[(kit + w) % kst]);
-          kit += npair;
-        }
+        for (int j = 0; j < it.J && ok; ++j) ok = mbar_wait(&q_full[j], q_use[j] & 1, abort_flag, status);
         if (!ok) break;
-        mma_commit(q_empty);
-        ++qit;
+        for (int t = it.t0; t < it.t1 && ok; ++t) {
+          const int ks = kcount % kst;
+          if (!(ok = mbar_wait(&k_full[ks], (kcount / kst) & 1, abort_flag, status))) break;
+          const uint32_t k_base = smem_u32(sK + ks * C::kTileBytes);
+          for (int j = 0; j < it.J; ++j) {
+            const uint32_t w = jc & 1;
+            const uint32_t slot = w * NBW + (cnt[w] % NBW);
+            const uint32_t use = cnt[w] / NBW;
+            if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status))) break;
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem + slot * SLOT_COLS;
+            const uint32_t sub_base = q_base + j * sub_bytes;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t koff_k = (k >> 2) * C::kKbBytes + (k & 3) * 32;
+              const uint32_t koff_q = (k >> 2) * (uint32_t)(sub_rows * 128) + (k & 3) * 32;
+              if (PASS == 1)
+                mma_bf16(d_tmem, sdesc_k_sw128(sub_base + koff_q), sdesc_k_sw128(k_base + koff_k), idesc,
+                         k > 0);
+              else
+                mma_bf16(d_tmem, sdesc_k_sw128(k_base + koff_k), sdesc_k_sw128(sub_base + koff_q), idesc,
+                         k > 0);
+            }
+            mma_commit(&t_full[slot]);
+            if (t == it.t1 - 1) mma_commit(&q_empty[j]);  // last use of this Q sub-tile
+            issued = true;
+            last_slot = slot;
+            last_use = use;
+            ++cnt[w];
+            ++jc;
+          }
+          if (!ok) break;
+          mma_commit(&k_empty[ks]);
+          ++kcount;
+        }
+        for (int j = 0; j < it.J; ++j) ++q_use[j];
       }
       if (!ok && issued)  // the last commit covers every MMA issued
         mbar_wait(&t_full[last_slot], last_use & 1, nullptr, status);
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = sub * 32 + lane;  // TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(sub * 32) << 16);
     const float c = meta.scale * kLog2e;
-    uint32_t cnt = 0;
+    uint32_t cnt = 0, jc = 0, tiles_done = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
       const Item it = decode_item(meta, item, total_sub);
@@ -308,11 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_run[j] = 0.0f;
       }
       const int64_t u = ((int64_t)it.u.b * meta.L + it.u.l) * meta.H + it.u.h;
-      for (int p = it.t0 + wg; p < it.t1 && ok; p += 2) {
-        const int valid = min(kTile, it.u.n - p * kTile);
+      for (int t = it.t0; t < it.t1 && ok; ++t, ++tiles_done) {
+        const int valid = min(kTile, it.u.n - t * kTile);
         float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        bool mine = false;
 #pragma unroll 1
-        for (int j = 0; j < it.J; ++j) {
+        for (int j = 0; j < it.J; ++j, ++jc) {
+          if ((int)(jc & 1) != wg) continue;
+          mine = true;
           const uint32_t slot = wg * NBW + (cnt % NBW);
           const uint32_t use = cnt / NBW;
           ok = mbar_wait(&t_full[slot], use & 1, abort_flag, status);
@@ -407,10 +417,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (PASS == 2) {
-          const int key = p * kTile + r;
-          if (key < it.u.n) {
-            const float2 s2 = __fadd2_rn(acc2[0], acc2[1]);
-            const float acc = s2.x + s2.y;
+          const float2 s2 = __fadd2_rn(acc2[0], acc2[1]);
+          float acc = s2.x + s2.y;
+          bool writer = mine;
+          if (it.J > 1) {  // both warpgroups hold a share of this tile's rows
+            float* rb = red + (tiles_done & 1) * kTile;
+            writer = (wg == (int)(tiles_done & 1));
+            if (!writer) rb[r] = acc;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (writer) acc += rb[r];
+          }
+          const int key = t * kTile + r;
+          if (writer && key < it.u.n) {
             const int64_t o = ((int64_t)it.u.l * meta.H + it.u.h) * meta.Ntot + it.u.off + key;
             if (meta.ngroups == 1)
               out2[o] = sqrtf(acc / (float)meta.R) * exp2f(-0.5f * kBias);
@@ -531,7 +549,7 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
     const LaunchMeta& m1 = sl.pass1[c];
     if (sl.phases & kPhaseLse) {
       if (m1.items > 0) {
-        const int grid = (int)std::min<int64_t>(m1.items, sl.num_sms);
+        const int grid = (int)std::min<int64_t>(m1.items, sl.grid_limit);
         const int smem = score_smem_bytes(m1.qbytes, m1.kst, D);
         score_pass_kernel<D, 1><<<grid, kThreads, smem, stream>>>(*sl.tmK, *sl.tmQ1, m1, sl.block_table,
                                                                   sl.part, nullptr, nullptr, sl.status);
@@ -559,7 +577,7 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
     if (sl.phases & kPhaseAlpha) {
       const LaunchMeta& m2 = sl.pass2[c];
       if (m2.items > 0) {
-        const int grid = (int)std::min<int64_t>(m2.items, sl.num_sms);
+        const int grid = (int)std::min<int64_t>(m2.items, sl.grid_limit);
         const int smem = score_smem_bytes(m2.qbytes, m2.kst, D);
         float* out = (m2.ngroups == 1) ? sl.scores : sl.part2;
         score_pass_kernel<D, 2><<<grid, kThreads, smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,

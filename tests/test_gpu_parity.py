@@ -115,6 +115,19 @@ def test_micro_shapes(d, P, G, q, lengths, budget):
     full_check(case, f"micro d={d} P={P} R={sp.R} n={lengths}")
 
 
+@pytest.mark.parametrize("grid", ["3", "1"])
+@pytest.mark.parametrize("shape", [(128, 16, 8, 64, (2048, 1500, 700)), (64, 32, 4, 8, (3000, 130)),
+                                   (128, 16, 16, 128, (900,))])
+def test_many_items_per_cta(monkeypatch, grid, shape):
+    """A persistent grid of 1 or 3 CTAs walks every work item: rings and Q sub-tile barriers wrap
+    many times, items of different lengths and row groups follow each other."""
+    d, P, G, q, lengths = shape
+    monkeypatch.setenv("KVC_GRID_LIMIT", grid)
+    sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, shuffle_pages=True)
+    case = workloads.build(sp, 7, DEV)
+    full_check(case, f"grid={grid} d={d} R={sp.R} n={lengths}")
+
+
 @pytest.mark.parametrize("mode", ["zero", "one", "n-1", "all"])
 def test_edge_budgets(mode):
     sp = workloads.custom(L=1, H=2, G=4, d=128, P=16, q=8, lengths=(100, 47, 16), shuffle_pages=True)
