@@ -52,6 +52,9 @@ kvc_status ok() {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The planner keeps a bitmap of the target region in shared memory (<= 192 KB).
+constexpr int kMaxTargetSlots = 192 * 1024 * 8;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DeviceInfo {
@@ -200,6 +203,9 @@ LaunchMeta base_meta(const kvc_cache* c, const Plan& p) {
   lm.Ntot = p.Ntot;
   lm.Mtot = p.Mtot;
   lm.Ftot = p.Ftot;
+  int lp = 0;
+  while ((1 << lp) < c->page_size) ++lp;
+  lm.log2P = lp;
   return lm;
 }
 
@@ -636,13 +642,14 @@ void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta
       for (LaunchMeta* lm : {&a, &r, &c, &f}) fill_seq(&lm->seq[j], p, i);
       const Seq& q = p.seqs[i];
       a.seq[j].item0 = ia;
-      ia += LH * std::max<int64_t>(1, ceil_div((int64_t)q.X * P, 256));
-      c.seq[j].item0 = ic;  // chunk-local prefix of m
-      ic += q.m;
+      ia += LH;  // one planning CTA per unit
+      a.words = std::max<int32_t>(a.words, (int32_t)ceil_div((int64_t)q.X * P, 32));
+      c.seq[j].item0 = ic;  // copy blocks: one per (unit, 128 moves)
+      ic += LH * std::max<int64_t>(1, ceil_div(q.m, 128));
       fc += q.nb - q.X;
     }
     a.items = ia;
-    c.items = LH * ic;
+    c.items = ic;
     f.Ftot = fc;
     plan_m->push_back(a);
     rows_m->push_back(r);
@@ -660,6 +667,10 @@ kvc_status kvc_plan_compact(const kvc_cache* cache, const kvc_segments* segs, co
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
   Plan p;
   if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  for (const Seq& q : p.seqs)
+    if ((int64_t)q.X * cache->page_size > kMaxTargetSlots)
+      return fail(KVC_ERR_UNSUPPORTED, "target region of %lld slots exceeds %d (budget too large)",
+                  (long long)q.X * cache->page_size, kMaxTargetSlots);
   if ((st = check_plan(cache, p, plan)) != KVC_OK) return st;
   if (p.seqs.empty()) return ok();
   if (p.Mtot > 0 && keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");

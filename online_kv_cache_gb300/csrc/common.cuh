@@ -43,6 +43,8 @@ struct LaunchMeta {
   int32_t gsub;     // jobs per K tile of a full group (row tiles or chunks)
   int32_t kst;      // K-tile ring stages of a scoring pass
   int32_t qbytes;   // shared-memory bytes of one resident row group
+  int32_t log2P;    // log2(P)
+  int32_t words;    // plan: 32-bit bitmap words covering the largest target region
   float scale;      // logit scale
   float pad2;
   int64_t Ntot, Mtot, Ftot;

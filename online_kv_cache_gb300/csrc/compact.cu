@@ -26,7 +26,8 @@ namespace kvc {
 
 namespace {
 
-constexpr int kPlanThreads = 256;
+constexpr int kPlanThreads = 512;
+constexpr int kMovesPerBlock = 128;
 
 __device__ __forceinline__ int32_t phys_slot(const int32_t* bt_row, int slot, int P, int num_pages,
                                              unsigned* status) {
@@ -38,68 +39,140 @@ __device__ __forceinline__ int32_t phys_slot(const int32_t* bt_row, int slot, in
   return page * P + slot % P;
 }
 
+// Block-wide exclusive prefix sum of one value per thread (kPlanThreads threads);
+// returns the exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < kPlanThreads / 32 ? warp_sums[lane] : 0u;
+    uint32_t y = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += t;
+    }
+    if (lane < kPlanThreads / 32) warp_sums[lane] = y - w;
+    if (lane == 31) *total = y;
+  }
+  __syncthreads();
+  const uint32_t r = warp_sums[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+// One CTA per unit (sequence, layer, head).  Inside survivors keep[c_out..m)
+// are marked in a shared-memory bitmap of the target region T; a block scan over
+// the bitmap words numbers the holes of T in ascending slot order; hole k takes
+// the k-th outside survivor (k < c_out) or is dead.
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
                 const int32_t* __restrict__ keep, int32_t* __restrict__ moves,
                 int32_t* __restrict__ move_count, int32_t* __restrict__ dead,
                 int32_t* __restrict__ dead_count, unsigned* status) {
-  __shared__ int sh_cout;
+  extern __shared__ uint32_t bitmap[];  // meta.words words
+  __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t sh_total;
   const int64_t item = blockIdx.x;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
   const int P = meta.P;
-  const int per = max(1, (s.X * P + kPlanThreads - 1) / kPlanThreads);
-  int64_t local = item - s.item0;
-  const int chunk = (int)(local % per);
-  local /= per;
+  const int64_t local = item - s.item0;
   const int h = (int)(local % meta.H);
   const int l = (int)(local / meta.H);
   const int64_t lh = (int64_t)l * meta.H + h;
   const int64_t u = lh * meta.B + s.b;
   const int32_t* ku = keep + lh * meta.Mtot + s.moff;
   const int m = s.m;
+  const int XP = s.X * P;
   const int Bs = (s.nb - s.X) * P;
-  if (threadIdx.x == 0) {
-    int lo = 0, hi = m;  // first index with keep >= Bs
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(ku + mid) < Bs) lo = mid + 1; else hi = mid;
+  const int tid = threadIdx.x;
+
+  // c_out = #{keep < Bs}.  keep is ascending, so probes below Bs form a prefix:
+  // each round narrows [lo, hi] (which holds the answer) by a factor of the
+  // block size; every thread takes the same branches.
+  int lo = 0, hi = m;
+  while (lo < hi) {
+    const int step = (hi - lo + kPlanThreads - 1) / kPlanThreads;
+    const int i = lo + tid * step;
+    const int below = __syncthreads_count((i < hi) && (__ldg(ku + i) < Bs));
+    if (below == 0) {
+      hi = lo;
+    } else {
+      const int last = lo + (below - 1) * step;  // last probe below Bs
+      hi = min(hi, last + step);
+      lo = last + 1;
     }
-    sh_cout = lo;
-    if (chunk == 0) {
-      move_count[u] = lo;
-      dead_count[u] = s.X * P - m;
+  }
+  const int c_out = lo;
+  if (tid == 0) {
+    move_count[u] = c_out;
+    dead_count[u] = XP - m;
+  }
+  if (XP == 0) return;
+
+  // bitmap of inside survivors
+  const int words = (XP + 31) >> 5;
+  for (int w = tid; w < words; w += kPlanThreads) bitmap[w] = 0u;
+  __syncthreads();
+  for (int i = c_out + tid; i < m; i += kPlanThreads) {
+    const int32_t pos = __ldg(ku + i);
+    const int rel = pos - Bs;
+    if (rel < 0 || rel >= XP || pos >= s.n) {
+      atomicOr(status, KVC_DEV_BAD_KEEP);
+      continue;
     }
+    atomicOr(&bitmap[rel >> 5], 1u << (rel & 31));
   }
   __syncthreads();
-  const int c_out = sh_cout;
-  const int k = chunk * kPlanThreads + threadIdx.x;
-  if (k >= c_out + (s.X * P - m)) return;
-  // number of retained entries of T that precede hole k
-  int lo = c_out, hi = m;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(ku + mid) - Bs - (mid - c_out) <= k) lo = mid + 1; else hi = mid;
-  }
-  const int t = Bs + k + (lo - c_out);
+
+  // number the holes and emit moves / dead slots
   const int32_t* bt_row = block_table + (int64_t)s.b * meta.max_blocks;
-  const int32_t dst = phys_slot(bt_row, s.s0 + t, P, meta.num_pages, status);
-  if (k < c_out) {
-    const int32_t pos = __ldg(ku + k);
-    int32_t src = -1;
-    if (pos < 0 || pos >= s.n) atomicOr(status, KVC_DEV_BAD_KEEP);
-    else src = phys_slot(bt_row, s.s0 + pos, P, meta.num_pages, status);
-    const int64_t mi = lh * meta.Mtot + s.moff + k;
-    moves[2 * mi] = src;
-    moves[2 * mi + 1] = dst;
-  } else {
-    dead[u * P + (k - c_out)] = dst;
+  const int ndead = XP - m;
+  uint32_t base = 0;
+  for (int w0 = 0; w0 < words; w0 += kPlanThreads) {
+    const int w = w0 + tid;
+    uint32_t holes = 0u;
+    if (w < words) {
+      holes = ~bitmap[w];
+      const int valid = XP - (w << 5);
+      if (valid < 32) holes &= (1u << valid) - 1u;
+    }
+    const uint32_t before = block_exclusive_scan(__popc(holes), warp_sums, &sh_total);
+    const uint32_t total = sh_total;
+    uint32_t k = base + before;
+    while (holes != 0u) {
+      const int bit = __ffs(holes) - 1;
+      holes &= holes - 1u;
+      const int t = Bs + (w << 5) + bit;
+      if ((int)k < c_out + ndead) {
+        const int32_t dst = phys_slot(bt_row, s.s0 + t, P, meta.num_pages, status);
+        if ((int)k < c_out) {
+          const int32_t pos = __ldg(ku + k);
+          int32_t src = -1;
+          if (pos < 0 || pos >= s.n) atomicOr(status, KVC_DEV_BAD_KEEP);
+          else src = phys_slot(bt_row, s.s0 + pos, P, meta.num_pages, status);
+          reinterpret_cast<int2*>(moves)[lh * meta.Mtot + s.moff + k] = make_int2(src, dst);
+        } else {
+          dead[u * P + (k - c_out)] = dst;
+        }
+      }
+      ++k;
+    }
+    base += total;
   }
 }
 
 // Block-table rows after the release and the list of freed pages (sequence
 // order, ascending block order).  One CTA per sequence.
-__global__ void __launch_bounds__(kPlanThreads)
+__global__ void __launch_bounds__(256)
     rows_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
                 const int32_t* __restrict__ nblocks, int32_t* __restrict__ freed,
                 int32_t* __restrict__ new_rows, unsigned* status) {
@@ -124,84 +197,74 @@ __global__ void __launch_bounds__(kPlanThreads)
   for (int i = threadIdx.x; i < f; i += blockDim.x) freed[s.foff + i] = row[sb + i];
 }
 
-// One parallel copy: each move copies a K row, a V row (d bf16 each, 16-byte
-// vectors, D/4 lanes per move) and the tag; then dead holes get tag -1.
+// One parallel copy.  A block copies up to kMovesPerBlock moves of one unit
+// (the unit is decoded once per block): each move moves a K row and a V row
+// (d bf16 each, 16-byte vectors, D/4 lanes per move) and the tag; U moves are
+// in flight per lane group.  The unit's first block also writes tag -1 to its
+// dead holes.
 template <int D>
 __global__ void __launch_bounds__(256)
     copy_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ moves,
                 const int32_t* __restrict__ move_count, const int32_t* __restrict__ dead,
                 const int32_t* __restrict__ dead_count, uint8_t* __restrict__ k_pool,
                 uint8_t* __restrict__ v_pool, int32_t* __restrict__ tags) {
-  constexpr int LPM = D / 4;        // lanes per move (16 B each, K and V rows)
-  constexpr int MPW = 32 / LPM;     // moves per warp per step
-  constexpr int CH = D / 8;         // 16-byte chunks per row
-  constexpr int U = 4;              // moves in flight per lane group
+  constexpr int LPM = D / 4;     // lanes per move
+  constexpr int MPW = 32 / LPM;  // moves per warp step
+  constexpr int CH = D / 8;      // 16-byte chunks per row
+  constexpr int U = 4;           // moves in flight per lane group
   constexpr int64_t kRowBytes = (int64_t)D * 2;
-  const int lane = threadIdx.x & 31;
+  const int64_t item = blockIdx.x;
+  const int si = find_seq(meta, item);
+  const SeqMeta& s = meta.seq[si];
+  const int per = max(1, (s.m + kMovesPerBlock - 1) / kMovesPerBlock);
+  const int64_t local = item - s.item0;
+  const int chunk = (int)(local % per);
+  const int64_t lh = local / per;
+  const int h = (int)(lh % meta.H), l = (int)(lh / meta.H);
+  const int64_t u = lh * meta.B + s.b;
+  const int P = meta.P, lp = meta.log2P;
+  const int64_t HP = (int64_t)meta.H * P;
+  const int64_t lbase = (int64_t)l * meta.num_pages * HP + (int64_t)h * P;
+  const int cnt = __ldg(move_count + u);
+  const int k0 = chunk * kMovesPerBlock, k1 = min(k0 + kMovesPerBlock, cnt);
+  const int2* mv = reinterpret_cast<const int2*>(moves) + (lh * meta.Mtot + s.moff);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = lane / LPM, c = lane % LPM;
   const int which = c / CH, ch = c % CH;
   uint8_t* pool = which ? v_pool : k_pool;
-  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t Mc = meta.items / ((int64_t)meta.L * meta.H);  // moves per (l, h) in this launch
-  const int P = meta.P;
-  const int64_t layer_rows = (int64_t)meta.num_pages * meta.H * P;
-
-  for (int64_t base = gw * (MPW * U); base < meta.items; base += nw * (MPW * U)) {
+  constexpr int kStride = 8 * MPW;  // moves per block step (8 warps)
+  for (int kb = k0 + warp * MPW + grp; kb < k1; kb += U * kStride) {
     int4 val[U];
-    int64_t dst_row[U];
+    int64_t drow[U];
     int32_t tag[U];
-    bool act[U];
 #pragma unroll
     for (int q = 0; q < U; ++q) {
-      const int64_t g = base + q * MPW + grp;
-      act[q] = false;
-      dst_row[q] = 0;
-      tag[q] = 0;
-      if (g < meta.items) {
-        const int64_t lh = g / Mc;
-        const int64_t rem = g - lh * Mc;
-        const int si = find_seq(meta, rem);
-        const SeqMeta& s = meta.seq[si];
-        const int k = (int)(rem - s.item0);
-        const int h = (int)(lh % meta.H), l = (int)(lh / meta.H);
-        if (k < __ldg(move_count + lh * meta.B + s.b)) {
-          const int64_t mi = lh * meta.Mtot + s.moff + k;
-          const int32_t src = __ldg(moves + 2 * mi), dst = __ldg(moves + 2 * mi + 1);
-          if (src >= 0 && dst >= 0) {
-            const int64_t lbase = l * layer_rows + h * P;
-            const int64_t src_row = lbase + (int64_t)(src / P) * meta.H * P + src % P;
-            dst_row[q] = lbase + (int64_t)(dst / P) * meta.H * P + dst % P;
-            val[q] = *reinterpret_cast<const int4*>(pool + src_row * kRowBytes + ch * 16);
-            if (c == 0) tag[q] = tags[src_row];
-            act[q] = true;
-          }
+      const int k = kb + q * kStride;
+      drow[q] = -1;
+      if (k < k1) {
+        const int2 m2 = __ldg(mv + k);
+        if (m2.x >= 0 && m2.y >= 0) {
+          const int64_t srow = lbase + (int64_t)(m2.x >> lp) * HP + (m2.x & (P - 1));
+          drow[q] = lbase + (int64_t)(m2.y >> lp) * HP + (m2.y & (P - 1));
+          val[q] = *reinterpret_cast<const int4*>(pool + srow * kRowBytes + ch * 16);
+          if (c == 0) tag[q] = tags[srow];
         }
       }
     }
 #pragma unroll
     for (int q = 0; q < U; ++q) {
-      if (!act[q]) continue;
-      *reinterpret_cast<int4*>(pool + dst_row[q] * kRowBytes + ch * 16) = val[q];
-      if (c == 0) tags[dst_row[q]] = tag[q];
+      if (drow[q] < 0) continue;
+      *reinterpret_cast<int4*>(pool + drow[q] * kRowBytes + ch * 16) = val[q];
+      if (c == 0) tags[drow[q]] = tag[q];
     }
   }
-
-  // dead holes of every unit of this launch: tag -1, bytes untouched
-  const int64_t ndead = (int64_t)meta.L * meta.H * meta.nseq * P;
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ndead;
-       g += (int64_t)gridDim.x * blockDim.x) {
-    const int j = (int)(g % P);
-    const int64_t r2 = g / P;
-    const int si = (int)(r2 % meta.nseq);
-    const int64_t lh = r2 / meta.nseq;
-    const SeqMeta& s = meta.seq[si];
-    const int64_t u = lh * meta.B + s.b;
-    if (j >= __ldg(dead_count + u)) continue;
-    const int32_t dst = __ldg(dead + u * P + j);
-    if (dst < 0) continue;
-    const int h = (int)(lh % meta.H), l = (int)(lh / meta.H);
-    tags[l * layer_rows + h * P + (int64_t)(dst / P) * meta.H * P + dst % P] = -1;
+  if (chunk == 0) {
+    const int nd = __ldg(dead_count + u);
+    for (int j = threadIdx.x; j < nd; j += blockDim.x) {
+      const int32_t dst = __ldg(dead + u * P + j);
+      if (dst >= 0) tags[lbase + (int64_t)(dst >> lp) * HP + (dst & (P - 1))] = -1;
+    }
   }
 }
 
@@ -245,7 +308,13 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
   for (size_t c = 0; c < cl.chunks; ++c) {
     const LaunchMeta& m = cl.plan_meta[c];
     if (m.items > 0) {
-      plan_kernel<<<(unsigned)m.items, kPlanThreads, 0, stream>>>(
+      const size_t smem = (size_t)std::max(1, m.words) * sizeof(uint32_t);
+      if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+      }
+      plan_kernel<<<(unsigned)m.items, kPlanThreads, smem, stream>>>(
           m, cl.block_table, cl.keep, cl.moves, cl.move_count, cl.dead, cl.dead_count, cl.status);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
@@ -253,8 +322,8 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
     }
     const LaunchMeta& r = cl.rows_meta[c];
     if (r.nseq > 0) {
-      rows_kernel<<<(unsigned)r.nseq, kPlanThreads, 0, stream>>>(r, cl.block_table, cl.nblocks,
-                                                                 cl.freed, cl.new_rows, cl.status);
+      rows_kernel<<<(unsigned)r.nseq, 256, 0, stream>>>(r, cl.block_table, cl.nblocks, cl.freed,
+                                                        cl.new_rows, cl.status);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       count_launch();
@@ -266,17 +335,13 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
 cudaError_t launch_compact(const CompactLaunch& cl, cudaStream_t stream) {
   for (size_t c = 0; c < cl.chunks; ++c) {
     const LaunchMeta& m = cl.copy_meta[c];
-    if (m.nseq <= 0) continue;
-    const int64_t warps_needed = (m.items + 3) / 4 + 1;
-    const int64_t dead_threads = (int64_t)m.L * m.H * m.nseq * m.P;
-    int64_t blocks = std::max<int64_t>((warps_needed + 7) / 8, (dead_threads + 255) / 256);
-    blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)cl.num_sms * 8);
+    if (m.items <= 0) continue;
     if (m.d == 128)
-      copy_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(
+      copy_kernel<128><<<(unsigned)m.items, 256, 0, stream>>>(
           m, cl.moves, cl.move_count, cl.dead, cl.dead_count, static_cast<uint8_t*>(cl.k_pool),
           static_cast<uint8_t*>(cl.v_pool), cl.tags);
     else
-      copy_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(
+      copy_kernel<64><<<(unsigned)m.items, 256, 0, stream>>>(
           m, cl.moves, cl.move_count, cl.dead, cl.dead_count, static_cast<uint8_t*>(cl.k_pool),
           static_cast<uint8_t*>(cl.v_pool), cl.tags);
     const cudaError_t e = cudaGetLastError();
