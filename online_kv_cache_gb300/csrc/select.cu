@@ -5,7 +5,7 @@
 // section).  Equal scores go to the lower position; the kept positions are
 // written in ascending order (the order the slot plan consumes them).
 //
-// One 1024-thread CTA per unit.  Scores are >= 0, so their fp32 bit patterns
+// One 512-thread CTA per unit.  Scores are >= 0, so their fp32 bit patterns
 // order like the values.  Three radix passes over the bits (11, 11, 10 from
 // the top) find the exact bit pattern T of the m-th largest score and how many
 // elements equal to T are kept (k_eq).  A final pass keeps every element > T
@@ -22,15 +22,21 @@ namespace kvc {
 
 namespace {
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;
+constexpr int kWarps = kSelThreads / 32;
+constexpr int kU = 8;                         // elements per thread per tile
+constexpr int kTileElems = kSelThreads * kU;  // element e of a tile: q * kSelThreads + tid
 constexpr int kBins = 2048;
 
-__global__ void __launch_bounds__(kSelThreads, 1)
+// One CTA per unit.  Element i of a tile sits at tile + q * kSelThreads + tid, so
+// every load instruction is coalesced and the (q, warp, lane) order is the index
+// order used for ranks.
+__global__ void __launch_bounds__(kSelThreads)
     select_topm_kernel(const __grid_constant__ LaunchMeta meta, const float* __restrict__ scores,
                        int32_t* __restrict__ keep) {
   __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t warp_gt[32], warp_eq[32];
-  __shared__ uint32_t sh_digit, sh_k;
+  __shared__ uint32_t pre_gt[kU * kWarps], pre_eq[kU * kWarps];
+  __shared__ uint32_t sh_digit, sh_k, sh_tot_gt, sh_tot_eq;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t item = blockIdx.x;
@@ -49,26 +55,31 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     return;
   }
 
-  // ---- radix select of the m-th largest bit pattern
+  // ---- radix select of the m-th largest bit pattern (11, 11, 10 bits)
   uint32_t prefix = 0, pmask = 0, k = (uint32_t)m;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t dmask = (1u << widths[pass]) - 1u;
-    const int nbins = 1 << widths[pass];
+    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int width = pass == 2 ? 10 : 11;
+    const uint32_t dmask = (1u << width) - 1u;
+    const int nbins = 1 << width;
     for (int i = tid; i < kBins; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int base = 0; base < n; base += kSelThreads) {  // warp-uniform trip count
-      const int i = base + tid;
-      uint32_t d = 0xFFFFFFFFu;  // "no digit"
-      if (i < n) {
-        const uint32_t u = __ldg(key + i);
-        if ((u & pmask) == prefix) d = (u >> sh) & dmask;
+#pragma unroll 1
+    for (int tile = 0; tile < n; tile += kTileElems) {
+      uint32_t u[kU];
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+        const int i = tile + q * kSelThreads + tid;
+        u[q] = (i < n) ? __ldg(key + i) : 0u;
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+        const int i = tile + q * kSelThreads + tid;
+        const uint32_t d = (i < n && (u[q] & pmask) == prefix) ? ((u[q] >> sh) & dmask) : 0xFFFFFFFFu;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -106,42 +117,68 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const uint32_t T = prefix;   // bit pattern of the m-th largest score
   const uint32_t k_eq = k;     // elements equal to T that are kept (lowest positions first)
 
-  // ---- order-preserving compaction
+  // ---- order-preserving compaction: rank = #(> T before) + min(#(== T before), k_eq)
   uint32_t base_gt = 0, base_eq = 0;
   const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll 1
-  for (int start = 0; start < n; start += kSelThreads) {
-    const int i = start + tid;
-    const uint32_t u = (i < n) ? __ldg(key + i) : 0u;
-    const bool gt = (i < n) && (u > T);
-    const bool eq = (i < n) && (u == T);
-    const unsigned bg = __ballot_sync(0xffffffffu, gt);
-    const unsigned be = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) {
-      warp_gt[warp] = __popc(bg);
-      warp_eq[warp] = __popc(be);
+  for (int tile = 0; tile < n; tile += kTileElems) {
+    uint32_t u[kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int i = tile + q * kSelThreads + tid;
+      u[q] = (i < n) ? __ldg(key + i) : 0u;
+    }
+    unsigned bg[kU], be[kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int i = tile + q * kSelThreads + tid;
+      bg[q] = __ballot_sync(0xffffffffu, i < n && u[q] > T);
+      be[q] = __ballot_sync(0xffffffffu, i < n && u[q] == T);
+      if (lane == 0) {
+        pre_gt[q * kWarps + warp] = __popc(bg[q]);
+        pre_eq[q * kWarps + warp] = __popc(be[q]);
+      }
     }
     __syncthreads();
-    if (warp == 0) {
-      const uint32_t g = warp_gt[lane], e = warp_eq[lane];
-      uint32_t ig = g, ie = e;
+    if (warp == 0) {  // exclusive scan of the kU * kWarps counts in (q, warp) order
+      constexpr int per = kU * kWarps / 32;
+      uint32_t g[per], e[per], sg = 0, se = 0;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        g[j] = pre_gt[lane * per + j];
+        e[j] = pre_eq[lane * per + j];
+        sg += g[j];
+        se += e[j];
+      }
+      uint32_t ig = sg, ie = se;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t tg = __shfl_up_sync(0xffffffffu, ig, o);
         const uint32_t te = __shfl_up_sync(0xffffffffu, ie, o);
         if (lane >= o) { ig += tg; ie += te; }
       }
-      warp_gt[lane] = ig - g;  // exclusive prefix over warps
-      warp_eq[lane] = ie - e;
-      if (lane == 31) { sh_digit = ig; sh_k = ie; }  // tile totals
+      uint32_t rg = ig - sg, re = ie - se;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        pre_gt[lane * per + j] = rg;
+        pre_eq[lane * per + j] = re;
+        rg += g[j];
+        re += e[j];
+      }
+      if (lane == 31) { sh_tot_gt = ig; sh_tot_eq = ie; }
     }
     __syncthreads();
-    const uint32_t gt_before = base_gt + warp_gt[warp] + __popc(bg & lt_mask);
-    const uint32_t eq_before = base_eq + warp_eq[warp] + __popc(be & lt_mask);
-    const uint32_t rank = gt_before + min(eq_before, k_eq);
-    if ((gt || (eq && eq_before < k_eq)) && rank < (uint32_t)m) out[rank] = i;
-    base_gt += sh_digit;
-    base_eq += sh_k;
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int i = tile + q * kSelThreads + tid;
+      const uint32_t gt_before = base_gt + pre_gt[q * kWarps + warp] + __popc(bg[q] & lt_mask);
+      const uint32_t eq_before = base_eq + pre_eq[q * kWarps + warp] + __popc(be[q] & lt_mask);
+      const bool gt = (bg[q] >> lane) & 1u, eq = (be[q] >> lane) & 1u;
+      const uint32_t rank = gt_before + min(eq_before, k_eq);
+      if ((gt || (eq && eq_before < k_eq)) && rank < (uint32_t)m) out[rank] = i;
+    }
+    base_gt += sh_tot_gt;
+    base_eq += sh_tot_eq;
     __syncthreads();
   }
 }

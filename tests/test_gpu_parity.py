@@ -219,3 +219,30 @@ def test_logical_view_after_compaction():
                 assert [e[0] for e in live] == list(pos)
                 assert np.array_equal(np.array([e[1] for e in live]).reshape(Kc.shape), Kc)
                 assert np.array_equal(np.array([e[2] for e in live]).reshape(Vc.shape), Vc)
+
+
+@pytest.mark.parametrize("distinct", [1, 3])
+def test_exact_ties_keep_lowest_positions(distinct):
+    """Keys drawn from `distinct` vectors: scores tie exactly on both sides, and the lower
+    position wins, so the GPU keep sets equal the oracle's exactly."""
+    sp = workloads.custom(L=1, H=2, G=4, d=128, P=16, q=8, lengths=(1000, 4096), shuffle_pages=True)
+    case = workloads.build(sp, 9, DEV, with_q=False)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(123)
+    basis = torch.randn((distinct, sp.d), generator=g, device=DEV).to(torch.bfloat16)
+    pick = torch.randint(0, distinct, case.k_pool.shape[:-1], generator=g, device=DEV)
+    case.k_pool.copy_(basis[pick])
+    workloads.make_q(case, 9)
+    m = PT.lib_budgets(case)
+    s_orc, _ = PT.oracle_scores(case)
+    keep_orc = oracle.select_cache(s_orc, case.seg_start, case.seg_end, m)
+    cp = PT.compactor(case, m)
+    cp.score(case.q, sp.scale)
+    cp.select()
+    torch.cuda.synchronize()
+    k_gpu = cp.keep.cpu().numpy()[:, :, :cp.Mtot]
+    assert np.array_equal(k_gpu, keep_orc)
+    if distinct == 1:
+        noff, moff = PT.unit_offsets(case, m)
+        for b in range(sp.B):
+            assert np.array_equal(k_gpu[0, 0, moff[b]:moff[b + 1]], np.arange(m[b]))
