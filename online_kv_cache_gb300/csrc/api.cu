@@ -251,7 +251,7 @@ ScoreGeom score_geom(int R, int d) {
   const int fixed = score_smem_bytes(0, 0, d);
   g.gsub1 = std::min(4, g.rowtiles);
   g.ngroups1 = (int)ceil_div(g.rowtiles, g.gsub1);
-  g.qbytes1 = g.gsub1 * 128 * d * 2;
+  g.qbytes1 = 2 * 128 * d * 2;  // two staging buffers: pass 1 keeps Q in TMEM
   g.kst1 = std::min(8, (kScoreSmemLimit - fixed - g.qbytes1) / tile_bytes);
   g.gsub2 = std::min(g.nchunks, std::max(1, 512 / g.W));
   g.ngroups2 = (int)ceil_div(g.nchunks, g.gsub2);

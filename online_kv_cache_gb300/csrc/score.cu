@@ -114,13 +114,17 @@ __device__ __forceinline__ int32_t page_row(const LaunchMeta& meta, const int32_
 
 // ============================================================== skeleton
 
-// PASS 1: A = Q row tile (M = 128 rows), B = K tile (N = 128 keys).
-// PASS 2: A = K tile (M = 128 keys), B = Q chunk (N = W rows).
+// PASS 1: A = Q row tile (M = 128 rows) read from TMEM, B = K tile (N = 128
+//         keys).  At the start of each item the group's row tiles pass through
+//         a two-buffer shared-memory staging ring and tcgen05.cp copies them
+//         into TMEM columns 256..511, so the MMAs fetch only B from shared memory.
+// PASS 2: A = K tile (M = 128 keys), B = Q chunk (N = W rows), both from shared
+//         memory (the Q group stays resident there).
 // Jobs run tile by tile: for each K tile, one job per row tile / chunk of the
 // group; job number jc (counted over the CTA's whole run) goes to warpgroup
-// jc & 1, which uses its own TMEM slots (two of 128 columns in pass 1, one of
-// 256 in pass 2).  Only one K tile is in use at a time, so a ring of kst tiles
-// keeps kst - 1 tiles in flight.
+// jc & 1, which owns one TMEM accumulator slot (128 columns in pass 1, 256 in
+// pass 2).  Only one K tile is in use at a time, so a ring of kst tiles keeps
+// kst - 1 tiles in flight.
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     score_pass_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -128,8 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       float2* __restrict__ part1, const float* __restrict__ nob,
                       float* __restrict__ out2, unsigned* status) {
   using C = Cfg<D>;
-  constexpr int NBW = (PASS == 1) ? 2 : 1;        // TMEM slots per warpgroup
+  constexpr int NBW = 1;                          // TMEM slots per warpgroup
   constexpr int SLOT_COLS = (PASS == 1) ? 128 : 256;
+  constexpr uint32_t kQTmemCol = 256;             // pass 1: resident Q row tiles
+  constexpr uint32_t kQTmemCols = D / 2;          // TMEM columns per 128-row Q tile
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // [barriers, TMEM address, abort flag, reduction buffer][pad to 1024][Q group][K ring]
   const int kst = meta.kst;
@@ -142,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + kMaxKStages;
   uint64_t* t_full = k_empty + kMaxKStages;  // [4] TMEM slots
   uint64_t* t_empty = t_full + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 4);
+  uint64_t* drain = t_empty + 4;         // pass 1: all MMAs of the previous item done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parity][128] (pass 2)
 
@@ -154,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 4; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     for (int i = 0; i < kMaxKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < 4; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 128); }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
@@ -172,13 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- producer (whole warp)
     // Load order per item: its first min(kst-1, tiles) K tiles, then its Q group
     // (sub-tile by sub-tile as the previous item releases them), then the rest.
-    uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0};
+    uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0}, qc = 0;
     bool ok = true;
     int64_t k_item = blockIdx.x, q_item = blockIdx.x;
     Item kit_ = k_item < meta.items ? decode_item(meta, k_item, total_sub) : Item{};
     int kt = kit_.t0;
     int32_t prow = k_item < meta.items ? page_row(meta, block_table, kit_.u, kt, lane, status) : -1;
     const int ppt = kTile / meta.P;
+
     while (ok && (k_item < meta.items || q_item < meta.items)) {
       const int pre = min(kst - 1, kit_.t1 - kit_.t0);
       // Q of item q_item goes after that item's first `pre` K tiles (or at once
@@ -191,18 +200,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = ((qi.u.b * meta.L + qi.u.l) * meta.H + qi.u.h) * meta.R +
                          qi.u.g * meta.gsub * sub_rows;
         for (int j = 0; j < qi.J && ok; ++j) {
+          // pass 1: staging buffer qc % 2; pass 2: the group's own sub-tile slot j
+          const int qs = (PASS == 1) ? (int)(qc & 1) : j;
+          const uint32_t qpar = (PASS == 1) ? ((qc >> 1) & 1) : (q_use[j] & 1);
           if (lane == 0) {
-            ok = mbar_wait(&q_empty[j], (q_use[j] & 1) ^ 1, abort_flag, status);
+            ok = mbar_wait(&q_empty[qs], qpar ^ 1, abort_flag, status);
             if (ok) {
-              mbar_arrive_expect_tx(&q_full[j], sub_bytes);
+              mbar_arrive_expect_tx(&q_full[qs], sub_bytes);
 #pragma unroll
               for (int kb = 0; kb < C::KB; ++kb)
-                tma_load_2d(sQ + (j * C::KB + kb) * sub_rows * 128, &tmQ, &q_full[j], kb * 64,
+                tma_load_2d(sQ + (qs * C::KB + kb) * sub_rows * 128, &tmQ, &q_full[qs], kb * 64,
                             qrow + j * sub_rows);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           ++q_use[j];
+          ++qc;
         }
         q_item += gridDim.x;
         continue;
@@ -219,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int32_t prow_next = nitem < meta.items ? page_row(meta, block_table, nit.u, nt, lane, status) : -1;
+
       const int ks = kcount % kst;
       if (lane == 0) ok = mbar_wait(&k_empty[ks], ((kcount / kst) & 1) ^ 1, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -243,19 +257,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) {  // let issued copies land before the CTA exits
       for (uint32_t j = (kcount > (uint32_t)kst ? kcount - kst : 0); j < kcount; ++j)
         mbar_wait(&k_full[j % kst], (j / kst) & 1, nullptr, status);
-      for (int j = 0; j < 4; ++j)
-        if (q_use[j] > 0) mbar_wait(&q_full[j], (q_use[j] - 1) & 1, nullptr, status);
+      if (PASS == 1) {
+        for (uint32_t j = (qc > 2 ? qc - 2 : 0); j < qc; ++j)
+          mbar_wait(&q_full[j & 1], (j >> 1) & 1, nullptr, status);
+      } else {
+        for (int j = 0; j < 4; ++j)
+          if (q_use[j] > 0) mbar_wait(&q_full[j], (q_use[j] - 1) & 1, nullptr, status);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = (PASS == 1) ? idesc_bf16_f32(kTile, kTile) : idesc_bf16_f32(kTile, meta.W);
       uint32_t kcount = 0, jc = 0, cnt[2] = {0, 0}, q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
+      uint32_t qc = 0, dc = 0;
       bool issued = false, ok = true;
       const uint32_t q_base = smem_u32(sQ);
       for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
         const Item it = decode_item(meta, item, total_sub);
-        for (int j = 0; j < it.J && ok; ++j) ok = mbar_wait(&q_full[j], q_use[j] & 1, abort_flag, status);
+        if (PASS == 1) {
+          // the previous item's MMAs read the TMEM copy of Q: let them finish
+          if (issued) {
+            mma_commit(drain);
+            if (!(ok = mbar_wait(drain, dc & 1, abort_flag, status))) break;
+            ++dc;
+            tc_fence_after_sync();
+          }
+          for (int j = 0; j < it.J && ok; ++j) {
+            const uint32_t qs = qc & 1;
+            if (!(ok = mbar_wait(&q_full[qs], (qc >> 1) & 1, abort_flag, status))) break;
+            const uint32_t stage = q_base + qs * sub_bytes;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              tmem_cp_128x256b(tmem + kQTmemCol + j * kQTmemCols + k * 8,
+                               sdesc_k_sw128(stage + (k >> 2) * C::kKbBytes + (k & 3) * 32));
+            mma_commit(&q_empty[qs]);  // staging buffer free once the copy is done
+            issued = true;
+            ++qc;
+          }
+        } else {
+          for (int j = 0; j < it.J && ok; ++j) ok = mbar_wait(&q_full[j], q_use[j] & 1, abort_flag, status);
+        }
         if (!ok) break;
         for (int t = it.t0; t < it.t1 && ok; ++t) {
           const int ks = kcount % kst;
@@ -274,14 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t koff_k = (k >> 2) * C::kKbBytes + (k & 3) * 32;
               const uint32_t koff_q = (k >> 2) * (uint32_t)(sub_rows * 128) + (k & 3) * 32;
               if (PASS == 1)
-                mma_bf16(d_tmem, sdesc_k_sw128(sub_base + koff_q), sdesc_k_sw128(k_base + koff_k), idesc,
-                         k > 0);
+                mma_bf16_tmem_a(d_tmem, tmem + kQTmemCol + j * kQTmemCols + k * 8,
+                                sdesc_k_sw128(k_base + koff_k), idesc, k > 0);
               else
                 mma_bf16(d_tmem, sdesc_k_sw128(k_base + koff_k), sdesc_k_sw128(sub_base + koff_q), idesc,
                          k > 0);
             }
             mma_commit(&t_full[slot]);
-            if (t == it.t1 - 1) mma_commit(&q_empty[j]);  // last use of this Q sub-tile
+            if (PASS == 2 && t == it.t1 - 1) mma_commit(&q_empty[j]);  // last use of this Q sub-tile
             issued = true;
             last_slot = slot;
             last_use = use;
