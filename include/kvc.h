@@ -212,6 +212,26 @@ kvc_status kvc_score_alpha(const kvc_cache *cache, const kvc_segments *segs, con
                            int32_t R, float scale, const float *lse, float *scores, void *ws,
                            size_t ws_bytes, kvc_stream_t stream);
 
+/* kvc_score without a caller workspace.  (No counterpart on the pages: this is
+ * an interface convenience.)  Some callers cannot allocate device memory for
+ * the workspace: a serving engine whose allocator already owns the device's
+ * memory for its page pool, code that must not enter the CUDA allocator on its
+ * hot path, or a plugin that only receives the cache's pointers.  This entry
+ * point takes the same inputs and outputs as kvc_score and puts the workspace
+ * in a fixed 16 MiB device array inside the library; it calls no cudaMalloc,
+ * cudaFree or allocating routine.
+ *   - Every GPU that loads the library holds the 16 MiB array until the
+ *     process exits.  A call whose workspace (kvc_score_workspace_size) is
+ *     larger returns KVC_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share its array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose kernels
+ *     may overlap on the GPU (issued on different streams) race on the array:
+ *     issue them on one stream. */
+kvc_status kvc_score_noalloc(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
+                             int32_t R, float scale, float *scores, float *lse, kvc_stream_t stream);
+
 /* Bytes of workspace kvc_select_topm needs (may be 0). */
 kvc_status kvc_select_workspace_size(const kvc_cache *cache, const kvc_segments *segs,
                                      const int32_t *m, size_t *bytes);

@@ -44,7 +44,7 @@ EXPORTED = (
     "kvc_select_workspace_size", "kvc_select_topm", "kvc_plan_buffer_sizes", "kvc_plan_compact",
     "kvc_compact", "kvc_free_pages", "kvc_status_string", "kvc_last_error",
     "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
-    "kvc_score_alpha", "kvc_launch_count",
+    "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc",
 )
 
 
@@ -133,6 +133,7 @@ def lib():
             "kvc_score_lse": (I32, [C, SG, P, I32, F, P, P, S, P]),
             "kvc_score_alpha": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
             "kvc_launch_count": (ctypes.c_uint64, [I32]),
+            "kvc_score_noalloc": (I32, [C, SG, P, I32, F, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -263,6 +264,15 @@ def kvc_score_alpha(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale
                                  float(scale), _dev_ptr(lse, "lse", torch.float32),
                                  _dev_ptr(scores, "scores", torch.float32), _dev_ptr(ws, "ws"),
                                  ws.numel() * ws.element_size(), _stream(stream)), "kvc_score_alpha")
+
+
+def kvc_score_noalloc(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale: float,
+                      scores: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None):
+    """kvc_score with the library's fixed device scratch instead of a caller workspace."""
+    _check(lib().kvc_score_noalloc(cache.ref, segs.ref, _dev_ptr(q, "q", torch.bfloat16), int(R),
+                                   float(scale), _dev_ptr(scores, "scores", torch.float32),
+                                   _dev_ptr(lse, "lse", torch.float32), _stream(stream)),
+           "kvc_score_noalloc")
 
 
 def kvc_launch_count(reset: bool = False) -> int:

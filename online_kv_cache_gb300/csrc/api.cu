@@ -533,6 +533,60 @@ kvc_status kvc_score_alpha(const kvc_cache* cache, const kvc_segments* segs, con
                       ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- no-alloc scoring
+//
+// kvc_score with its workspace in a fixed device array owned by the library,
+// for callers that cannot hand the library a cudaMalloc'ed workspace.
+
+}  // extern "C"
+
+namespace kvc {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (cudaGetSymbolAddress must run with that device current; in host code
+// the symbol itself is only a host-side stand-in).
+kvc_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(KVC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_score_noalloc(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q,
+                             int32_t R, float scale, float* scores, float* lse, kvc_stream_t stream) {
+  size_t need = 0;
+  kvc_status st = kvc_score_workspace_size(cache, segs, R, &need);
+  if (st != KVC_OK) return st;
+  if (need > kNoAllocScratchBytes)
+    return fail(KVC_ERR_WORKSPACE,
+                "kvc_score_noalloc: this call needs %zu bytes of workspace; the library's fixed "
+                "scratch holds %zu (use kvc_score with a caller workspace)",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != KVC_OK) return st;
+  return kvc_score(cache, segs, q, R, scale, scores, lse, ws, kNoAllocScratchBytes, stream);
+}
+
 uint64_t kvc_launch_count(int32_t reset) {
   return reset ? g_launches.exchange(0) : g_launches.load();
 }

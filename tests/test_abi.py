@@ -188,3 +188,15 @@ def test_validator_seq_len(lib):
     bt, nb, free = good_state()
     with pytest.raises(kvc.KvcError):
         kvc.kvc_validate_cache_host(bt, nb, [49, 20], 8, 16, free, 3)  # 49 slots need 4 blocks
+
+
+def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
+    """kvc_score_noalloc refuses, before any launch, a call whose workspace exceeds its 16 MiB."""
+    c = fake_cache(L=64, num_pages=40000, H=8, P=16, d=128, max_blocks=4096, batch=1)
+    s, _ = segs([0], [65536], [65536])
+    need = ctypes.c_size_t(0)
+    assert lib.kvc_score_workspace_size(ctypes.byref(c), ctypes.byref(s), 4096, ctypes.byref(need)) == 0
+    assert need.value > 16 << 20
+    st = lib.kvc_score_noalloc(ctypes.byref(c), ctypes.byref(s), 0x60000, 4096, 0.1, 0x70000, None, None)
+    assert st == kvc.KVC_ERR_WORKSPACE
+    assert "scratch" in kvc.kvc_last_error()
