@@ -377,6 +377,25 @@ kvc_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int d, in
   return KVC_OK;
 }
 
+// The K pool as a 4-D tensor [row group][k-block][row in group][64 elements]
+// (k-blocks of 64 head-dim elements = 128 B, groups of 8 rows): one box of
+// {64, 8, d/64, P/8} fetches a whole page of one head in one copy and lands in
+// shared memory as 1024-byte swizzle atoms ordered (row group, k-block), the
+// layout the MMA reads with a group stride of (d/64) x 1024 B.
+kvc_status make_kmap(CUtensorMap* map, const void* base, int64_t rows, int d, int P) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[4] = {64, 8, (cuuint64_t)(d / 64), (cuuint64_t)(rows / 8)};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * 8};
+  const cuuint32_t box[4] = {64, 8, (cuuint32_t)(d / 64), (cuuint32_t)(P / 8)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled (K pages) failed (%d)", (int)r);
+  return KVC_OK;
+}
+
 }  // namespace
 }  // namespace kvc
 
@@ -472,7 +491,7 @@ kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cac
   const int64_t qrows = (int64_t)cache->batch * cache->num_layers * cache->num_kv_heads * R;
   if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
   CUtensorMap tmK, tmQ1, tmQ2;
-  if ((st = make_tmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
+  if ((st = make_kmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
   if ((st = make_tmap(&tmQ1, q, qrows, cache->head_dim, 128)) != KVC_OK) return st;
   if ((st = make_tmap(&tmQ2, q, qrows, cache->head_dim, g.W)) != KVC_OK) return st;
 

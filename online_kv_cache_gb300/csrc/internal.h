@@ -25,7 +25,7 @@ enum ScorePhase : unsigned {
 // Dynamic shared memory of a scoring pass: the barrier block, up to 1024 B of
 // alignment padding, the resident row group of Q and `kst` K tiles of 128 keys.
 constexpr int kScoreSmemLimit = 232448;  // 227 KB per block on sm_103a
-constexpr int kScoreSmemHead = 1536;     // barriers, TMEM address, reduction buffer
+constexpr int kScoreSmemHead = 2048;     // barriers, TMEM address, reduction buffer, page ring
 __host__ __device__ constexpr int score_smem_bytes(int qbytes, int kst, int d) {
   return kScoreSmemHead + 1024 + qbytes + kst * 128 * d * 2;
 }

@@ -82,6 +82,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------------------------ cp.async (4-byte)
+
+// Asynchronous 4-byte global -> shared copy (completion tracked per thread by
+// commit/wait groups).  Used for small gathers that must not hold a register.
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gmem_src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -96,6 +112,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// 4-D tiled bulk tensor load (x innermost; x must be 16-byte aligned in bytes).
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 
@@ -137,12 +163,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes, the layout
 // TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).  `saddr` may be offset by a
-// multiple of 32 bytes inside the atom row to step along K.
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+// multiple of 32 bytes inside the atom row to step along K; `group_stride` is
+// the distance between consecutive 8-row atoms (1024 B when the atoms of one
+// 64-element k-block are contiguous).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr, uint32_t group_stride = 1024) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address / 16
   d |= (uint64_t)1 << 16;                    // leading-dimension offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride between 8-row groups: 1024 B
+  d |= (uint64_t)(group_stride >> 4) << 32;  // stride between 8-row groups
   d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
   d |= (uint64_t)2 << 61;                    // swizzle mode: 128 B
   return d;

@@ -8,13 +8,13 @@
 //   s_j   = sqrt((1/R) sum_i exp(2 (scale q_i.k_j - LSE_i)))
 //
 // Both passes share one persistent, warp-specialised skeleton (one CTA per SM):
-//   warp 0      producer: keeps a row group of Q resident in shared memory and
-//               streams 128-key K tiles through a ring, gathered page by page
-//               through the block table with 2-D TMA (the warp's lanes fetch
-//               the block-table entries of the next tile ahead of time)
+//   warp 0      producer: loads the row group of Q and streams 128-key K
+//               tiles through a ring, gathered page by page through the block
+//               table with 2-D TMA (the block-table entries arrive kPageRing - 1
+//               tiles ahead through cp.async)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2..9  two epilogue warpgroups; warpgroup w owns every other K tile
-//               of an item and drains its own TMEM slots
+//   warps 2..9  two epilogue warpgroups; they take the MMA jobs alternately
+//               and drain the TMEM accumulator slots round robin
 // A work item is (unit, row group, key range).  Each K tile yields one MMA job
 // per 128-row tile (pass 1) or per W-row chunk (pass 2) of the group.
 //
@@ -48,12 +48,17 @@ constexpr float kBias = 100.0f;     // alpha^2 is accumulated as alpha^2 * 2^kBi
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 320;       // producer, MMA, 2 x 4 epilogue warps
 constexpr int kMaxKStages = 8;
+constexpr int kPageRing = 8;        // key tiles whose block-table entries are in flight
+constexpr int kPagesPerTileMax = 16; // 128 keys in pages of >= 8 slots
 
 template <int D>
 struct Cfg {
   static constexpr int KB = D / 64;                 // 128-byte k-blocks per row
   static constexpr int kTileBytes = kTile * D * 2;  // one 128-row operand tile
-  static constexpr int kKbBytes = kTile * 128;      // one k-block of a 128-row tile
+  static constexpr int kKbBytes = kTile * 128;      // one k-block of a 128-row Q tile
+  // K tiles: 1024-byte atoms (8 rows x one k-block) ordered (row group, k-block)
+  static constexpr int kKGroup = KB * 1024;          // stride between 8-key row groups
+  static constexpr int kKPageBytesPerRow = D * 2;    // a page of P keys fills P * D * 2 bytes
 };
 
 struct Unit {
@@ -95,21 +100,23 @@ __device__ __forceinline__ Item decode_item(const LaunchMeta& meta, int64_t item
   return it;
 }
 
-// TMA row of page `lane` of key tile t (-1 for lanes past the tile's pages and
-// for pages past the segment end).  A block-table entry outside the pool is
-// reported in the status word and skipped.
-__device__ __forceinline__ int32_t page_row(const LaunchMeta& meta, const int32_t* block_table,
-                                            const Unit& u, int t, int lane, unsigned* status) {
-  const int P = meta.P;
-  if (lane >= kTile / P) return -1;
-  const int slot = t * kTile + lane * P;
-  if (slot >= u.n) return -1;
-  const int32_t page = __ldg(block_table + (int64_t)u.b * meta.max_blocks + (u.s0 + slot) / P);
-  if (page < 0 || page >= meta.num_pages) {
-    atomicOr(status, KVC_DEV_BAD_PAGE);
-    return -1;
+// sum_jj 2^(c v_jj - m) over one TMEM row of a key tile (masked keys hold -inf).
+__device__ __forceinline__ float tile_exp2_sum(const float (&v)[kTile], float c, float m) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+  for (int jj = 0; jj < kTile; jj += 8) {
+    const float2 x0 = __ffma2_rn(make_float2(v[jj + 0], v[jj + 1]), cc, nm);
+    const float2 x1 = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), cc, nm);
+    const float2 x2 = __ffma2_rn(make_float2(v[jj + 4], v[jj + 5]), cc, nm);
+    const float2 x3 = __ffma2_rn(make_float2(v[jj + 6], v[jj + 7]), cc, nm);
+    a0 = __fadd2_rn(a0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
+    a1 = __fadd2_rn(a1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
+    a2 = __fadd2_rn(a2, make_float2(ex2_approx(x2.x), ex2_approx(x2.y)));
+    a3 = __fadd2_rn(a3, make_float2(ex2_approx(x3.x), ex2_approx(x3.y)));
   }
-  return ((u.l * meta.num_pages + page) * meta.H + u.h) * P;
+  const float2 s01 = __fadd2_rn(a0, a1), s23 = __fadd2_rn(a2, a3);
+  return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
 // ============================================================== skeleton
@@ -122,9 +129,13 @@ __device__ __forceinline__ int32_t page_row(const LaunchMeta& meta, const int32_
 //         memory (the Q group stays resident there).
 // Jobs run tile by tile: for each K tile, one job per row tile / chunk of the
 // group; job number jc (counted over the CTA's whole run) goes to warpgroup
-// jc & 1, which owns one TMEM accumulator slot (128 columns in pass 1, 256 in
-// pass 2).  Only one K tile is in use at a time, so a ring of kst tiles keeps
-// kst - 1 tiles in flight.
+// jc & 1 and to TMEM accumulator slot jc % nslots.  Slots are 128 columns wide
+// (256 in pass 2 when W > 128) and fill the columns pass 1's resident Q leaves
+// free, so small row groups get three or four slots and a deeper
+// MMA -> epilogue pipeline.  Only one K tile is in use at a time, so a ring of
+// kst tiles keeps kst - 1 tiles in flight.  The block-table entries of the
+// next kPageRing - 1 tiles travel ahead of the K ring through cp.async into a
+// shared-memory ring, so no TMA issue waits on a global load.
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     score_pass_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -132,12 +143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       float2* __restrict__ part1, const float* __restrict__ nob,
                       float* __restrict__ out2, unsigned* status) {
   using C = Cfg<D>;
-  constexpr int NBW = 1;                          // TMEM slots per warpgroup
-  constexpr int SLOT_COLS = (PASS == 1) ? 128 : 256;
-  constexpr uint32_t kQTmemCol = 256;             // pass 1: resident Q row tiles
   constexpr uint32_t kQTmemCols = D / 2;          // TMEM columns per 128-row Q tile
+  // TMEM: accumulator slots from column 0; pass 1 keeps its Q row tiles at the top
+  const uint32_t slot_cols = (PASS == 1 || meta.W <= 128) ? 128u : 256u;
+  const uint32_t q_col0 = (PASS == 1) ? 512u - (uint32_t)meta.gsub * kQTmemCols : 512u;
+  const uint32_t nslots = min(4u, q_col0 / slot_cols);
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  // [barriers, TMEM address, abort flag, reduction buffer][pad to 1024][Q group][K ring]
+  // [barriers | TMEM address, abort flag | reduction buffer | page ring][pad to 1024][Q group][K ring]
   const int kst = meta.kst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
   uint8_t* sQ = align1024(smem_raw + kScoreSmemHead);
@@ -149,9 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* t_full = k_empty + kMaxKStages;  // [4] TMEM slots
   uint64_t* t_empty = t_full + 4;
   uint64_t* drain = t_empty + 4;         // pass 1: all MMAs of the previous item done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 384);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parity][128] (pass 2)
+  float* red = reinterpret_cast<float*>(smem_raw + 512);           // [2 parity][128] (pass 2)
+  int32_t* page_ring = reinterpret_cast<int32_t*>(smem_raw + 1536);  // [kPageRing][16]
 
   const int total_sub = (PASS == 1) ? meta.rowtiles : meta.nchunks;
   const int sub_rows = (PASS == 1) ? kTile : meta.W;  // Q rows per job
@@ -160,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     for (int i = 0; i < kMaxKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
-    for (int i = 0; i < 4; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 128); }
+    for (int i = 0; i < 4; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 4); }  // 4 warps
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -182,11 +195,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (sub-tile by sub-tile as the previous item releases them), then the rest.
     uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0}, qc = 0;
     bool ok = true;
+    const int ppt = kTile / meta.P;  // pages per key tile (<= kPagesPerTileMax)
+    // Page-ring cursor: one commit group per key tile of this CTA, in K order;
+    // lane p < ppt copies the block-table entry of page p of the tile.
+    int64_t pf_item = blockIdx.x;
+    Item pf = pf_item < meta.items ? decode_item(meta, pf_item, total_sub) : Item{};
+    int pf_t = pf.t0;
+    uint32_t pf_count = 0;
+    auto page_prefetch = [&]() {
+      if (pf_item < meta.items) {
+        const int slot = pf_t * kTile + lane * meta.P;
+        if (lane < ppt && slot < pf.u.n)
+          cp_async_4(page_ring + (pf_count % kPageRing) * kPagesPerTileMax + lane,
+                     block_table + (int64_t)pf.u.b * meta.max_blocks + (pf.u.s0 + slot) / meta.P);
+        if (++pf_t >= pf.t1) {
+          pf_item += gridDim.x;
+          if (pf_item < meta.items) {
+            pf = decode_item(meta, pf_item, total_sub);
+            pf_t = pf.t0;
+          }
+        }
+      }
+      cp_async_commit();
+      ++pf_count;
+    };
+    for (int i = 0; i < kPageRing - 1; ++i) page_prefetch();
+
     int64_t k_item = blockIdx.x, q_item = blockIdx.x;
     Item kit_ = k_item < meta.items ? decode_item(meta, k_item, total_sub) : Item{};
     int kt = kit_.t0;
-    int32_t prow = k_item < meta.items ? page_row(meta, block_table, kit_.u, kt, lane, status) : -1;
-    const int ppt = kTile / meta.P;
 
     while (ok && (k_item < meta.items || q_item < meta.items)) {
       const int pre = min(kst - 1, kit_.t1 - kit_.t0);
@@ -220,18 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         q_item += gridDim.x;
         continue;
       }
-      // the K tile after this one, and its page rows (consumed next iteration)
-      Item nit = kit_;
-      int nt = kt + 1;
-      int64_t nitem = k_item;
-      if (nt >= kit_.t1) {
-        nitem = k_item + gridDim.x;
-        if (nitem < meta.items) {
-          nit = decode_item(meta, nitem, total_sub);
-          nt = nit.t0;
-        }
+      // page rows of key tile kt (its ring entry was committed kPageRing - 1 groups ago)
+      page_prefetch();
+      cp_async_wait_group<kPageRing - 1>();
+      int32_t prow = -1;
+      if (lane < ppt && kt * kTile + lane * meta.P < kit_.u.n) {
+        const int32_t page = page_ring[(kcount % kPageRing) * kPagesPerTileMax + lane];
+        if (page < 0 || page >= meta.num_pages)
+          atomicOr(status, KVC_DEV_BAD_PAGE);  // outside the pool: reported, not read
+        else
+          prow = ((kit_.u.l * meta.num_pages + page) * meta.H + kit_.u.h) * meta.P;
       }
-      const int32_t prow_next = nitem < meta.items ? page_row(meta, block_table, nit.u, nt, lane, status) : -1;
 
       const int ks = kcount % kst;
       if (lane == 0) ok = mbar_wait(&k_empty[ks], ((kcount / kst) & 1) ^ 1, abort_flag, status);
@@ -242,18 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* dst = sK + ks * C::kTileBytes;
       for (int p = 0; p < ppt; ++p) {
         const int32_t row = __shfl_sync(0xffffffffu, prow, p);
-        if (lane == 0 && row >= 0) {
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(dst + kb * C::kKbBytes + p * meta.P * 128, &tmK, &k_full[ks], kb * 64, row);
-        }
+        if (lane == 0 && row >= 0)  // the page's P keys, every k-block, in one copy
+          tma_load_4d(dst + p * meta.P * C::kKPageBytesPerRow, &tmK, &k_full[ks], 0, 0, 0, row >> 3);
       }
       ++kcount;
-      k_item = nitem;
-      kit_ = nit;
-      kt = nt;
-      prow = prow_next;
+      if (++kt >= kit_.t1) {
+        k_item += gridDim.x;
+        if (k_item < meta.items) {
+          kit_ = decode_item(meta, k_item, total_sub);
+          kt = kit_.t0;
+        }
+      }
     }
+    cp_async_wait_all();  // no page copy outlives the CTA
     if (!ok && lane == 0) {  // let issued copies land before the CTA exits
       for (uint32_t j = (kcount > (uint32_t)kst ? kcount - kst : 0); j < kcount; ++j)
         mbar_wait(&k_full[j % kst], (j / kst) & 1, nullptr, status);
@@ -267,12 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // One thread issues every MMA; its loop is on the critical path for short
+    // jobs, so descriptors are built once per tile and stepped along K by adding
+    // the 16-byte-unit offset of each k-step to the start-address field.
     if (lane == 0) {
       const uint32_t idesc = (PASS == 1) ? idesc_bf16_f32(kTile, kTile) : idesc_bf16_f32(kTile, meta.W);
-      uint32_t kcount = 0, jc = 0, cnt[2] = {0, 0}, q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
+      uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
+      uint32_t slot = 0, use = 0;  // accumulator slot of the next job and its use count
       uint32_t qc = 0, dc = 0;
       bool issued = false, ok = true;
       const uint32_t q_base = smem_u32(sQ);
+      const uint64_t q_desc = sdesc_k_sw128(q_base);
+      const uint32_t q_kb_step = (uint32_t)(sub_rows * 128) >> 4;  // one k-block of a Q sub-tile
       for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
         const Item it = decode_item(meta, item, total_sub);
         if (PASS == 1) {
@@ -286,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < it.J && ok; ++j) {
             const uint32_t qs = qc & 1;
             if (!(ok = mbar_wait(&q_full[qs], (qc >> 1) & 1, abort_flag, status))) break;
-            const uint32_t stage = q_base + qs * sub_bytes;
+            const uint64_t stage = q_desc + ((qs * sub_bytes) >> 4);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              tmem_cp_128x256b(tmem + kQTmemCol + j * kQTmemCols + k * 8,
-                               sdesc_k_sw128(stage + (k >> 2) * C::kKbBytes + (k & 3) * 32));
+              tmem_cp_128x256b(tmem + q_col0 + j * kQTmemCols + k * 8,
+                               stage + (((k >> 2) * C::kKbBytes + (k & 3) * 32) >> 4));
             mma_commit(&q_empty[qs]);  // staging buffer free once the copy is done
             issued = true;
             ++qc;
@@ -302,33 +345,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = it.t0; t < it.t1 && ok; ++t) {
           const int ks = kcount % kst;
           if (!(ok = mbar_wait(&k_full[ks], (kcount / kst) & 1, abort_flag, status))) break;
-          const uint32_t k_base = smem_u32(sK + ks * C::kTileBytes);
+          const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + ks * C::kTileBytes), C::kKGroup);
           for (int j = 0; j < it.J; ++j) {
-            const uint32_t w = jc & 1;
-            const uint32_t slot = w * NBW + (cnt[w] % NBW);
-            const uint32_t use = cnt[w] / NBW;
             if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status))) break;
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem + slot * SLOT_COLS;
-            const uint32_t sub_base = q_base + j * sub_bytes;
+            const uint32_t d_tmem = tmem + slot * slot_cols;
+            if (PASS == 1) {
+              const uint32_t a_tmem = tmem + q_col0 + j * kQTmemCols;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t koff_k = (k >> 2) * C::kKbBytes + (k & 3) * 32;
-              const uint32_t koff_q = (k >> 2) * (uint32_t)(sub_rows * 128) + (k & 3) * 32;
-              if (PASS == 1)
-                mma_bf16_tmem_a(d_tmem, tmem + kQTmemCol + j * kQTmemCols + k * 8,
-                                sdesc_k_sw128(k_base + koff_k), idesc, k > 0);
-              else
-                mma_bf16(d_tmem, sdesc_k_sw128(k_base + koff_k), sdesc_k_sw128(sub_base + koff_q), idesc,
-                         k > 0);
+              for (int k = 0; k < D / 16; ++k)
+                mma_bf16_tmem_a(d_tmem, a_tmem + k * 8, k_desc + (((k >> 2) * 1024 + (k & 3) * 32) >> 4),
+                                idesc, k > 0);
+            } else {
+              const uint64_t qj = q_desc + ((j * sub_bytes) >> 4);
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k)
+                mma_bf16(d_tmem, k_desc + (((k >> 2) * 1024 + (k & 3) * 32) >> 4),
+                         qj + (k >> 2) * q_kb_step + (k & 3) * 2, idesc, k > 0);
             }
             mma_commit(&t_full[slot]);
             if (PASS == 2 && t == it.t1 - 1) mma_commit(&q_empty[j]);  // last use of this Q sub-tile
             issued = true;
             last_slot = slot;
             last_use = use;
-            ++cnt[w];
-            ++jc;
+            if (++slot == nslots) {
+              slot = 0;
+              ++use;
+            }
           }
           if (!ok) break;
           mma_commit(&k_empty[ks]);
@@ -346,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = sub * 32 + lane;  // TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(sub * 32) << 16);
     const float c = meta.scale * kLog2e;
-    uint32_t cnt = 0, jc = 0, tiles_done = 0;
+    uint32_t jc = 0, tiles_done = 0;
+    uint32_t slot = 0, use = 0;  // accumulator slot of job jc and its use count
     bool ok = true;
     for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
       const Item it = decode_item(meta, item, total_sub);
@@ -362,24 +406,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         bool mine = false;
 #pragma unroll 1
-        for (int j = 0; j < it.J; ++j, ++jc) {
+        for (int j = 0; j < it.J; ++j, ++jc, slot = (slot + 1 == nslots) ? 0 : slot + 1,
+                 use += (slot == 0)) {
           if ((int)(jc & 1) != wg) continue;
           mine = true;
-          const uint32_t slot = wg * NBW + (cnt % NBW);
-          const uint32_t use = cnt / NBW;
           ok = mbar_wait(&t_full[slot], use & 1, abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t taddr = t_lane + slot * SLOT_COLS;
-          ++cnt;
+          const uint32_t taddr = t_lane + slot * slot_cols;
           float v[128];
           if (PASS == 1) {
             tmem_ld128(taddr, v);
             tc_fence_before_sync();
-            mbar_arrive(&t_empty[slot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&t_empty[slot]);  // the warp's 32 TMEM lanes are read
             if (valid < kTile) {
 #pragma unroll
               for (int jj = 0; jj < kTile; ++jj)
@@ -401,21 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sprev = s_run[q];
               }
             const float mnew = fmaxf(mprev, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
-            const float2 cc = make_float2(c, c), nm = make_float2(-mnew, -mnew);
-            float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll
-            for (int jj = 0; jj < kTile; jj += 8) {
-              const float2 x0 = __ffma2_rn(make_float2(v[jj + 0], v[jj + 1]), cc, nm);
-              const float2 x1 = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), cc, nm);
-              const float2 x2 = __ffma2_rn(make_float2(v[jj + 4], v[jj + 5]), cc, nm);
-              const float2 x3 = __ffma2_rn(make_float2(v[jj + 6], v[jj + 7]), cc, nm);
-              a0 = __fadd2_rn(a0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
-              a1 = __fadd2_rn(a1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
-              a2 = __fadd2_rn(a2, make_float2(ex2_approx(x2.x), ex2_approx(x2.y)));
-              a3 = __fadd2_rn(a3, make_float2(ex2_approx(x3.x), ex2_approx(x3.y)));
-            }
-            const float2 s01 = __fadd2_rn(a0, a1), s23 = __fadd2_rn(a2, a3);
-            const float tile_sum = (s01.x + s01.y) + (s23.x + s23.y);
+            const float tile_sum = tile_exp2_sum(v, c, mnew);
             const float snew = fmaf(sprev, ex2_approx(mprev - mnew), tile_sum);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -430,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld128(taddr + col0, v);
               if (col0 + 128 >= meta.W) {
                 tc_fence_before_sync();
-                mbar_arrive(&t_empty[slot]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&t_empty[slot]);
               }
               const int ncol = min(128, meta.W - col0);
               if (ncol == 128) {

@@ -221,6 +221,24 @@ def test_logical_view_after_compaction():
                 assert np.array_equal(np.array([e[2] for e in live]).reshape(Vc.shape), Vc)
 
 
+@pytest.mark.parametrize("d,R", [(128, 128), (128, 512), (64, 256)])
+def test_rising_logits(d, R):
+    """Key norms grow along the sequence (x1 at slot 0 to x24 at the end), so each row's
+    largest logits sit in the last tiles, far above every earlier tile: the LSE pass
+    must move its running reference up mid-item without overflowing or losing mass."""
+    sp = workloads.custom(L=1, H=2, G=4, d=d, P=16, q=R // 4, lengths=(3000, 1300),
+                          budget=("ratio", 0.2), shuffle_pages=True)
+    case = workloads.build(sp, 7, DEV)
+    P = sp.P
+    for b, n in enumerate(sp.lengths):
+        slots = torch.arange(n, device=DEV)
+        pages = case.block_table[b].long()[slots // P]
+        grow = (1.0 + 23.0 * slots.float() / max(1, n - 1)).view(-1, 1, 1, 1)
+        view = case.k_pool.permute(1, 3, 0, 2, 4)
+        view[pages, slots % P] = (view[pages, slots % P].float() * grow).to(torch.bfloat16)
+    full_check(case, f"rising logits d={d} R={R}")
+
+
 @pytest.mark.parametrize("distinct", [1, 3])
 def test_exact_ties_keep_lowest_positions(distinct):
     """Keys drawn from `distinct` vectors: scores tie exactly on both sides, and the lower
