@@ -13,7 +13,9 @@
 //               table with 2-D TMA (the block-table entries arrive kPageRing - 1
 //               tiles ahead through cp.async)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2..9  two epilogue warpgroups; they take the MMA jobs alternately
+//   warps 2, 3  idle (they complete warpgroup 0, which hands its registers to
+//               the epilogue through setmaxnreg)
+//   warps 4..11 two epilogue warpgroups; they take the MMA jobs alternately
 //               and drain the TMEM accumulator slots round robin
 // A work item is (unit, row group, key range).  Each K tile yields one MMA job
 // per 128-row tile (pass 1) or per W-row chunk (pass 2) of the group.
@@ -46,7 +48,16 @@ namespace {
 constexpr int kTile = 128;          // keys per K tile, rows per Q tile
 constexpr float kBias = 100.0f;     // alpha^2 is accumulated as alpha^2 * 2^kBias
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;       // producer, MMA, 2 x 4 epilogue warps
+// 12 warps: warpgroup 0 = producer, MMA issuer and two idle warps; warpgroups
+// 1 and 2 = epilogue.  After the start-up barrier warpgroup 0 gives registers
+// to the epilogue: 4 x 32 x kRegsControl + 8 x 32 x kRegsEpilogue equals the
+// launch allocation of 384 threads x kRegsLaunch (the host checks the kernel
+// was built with kRegsLaunch registers before the first launch).
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 72;
+constexpr int kRegsEpilogue = 216;
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue == kThreads * kRegsLaunch, "register split");
 constexpr int kMaxKStages = 8;
 constexpr int kPageRing = 8;        // key tiles whose block-table entries are in flight
 constexpr int kPagesPerTileMax = 16; // 128 keys in pages of >= 8 slots
@@ -119,6 +130,28 @@ __device__ __forceinline__ float tile_exp2_sum(const float (&v)[kTile], float c,
   return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
+// Pass-2 accumulation over up to 128 columns of a key's TMEM row:
+// acc += sum_col 2^(2c L_col + nob_col) for the first min(ncol, 128) columns
+// (ncol a multiple of 8; ob 32-byte aligned, read 8 offsets per load).
+__device__ __forceinline__ void alpha2_cols(const float (&v)[128], const float* __restrict__ ob, int ncol,
+                                            float2 c2, float2 (&acc2)[2]) {
+#pragma unroll
+  for (int jj = 0; jj < 128; jj += 8) {
+    if (ncol >= 128 || jj < ncol) {
+      float o[8];
+      ldg_nc_v8(ob + jj, o);
+      const float2 x0 = __ffma2_rn(make_float2(v[jj + 0], v[jj + 1]), c2, make_float2(o[0], o[1]));
+      const float2 x1 = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), c2, make_float2(o[2], o[3]));
+      const float2 x2 = __ffma2_rn(make_float2(v[jj + 4], v[jj + 5]), c2, make_float2(o[4], o[5]));
+      const float2 x3 = __ffma2_rn(make_float2(v[jj + 6], v[jj + 7]), c2, make_float2(o[6], o[7]));
+      acc2[0] = __fadd2_rn(acc2[0], make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
+      acc2[1] = __fadd2_rn(acc2[1], make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
+      acc2[0] = __fadd2_rn(acc2[0], make_float2(ex2_approx(x2.x), ex2_approx(x2.y)));
+      acc2[1] = __fadd2_rn(acc2[1], make_float2(ex2_approx(x3.x), ex2_approx(x3.y)));
+    }
+  }
+}
+
 // ============================================================== skeleton
 
 // PASS 1: A = Q row tile (M = 128 rows) read from TMEM, B = K tile (N = 128
@@ -161,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* t_full = k_empty + kMaxKStages;  // [4] TMEM slots
   uint64_t* t_empty = t_full + 4;
   uint64_t* drain = t_empty + 4;         // pass 1: all MMAs of the previous item done
+  uint64_t* red_full = drain + 1;        // [2] pass 2: a tile's other share is in `red`
+  uint64_t* red_empty = red_full + 2;    // [2] pass 2: `red` may be written again
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 384);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(smem_raw + 512);           // [2 parity][128] (pass 2)
@@ -175,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < 4; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 4); }  // 4 warps
     mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&red_full[i], 4); mbar_init(&red_empty[i], 4); }  // 4 warps
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
@@ -189,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ---------------------------------------------------------- producer (whole warp)
     // Load order per item: its first min(kst-1, tiles) K tiles, then its Q group
@@ -382,14 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && issued)  // the last commit covers every MMA issued
         mbar_wait(&t_full[last_slot], last_use & 1, nullptr, status);
     }
+  }  // warps 2 and 3: nothing to do
   } else {
+    setmaxnreg_inc<kRegsEpilogue>();
     // ---------------------------------------------------------- epilogue warpgroups
-    const int wg = (warp - 2) >> 2;
-    const int sub = warp & 3;
+    const int wg = (warp - 4) >> 2;
+    const int sub = warp & 3;  // TMEM lane quarter this warp may access
     const int r = sub * 32 + lane;  // TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(sub * 32) << 16);
     const float c = meta.scale * kLog2e;
-    uint32_t jc = 0, tiles_done = 0;
+    uint32_t jc = 0, red_count = 0;
     uint32_t slot = 0, use = 0;  // accumulator slot of job jc and its use count
     bool ok = true;
     for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
@@ -401,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_run[j] = 0.0f;
       }
       const int64_t u = ((int64_t)it.u.b * meta.L + it.u.l) * meta.H + it.u.h;
-      for (int t = it.t0; t < it.t1 && ok; ++t, ++tiles_done) {
+      for (int t = it.t0; t < it.t1 && ok; ++t) {
         const int valid = min(kTile, it.u.n - t * kTile);
         float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         bool mine = false;
@@ -462,28 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&t_empty[slot]);
               }
-              const int ncol = min(128, meta.W - col0);
-              if (ncol == 128) {
-#pragma unroll
-                for (int jj = 0; jj < 128; jj += 4) {
-                  const float4 o = __ldg(reinterpret_cast<const float4*>(ob + col0 + jj));
-                  const float2 x0 = __ffma2_rn(make_float2(v[jj + 0], v[jj + 1]), c2, make_float2(o.x, o.y));
-                  const float2 x1 = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), c2, make_float2(o.z, o.w));
-                  acc2[0] = __fadd2_rn(acc2[0], make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
-                  acc2[1] = __fadd2_rn(acc2[1], make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
-                }
-              } else {
-#pragma unroll
-                for (int jj = 0; jj < 128; jj += 4) {
-                  if (jj < ncol) {
-                    const float4 o = __ldg(reinterpret_cast<const float4*>(ob + col0 + jj));
-                    const float2 x0 = __ffma2_rn(make_float2(v[jj + 0], v[jj + 1]), c2, make_float2(o.x, o.y));
-                    const float2 x1 = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), c2, make_float2(o.z, o.w));
-                    acc2[0] = __fadd2_rn(acc2[0], make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
-                    acc2[1] = __fadd2_rn(acc2[1], make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
-                  }
-                }
-              }
+              alpha2_cols(v, ob + col0, meta.W - col0, c2, acc2);
             }
           }
         }
@@ -492,12 +511,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 s2 = __fadd2_rn(acc2[0], acc2[1]);
           float acc = s2.x + s2.y;
           bool writer = mine;
-          if (it.J > 1) {  // both warpgroups hold a share of this tile's rows
-            float* rb = red + (tiles_done & 1) * kTile;
-            writer = (wg == (int)(tiles_done & 1));
-            if (!writer) rb[r] = acc;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (writer) acc += rb[r];
+          if (it.J > 1) {
+            // Both warpgroups hold a share of this tile's rows.  The one that
+            // drained the tile's last job (usually the later one) adds the
+            // other's share from `red` and writes the score; the other never
+            // waits except for `red` to be free again, two tiles later.
+            const uint32_t par = red_count & 1, use = red_count >> 1;
+            ++red_count;
+            float* rb = red + par * kTile;
+            writer = (wg == (int)((jc - 1) & 1));
+            if (!writer) {
+              ok = mbar_wait(&red_empty[par], (use & 1) ^ 1, abort_flag, status);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+              rb[r] = acc;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&red_full[par]);
+            } else {
+              ok = mbar_wait(&red_full[par], use & 1, abort_flag, status);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+              acc += rb[r];
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&red_empty[par]);
+            }
           }
           const int key = t * kTile + r;
           if (writer && key < it.u.n) {
@@ -609,6 +650,12 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
+    // the register split inside the kernel assumes this launch allocation; a
+    // build with any other count is refused rather than launched
+    cudaFuncAttributes fa1, fa2;
+    if ((e = cudaFuncGetAttributes(&fa1, score_pass_kernel<D, 1>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa2, score_pass_kernel<D, 2>)) != cudaSuccess) return e;
+    if (fa1.numRegs != kRegsLaunch || fa2.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(score_pass_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kScoreSmemLimit);
     if (e != cudaSuccess) return e;
