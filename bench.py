@@ -366,11 +366,21 @@ def our_arm(args):
     dom_kernel = ("score_pass_kernel<128,2> (alpha pass)" if dom == "score_alpha"
                   else "score_pass_kernel<128,1> (LSE pass)")
     t_dom = per_stage[dom] * 1e-3
-    achieved = F_alg / t_dom / 1e12
-    roofline = {"bound": "tensor", "kernel": dom_kernel, "achieved": achieved,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "traffic": profile_traffic(dom_kernel, sp.name), "peak_source": pk["source"],
-                "algorithmic_flops_per_launch": F_alg}
+    # a pass reads every K row once and its Q group(s); the alpha pass also writes the scores.
+    # The pass is bound by whichever of its flops (at the bf16 peak) or bytes (at the copy
+    # peak) takes longer.
+    B_pass = 2.0 * d * entries + 2.0 * R * d * units + (4.0 * entries if dom == "score_alpha" else 0.0)
+    if F_alg / (pk["bf16_tflops"] * 1e12) >= B_pass / (pk["hbm_gbs"] * 1e9):
+        achieved = F_alg / t_dom / 1e12
+        roofline = {"bound": "tensor", "kernel": dom_kernel, "achieved": achieved,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"]}
+    else:
+        achieved = B_pass / t_dom / 1e9
+        roofline = {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved,
+                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                    "tensor_frac": F_alg / t_dom / 1e12 / pk["bf16_tflops"]}
+    roofline.update({"traffic": profile_traffic(dom_kernel, sp.name), "peak_source": pk["source"],
+                     "algorithmic_flops_per_launch": F_alg, "algorithmic_bytes_per_launch": B_pass})
     compact_bytes = moves * 8.0 * d + 4.0 * moves
     gbs = compact_bytes / (per_stage["compact"] * 1e-3) / 1e9 if per_stage["compact"] > 0 else 0.0
 
