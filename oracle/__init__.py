@@ -16,7 +16,10 @@ function cites the page passage it restates:
 * compact / free -- the ActKV conflict-free tail-region slot plan, simulated
   sequentially, and the return of the emptied blocks to the allocator;
 * logical view -- the order-preserving out-of-place view (Chain Cache's
-  logical-vs-physical split on the SparseEngine page).
+  logical-vs-physical split on the SparseEngine page);
+* sentinel eviction / fresh-page compaction -- the layout-preserving dead
+  slot (K = -10^4, V = 0) of the IntentKV page, and an order-preserving
+  compaction into freshly allocated pages.
 
 Parity status: the score, selection and compaction functions are pinned by the
 tests under ``tests/test_oracle_*.py`` (closed forms, invariants, brute force
@@ -82,6 +85,16 @@ def _load():
         lib.oracle_free_blocks.restype = I
         lib.oracle_logical_view.argtypes = [P, P, P, I, I, I, I, I, I, P, I, P, I, P, P, P]
         lib.oracle_logical_view.restype = I
+        lib.oracle_sentinel_k_bits.argtypes = []
+        lib.oracle_sentinel_k_bits.restype = ctypes.c_uint16
+        lib.oracle_evict_sentinel.argtypes = [P, P, P, I, I, I, I, I, I, I, P, I, P, P, I, P, P]
+        lib.oracle_evict_sentinel.restype = I
+        lib.oracle_fresh_pages.argtypes = [P, ctypes.c_int32, I, P, P, I, P, P, P]
+        lib.oracle_fresh_pages.restype = I
+        lib.oracle_compact_fresh.argtypes = [P, P, P, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
+        lib.oracle_compact_fresh.restype = I
+        lib.oracle_commit_fresh.argtypes = [P, P, I, P, P, I, I, P, P, I, P, P]
+        lib.oracle_commit_fresh.restype = I
         _lib = lib
         return lib
 
@@ -263,6 +276,84 @@ def logical_view(k_pool: np.ndarray, v_pool: np.ndarray, tags: np.ndarray, layer
                                      _ptr(Kc), _ptr(Vc), _ptr(pos))
     _check(st, "logical_view")
     return Kc[:m], Vc[:m], pos[:m]
+
+
+# --------------------------------------------------------------------------- layout variants
+
+def sentinel_k_bits() -> int:
+    """bf16 bit pattern of the sentinel key element, bf16(-10^4)."""
+    return int(_load().oracle_sentinel_k_bits())
+
+
+def _pool_args(k_pool, v_pool, tags):
+    for a, dt in ((k_pool, np.uint16), (v_pool, np.uint16), (tags, np.int32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise TypeError("pool slices must be contiguous uint16 / int32 arrays")
+    return k_pool.shape
+
+
+def evict_sentinel(k_pool: np.ndarray, v_pool: np.ndarray, tags: np.ndarray, layer_lo: int,
+                   L_total: int, block_table, seg_start, seg_end, m, keep: np.ndarray):
+    """In place: every evicted position of every unit becomes a sentinel dead slot."""
+    Lpart, num_pages, H, P, d = _pool_args(k_pool, v_pool, tags)
+    bt = _i32(block_table)
+    keep = _c(keep, np.int32)
+    if keep.size == 0:
+        keep = np.zeros(1, np.int32)
+    s0, s1, mm = _i32(seg_start), _i32(seg_end), _i32(m)
+    st = _load().oracle_evict_sentinel(_ptr(k_pool), _ptr(v_pool), _ptr(tags), int(layer_lo), Lpart,
+                                       int(L_total), num_pages, H, P, d, _ptr(bt), bt.shape[1],
+                                       _ptr(s0), _ptr(s1), len(s0), _ptr(mm), _ptr(keep))
+    _check(st, "evict_sentinel")
+
+
+def fresh_pages(free_ids: np.ndarray, free_top: int, P: int, seg_start, seg_end, m) -> np.ndarray:
+    """Pages the fresh-page compaction pops, in pop order (sequences ascending)."""
+    fi = _i32(free_ids)
+    s0, s1, mm = _i32(seg_start), _i32(seg_end), _i32(m)
+    count = np.zeros(1, np.int32)
+    lib = _load()
+    _check(lib.oracle_fresh_pages(_ptr(fi), int(free_top), int(P), _ptr(s0), _ptr(s1), len(s0),
+                                  _ptr(mm), None, _ptr(count)), "fresh_pages")
+    out = np.zeros(max(1, int(count[0])), np.int32)
+    _check(lib.oracle_fresh_pages(_ptr(fi), int(free_top), int(P), _ptr(s0), _ptr(s1), len(s0),
+                                  _ptr(mm), _ptr(out), _ptr(count)), "fresh_pages")
+    return out[:int(count[0])]
+
+
+def compact_fresh(k_pool: np.ndarray, v_pool: np.ndarray, tags: np.ndarray, layer_lo: int,
+                  L_total: int, block_table, seg_start, seg_end, m, keep: np.ndarray,
+                  fresh: np.ndarray):
+    """In place: survivors of active sequences copied, in order, into their fresh pages."""
+    Lpart, num_pages, H, P, d = _pool_args(k_pool, v_pool, tags)
+    bt = _i32(block_table)
+    keep = _c(keep, np.int32)
+    if keep.size == 0:
+        keep = np.zeros(1, np.int32)
+    fr = _c(fresh, np.int32)
+    if fr.size == 0:
+        fr = np.zeros(1, np.int32)
+    s0, s1, mm = _i32(seg_start), _i32(seg_end), _i32(m)
+    st = _load().oracle_compact_fresh(_ptr(k_pool), _ptr(v_pool), _ptr(tags), int(layer_lo), Lpart,
+                                      int(L_total), num_pages, H, P, d, _ptr(bt), bt.shape[1],
+                                      _ptr(s0), _ptr(s1), len(s0), _ptr(mm), _ptr(keep), _ptr(fr))
+    _check(st, "compact_fresh")
+
+
+def commit_fresh(block_table: np.ndarray, nblocks: np.ndarray, free_ids: np.ndarray,
+                 free_top: np.ndarray, P: int, seg_start, seg_end, m, fresh: np.ndarray):
+    """In place: pops the fresh pages, returns the old ones, installs the new rows."""
+    for a in (block_table, nblocks, free_ids, free_top):
+        if a.dtype != np.int32 or not a.flags.c_contiguous:
+            raise TypeError("allocator state must be contiguous int32 arrays")
+    fr = _c(fresh, np.int32)
+    if fr.size == 0:
+        fr = np.zeros(1, np.int32)
+    s0, s1, mm = _i32(seg_start), _i32(seg_end), _i32(m)
+    st = _load().oracle_commit_fresh(_ptr(block_table), _ptr(nblocks), block_table.shape[1],
+                                     _ptr(free_ids), _ptr(free_top), free_ids.shape[0], int(P),
+                                     _ptr(s0), _ptr(s1), len(s0), _ptr(mm), _ptr(fr))
+    _check(st, "commit_fresh")
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -463,3 +463,207 @@ int oracle_logical_view(const uint16_t *k_pool, const uint16_t *v_pool, const in
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Layout-preserving eviction and order-preserving fresh-page compaction.    */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 bit pattern nearest to x (round to nearest, ties to even), finite x. */
+static uint16_t bf16_bits_nearest(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+/* The sentinel key element of a dead slot, bf16(-10^4) [IK]. */
+uint16_t oracle_sentinel_k_bits(void) { return bf16_bits_nearest(-1.0e4); }
+
+/* Checks a unit's keep list (ascending, inside [0, n)) and marks it. */
+static int mark_kept(const int32_t *ku, int mb, int n, uint8_t *kept)
+{
+    for (int r = 0; r < mb; ++r) {
+        if (ku[r] < 0 || ku[r] >= n || (r > 0 && ku[r] <= ku[r - 1])) return ORC_ERR_ARG;
+        kept[ku[r]] = 1;
+    }
+    return ORC_OK;
+}
+
+/* Layout-preserving eviction ("IntentKV: Cross-Turn Intent-Aware KV Cache
+ * Pruning", section on layout-preserving eviction): an evicted position is
+ * turned into a dead slot whose K/V are constants that remove its attention
+ * contribution (K = -10^4, V = 0) while every retained entry keeps its
+ * physical slot.  Reading: each of the d key elements of an evicted position
+ * becomes bf16(-10^4), each value element +0, its tag -1; retained entries,
+ * slots past the segment end, the block table and the allocator are left as
+ * they are (no page is freed).  Pool slices hold layers
+ * [layer_lo, layer_lo + Lpart); keep is [L_total][H][Mtot]. */
+int oracle_evict_sentinel(uint16_t *k_pool, uint16_t *v_pool, int32_t *tags, int layer_lo,
+                          int Lpart, int L_total, int num_pages, int H, int P, int d,
+                          const int32_t *block_table, int max_blocks, const int32_t *seg_start,
+                          const int32_t *seg_end, int B, const int32_t *m, const int32_t *keep)
+{
+    if (!k_pool || !v_pool || !tags || !block_table || !seg_start || !seg_end || !m || !keep ||
+        Lpart <= 0 || layer_lo < 0 || layer_lo + Lpart > L_total || H <= 0 || P <= 0 || d <= 0)
+        return ORC_ERR_ARG;
+    const uint16_t ks = oracle_sentinel_k_bits();
+    int64_t Mtot = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = seg_end[b] - seg_start[b];
+        Mtot += (m[b] < n ? m[b] : n);
+    }
+    for (int lp = 0; lp < Lpart; ++lp) {
+        int l = layer_lo + lp;
+        for (int h = 0; h < H; ++h) {
+            int64_t moff = 0;
+            for (int b = 0; b < B; ++b) {
+                int s0 = seg_start[b], n = seg_end[b] - seg_start[b];
+                int mb = m[b] < n ? m[b] : n;
+                const int32_t *ku = keep + ((int64_t)l * H + h) * Mtot + moff;
+                moff += mb;
+                if (n == 0) continue;
+                const int32_t *bt_row = block_table + (size_t)b * max_blocks;
+                uint8_t *kept = (uint8_t *)calloc((size_t)n, 1);
+                if (!kept) return ORC_ERR_NOMEM;
+                if (mark_kept(ku, mb, n, kept) != ORC_OK) {
+                    free(kept);
+                    return ORC_ERR_ARG;
+                }
+                for (int t = 0; t < n; ++t) {
+                    if (kept[t]) continue;
+                    size_t e = pool_elem(bt_row, s0 + t, lp, h, num_pages, H, P, d);
+                    for (int c = 0; c < d; ++c) {
+                        k_pool[e + c] = ks;
+                        v_pool[e + c] = 0;
+                    }
+                    tags[tag_elem(bt_row, s0 + t, lp, h, num_pages, H, P)] = -1;
+                }
+                free(kept);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* Order-preserving compaction into fresh pages (the order objection of the
+ * IntentKV page, met by moving survivors instead of renumbering them in
+ * place).  Reading: a sequence whose segment keeps fewer than all of its n
+ * positions ("active") takes X = ceil(m/P) fresh pages from the free stack;
+ * the pops of all active sequences, in ascending sequence order, come before
+ * any page is returned.  This function lists them: fresh[k] is the page the
+ * k-th pop hands out, free_ids[top - 1 - k].  Writes the count to *count;
+ * fails if the stack holds fewer pages. */
+int oracle_fresh_pages(const int32_t *free_ids, int32_t free_top, int P, const int32_t *seg_start,
+                       const int32_t *seg_end, int B, const int32_t *m, int32_t *fresh,
+                       int32_t *count)
+{
+    if (!free_ids || !seg_start || !seg_end || !m || !count || P <= 0 || B <= 0) return ORC_ERR_ARG;
+    int32_t k = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = seg_end[b] - seg_start[b];
+        int mb = m[b] < n ? m[b] : n;
+        if (n == 0 || mb == n) continue;
+        int X = (int)ceil_div(mb, P);
+        for (int x = 0; x < X; ++x, ++k) {
+            if (free_top - 1 - k < 0) return ORC_ERR_STACK;
+            if (fresh) fresh[k] = free_ids[free_top - 1 - k];
+        }
+    }
+    *count = k;
+    return ORC_OK;
+}
+
+/* The copy of the fresh-page compaction: in every unit of an active
+ * sequence the r-th retained position (ascending) goes to slot r of the
+ * sequence's fresh pages (page fresh[xoff + r / P], offset r % P) with its K
+ * bytes, V bytes and tag; slots r = m .. X*P-1 of the last fresh page get tag
+ * -1, bytes untouched.  Sources are read through the old block table; fresh
+ * pages are disjoint from every mapped page, so the order of copies does not
+ * matter.  Inactive sequences (m = n) are left alone. */
+int oracle_compact_fresh(uint16_t *k_pool, uint16_t *v_pool, int32_t *tags, int layer_lo,
+                         int Lpart, int L_total, int num_pages, int H, int P, int d,
+                         const int32_t *block_table, int max_blocks, const int32_t *seg_start,
+                         const int32_t *seg_end, int B, const int32_t *m, const int32_t *keep,
+                         const int32_t *fresh)
+{
+    if (!k_pool || !v_pool || !tags || !block_table || !seg_start || !seg_end || !m || !keep ||
+        !fresh || Lpart <= 0 || layer_lo < 0 || layer_lo + Lpart > L_total || H <= 0 || P <= 0 ||
+        d <= 0)
+        return ORC_ERR_ARG;
+    int64_t Mtot = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = seg_end[b] - seg_start[b];
+        Mtot += (m[b] < n ? m[b] : n);
+    }
+    for (int lp = 0; lp < Lpart; ++lp) {
+        int l = layer_lo + lp;
+        for (int h = 0; h < H; ++h) {
+            int64_t moff = 0;
+            int xoff = 0;
+            for (int b = 0; b < B; ++b) {
+                int s0 = seg_start[b], n = seg_end[b] - seg_start[b];
+                int mb = m[b] < n ? m[b] : n;
+                const int32_t *ku = keep + ((int64_t)l * H + h) * Mtot + moff;
+                moff += mb;
+                if (n == 0 || mb == n) continue;
+                int X = (int)ceil_div(mb, P);
+                const int32_t *bt_row = block_table + (size_t)b * max_blocks;
+                for (int r = 0; r < mb; ++r)
+                    if (ku[r] < 0 || ku[r] >= n || (r > 0 && ku[r] <= ku[r - 1])) return ORC_ERR_ARG;
+                for (int r = 0; r < X * P; ++r) {
+                    int page = fresh[xoff + r / P];
+                    size_t dt = (((size_t)lp * num_pages + (size_t)page) * H + h) * P + (size_t)(r % P);
+                    if (r < mb) {
+                        size_t se = pool_elem(bt_row, s0 + ku[r], lp, h, num_pages, H, P, d);
+                        memcpy(k_pool + dt * d, k_pool + se, (size_t)d * sizeof(uint16_t));
+                        memcpy(v_pool + dt * d, v_pool + se, (size_t)d * sizeof(uint16_t));
+                        tags[dt] = tags[tag_elem(bt_row, s0 + ku[r], lp, h, num_pages, H, P)];
+                    } else {
+                        tags[dt] = -1;
+                    }
+                }
+                xoff += X;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* The bookkeeping of the fresh-page compaction: the stack loses the popped
+ * pages (top -= sum X), then every active sequence, in ascending order,
+ * returns all nb blocks of its old segment in ascending block order; in its
+ * block-table row the segment's nb entries are replaced by its X fresh
+ * pages, later entries shift down by nb - X, vacated tail entries become -1
+ * and nblocks drops by nb - X.  `fresh` is the list of oracle_fresh_pages. */
+int oracle_commit_fresh(int32_t *block_table, int32_t *nblocks, int max_blocks, int32_t *free_ids,
+                        int32_t *free_top, int capacity, int P, const int32_t *seg_start,
+                        const int32_t *seg_end, int B, const int32_t *m, const int32_t *fresh)
+{
+    if (!block_table || !nblocks || !free_ids || !free_top || !seg_start || !seg_end || !m ||
+        P <= 0 || B <= 0)
+        return ORC_ERR_ARG;
+    int32_t count = 0;
+    int st = oracle_fresh_pages(free_ids, *free_top, P, seg_start, seg_end, B, m, NULL, &count);
+    if (st != ORC_OK) return st;
+    if (count > 0 && !fresh) return ORC_ERR_ARG;
+    *free_top -= count;
+    int xoff = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = seg_end[b] - seg_start[b];
+        int mb = m[b] < n ? m[b] : n;
+        if (n == 0 || mb == n) continue;
+        int nb = (int)ceil_div(n, P), X = (int)ceil_div(mb, P), sb = seg_start[b] / P;
+        int32_t *row = block_table + (size_t)b * max_blocks;
+        if (*free_top + nb > capacity) return ORC_ERR_STACK;
+        for (int i = 0; i < nb; ++i) free_ids[(*free_top)++] = row[sb + i];
+        int old = nblocks[b], f = nb - X;
+        for (int x = 0; x < X; ++x) row[sb + x] = fresh[xoff + x];
+        for (int i = sb + X; i < old - f; ++i) row[i] = row[i + f];
+        for (int i = old - f; i < old; ++i) row[i] = -1;
+        nblocks[b] = old - f;
+        xoff += X;
+    }
+    return ORC_OK;
+}
