@@ -78,7 +78,7 @@ typedef int32_t kvc_status;
 
 /* Device status word bits (kvc_read_device_status). */
 #define KVC_DEV_WAIT_TIMEOUT 1u /* a bounded pipeline wait gave up           */
-#define KVC_DEV_FREE_STACK 2u   /* free stack would overflow its capacity   */
+#define KVC_DEV_FREE_STACK 2u   /* free stack too full (push) or too empty (fresh-page pop) */
 #define KVC_DEV_BAD_PAGE 4u     /* a block-table entry was outside the pool */
 #define KVC_DEV_BAD_KEEP 8u     /* a keep position was outside its segment   */
 
@@ -276,6 +276,54 @@ kvc_status kvc_compact(const kvc_cache *cache, const kvc_segments *segs, const i
  * KVC_DEV_FREE_STACK and pushes nothing. */
 kvc_status kvc_free_pages(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                           const kvc_allocator *alloc, const kvc_plan *plan, kvc_stream_t stream);
+
+/* ------------------------------------------------- layout variants of eviction */
+
+/* Layout-preserving eviction ("IntentKV: Cross-Turn Intent-Aware KV Cache
+ * Pruning", section on layout-preserving eviction: an evicted position is
+ * redirected to a sentinel dead slot with K = -10^4, V = 0, and surviving
+ * rows keep their slots).  Every position of each segment that is not in
+ * keep (the kvc_select_topm layout, ascending per unit) gets, in every
+ * (layer, KV head): each of its d key elements = bf16(-10^4) (bit pattern
+ * 0xC61C, value -9984), each value element = +0, tag = -1.  Retained
+ * entries, slots past the segment end, the block table and the allocator
+ * are untouched; no page is freed.  A keep entry outside [0, n) or out of
+ * ascending order sets KVC_DEV_BAD_KEEP.  Mutates k_pool, v_pool, tags. */
+kvc_status kvc_evict_sentinel(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                              const int32_t *keep, kvc_stream_t stream);
+
+/* Buffer sizes of the fresh-page plan: those of kvc_plan_buffer_sizes except
+ * freed_len = the sum of ceil(n_b/P) over sequences that keep fewer than all
+ * of their n_b positions. */
+kvc_status kvc_plan_fresh_buffer_sizes(const kvc_cache *cache, const kvc_segments *segs,
+                                       const int32_t *m, kvc_plan_sizes *out);
+
+/* Order-preserving compaction into fresh pages (an answer to the IntentKV
+ * page's objection that in-place compaction renumbers positions): a sequence
+ * keeping m_b < n_b positions takes X = ceil(m_b/P) pages from the free
+ * stack, in pop order (pop k of the call hands out free_ids[free_top-1-k];
+ * sequences ascending; every pop before any return), and in every unit its
+ * r-th retained position moves to slot r of those pages (page r / P, offset
+ * r % P), so physical order equals logical order; slots m_b .. X*P-1 of the
+ * last fresh page are dead (tag -1).  All nb old blocks of the segment are
+ * to be returned.  Fills *plan (moves, dead slots, the returned pages, the
+ * new rows) for kvc_compact and kvc_commit_fresh; reads the allocator and
+ * mutates nothing else.  A stack with fewer pages than the call pops sets
+ * KVC_DEV_FREE_STACK and plans no moves.  The allocator must not change
+ * between this call and kvc_commit_fresh. */
+kvc_status kvc_plan_fresh(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                          const int32_t *keep, const kvc_allocator *alloc, const kvc_plan *plan,
+                          kvc_stream_t stream);
+
+/* Bookkeeping of the fresh-page compaction, after kvc_compact on the same
+ * stream: pops the call's fresh pages, pushes every old block of the active
+ * segments (sequences ascending, blocks ascending), replaces each active
+ * segment's nb block-table entries by its X fresh pages (later entries shift
+ * down by nb - X, vacated entries become -1) and lowers nblocks[b] by
+ * nb - X.  If the device status word holds KVC_DEV_FREE_STACK (from the plan
+ * or from this step's own capacity check) it changes nothing. */
+kvc_status kvc_commit_fresh(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                            const kvc_allocator *alloc, const kvc_plan *plan, kvc_stream_t stream);
 
 /* -------------------------------------------------------------- helpers */
 

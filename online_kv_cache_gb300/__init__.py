@@ -44,7 +44,8 @@ EXPORTED = (
     "kvc_select_workspace_size", "kvc_select_topm", "kvc_plan_buffer_sizes", "kvc_plan_compact",
     "kvc_compact", "kvc_free_pages", "kvc_status_string", "kvc_last_error",
     "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
-    "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc",
+    "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc", "kvc_evict_sentinel",
+    "kvc_plan_fresh_buffer_sizes", "kvc_plan_fresh", "kvc_commit_fresh",
 )
 
 
@@ -134,6 +135,10 @@ def lib():
             "kvc_score_alpha": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
             "kvc_launch_count": (ctypes.c_uint64, [I32]),
             "kvc_score_noalloc": (I32, [C, SG, P, I32, F, P, P, P]),
+            "kvc_evict_sentinel": (I32, [C, SG, P, P, P]),
+            "kvc_plan_fresh_buffer_sizes": (I32, [C, SG, P, ctypes.POINTER(kvc_plan_sizes)]),
+            "kvc_plan_fresh": (I32, [C, SG, P, P, A, PL, P]),
+            "kvc_commit_fresh": (I32, [C, SG, P, A, PL, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -305,11 +310,20 @@ def kvc_plan_buffer_sizes(cache: Cache, segs: Segments, m) -> dict:
     return {name: int(getattr(out, name)) for name, _ in kvc_plan_sizes._fields_}
 
 
-class Plan:
-    """Caller-allocated plan buffers (device int32 tensors) for one (segments, budgets)."""
+def kvc_plan_fresh_buffer_sizes(cache: Cache, segs: Segments, m) -> dict:
+    mm = _host_i32(m)
+    out = kvc_plan_sizes()
+    _check(lib().kvc_plan_fresh_buffer_sizes(cache.ref, segs.ref, mm.ctypes.data, ctypes.byref(out)),
+           "kvc_plan_fresh_buffer_sizes")
+    return {name: int(getattr(out, name)) for name, _ in kvc_plan_sizes._fields_}
 
-    def __init__(self, cache: Cache, segs: Segments, m, device=None):
-        sizes = kvc_plan_buffer_sizes(cache, segs, m)
+
+class Plan:
+    """Caller-allocated plan buffers (device int32 tensors) for one (segments, budgets); with
+    fresh=True sized for the fresh-page compaction."""
+
+    def __init__(self, cache: Cache, segs: Segments, m, device=None, fresh: bool = False):
+        sizes = (kvc_plan_fresh_buffer_sizes if fresh else kvc_plan_buffer_sizes)(cache, segs, m)
         device = device or cache.tensors[0].device
         mk = lambda n: torch.empty(max(1, n), dtype=torch.int32, device=device)
         self.sizes = sizes
@@ -346,6 +360,26 @@ def kvc_free_pages(cache: Cache, segs: Segments, m, alloc: Allocator, plan: Plan
     mm = _host_i32(m)
     _check(lib().kvc_free_pages(cache.ref, segs.ref, mm.ctypes.data, alloc.ref, plan.ref,
                                 _stream(stream)), "kvc_free_pages")
+
+
+def kvc_evict_sentinel(cache: Cache, segs: Segments, m, keep: torch.Tensor, stream=None):
+    mm = _host_i32(m)
+    _check(lib().kvc_evict_sentinel(cache.ref, segs.ref, mm.ctypes.data,
+                                    _dev_ptr(keep, "keep", torch.int32), _stream(stream)),
+           "kvc_evict_sentinel")
+
+
+def kvc_plan_fresh(cache: Cache, segs: Segments, m, keep: torch.Tensor, alloc: Allocator, plan: Plan,
+                   stream=None):
+    mm = _host_i32(m)
+    _check(lib().kvc_plan_fresh(cache.ref, segs.ref, mm.ctypes.data, _dev_ptr(keep, "keep", torch.int32),
+                                alloc.ref, plan.ref, _stream(stream)), "kvc_plan_fresh")
+
+
+def kvc_commit_fresh(cache: Cache, segs: Segments, m, alloc: Allocator, plan: Plan, stream=None):
+    mm = _host_i32(m)
+    _check(lib().kvc_commit_fresh(cache.ref, segs.ref, mm.ctypes.data, alloc.ref, plan.ref,
+                                  _stream(stream)), "kvc_commit_fresh")
 
 
 def kvc_status_string(status: int) -> str:
@@ -427,8 +461,24 @@ class Compactor:
         kvc_plan_compact(self.cache, self.segs, self.m, self.keep if keep is None else keep,
                          self.plan, stream)
 
-    def compact(self, stream=None):
-        kvc_compact(self.cache, self.segs, self.m, self.plan, stream)
+    def compact(self, stream=None, plan: Optional[Plan] = None):
+        kvc_compact(self.cache, self.segs, self.m, self.plan if plan is None else plan, stream)
+
+    def evict_sentinel(self, keep: Optional[torch.Tensor] = None, stream=None):
+        """Layout-preserving eviction: sentinel dead slots, nothing moves or is freed."""
+        kvc_evict_sentinel(self.cache, self.segs, self.m, self.keep if keep is None else keep, stream)
+
+    def plan_fresh(self, keep: Optional[torch.Tensor] = None, stream=None) -> Plan:
+        """Plan of the order-preserving compaction into fresh pages (run it with compact(plan=...)
+        and finish with commit_fresh)."""
+        if getattr(self, "fresh_plan", None) is None:
+            self.fresh_plan = Plan(self.cache, self.segs, self.m, self.keep.device, fresh=True)
+        kvc_plan_fresh(self.cache, self.segs, self.m, self.keep if keep is None else keep, self.alloc,
+                       self.fresh_plan, stream)
+        return self.fresh_plan
+
+    def commit_fresh(self, stream=None):
+        kvc_commit_fresh(self.cache, self.segs, self.m, self.alloc, self.fresh_plan, stream)
 
     def free_pages(self, stream=None):
         kvc_free_pages(self.cache, self.segs, self.m, self.alloc, self.plan, stream)

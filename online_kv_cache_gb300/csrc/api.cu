@@ -833,6 +833,201 @@ kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, cons
   return ok();
 }
 
+// ------------------------------------------------------------- layout variants
+
+namespace {
+
+constexpr int kSentinelChunkHost = 4096;   // positions per sentinel block (layout.cu)
+constexpr int kFreshMovesHost = 1024;      // survivors per fresh-plan block (layout.cu)
+
+bool fresh_active(const Seq& q) { return q.m < q.n; }
+
+int64_t fresh_returned(const Plan& p) {
+  int64_t f = 0;
+  for (const Seq& q : p.seqs)
+    if (fresh_active(q)) f += q.nb;
+  return f;
+}
+
+kvc_status check_fresh_plan(const kvc_cache* cache, const Plan& p, const kvc_plan* plan) {
+  if (plan == nullptr) return fail(KVC_ERR_INVALID_ARG, "plan is NULL");
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  struct { const int32_t* ptr; int64_t have, need; const char* name; } bufs[] = {
+      {plan->moves, plan->moves_len, 2 * LH * p.Mtot, "moves"},
+      {plan->move_count, plan->units_len, LH * cache->batch, "move_count"},
+      {plan->dead, plan->dead_len, LH * cache->batch * cache->page_size, "dead"},
+      {plan->dead_count, plan->units_len, LH * cache->batch, "dead_count"},
+      {plan->freed, plan->freed_len, fresh_returned(p), "freed"},
+      {plan->new_rows, plan->new_rows_len, (int64_t)cache->batch * cache->max_blocks, "new_rows"},
+  };
+  for (const auto& b : bufs) {
+    if (b.need > 0 && (b.ptr == nullptr || b.have < b.need))
+      return fail(KVC_ERR_WORKSPACE, "fresh plan buffer %s needs %lld elements (have %lld)", b.name,
+                  (long long)b.need, (long long)b.have);
+  }
+  return KVC_OK;
+}
+
+// Metas of the fresh-page plan/commit: per-unit blocks (moves) and per-sequence
+// blocks (rows); the pop offsets (xoff) and return offsets (foff) run over
+// the whole call.
+void fresh_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta>* mv,
+                 std::vector<LaunchMeta>* rows) {
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  int64_t Xtot = 0;
+  for (const Seq& q : p.seqs)
+    if (fresh_active(q)) Xtot += q.X;
+  int64_t xoff = 0, foff = 0;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta a = base_meta(cache, p), r = base_meta(cache, p);
+    a.nseq = r.nseq = (int)(hi - lo);
+    a.Xtot = r.Xtot = Xtot;
+    int64_t it = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      const size_t j = i - lo;
+      fill_seq(&a.seq[j], p, i);
+      fill_seq(&r.seq[j], p, i);
+      const Seq& q = p.seqs[i];
+      a.seq[j].xoff = r.seq[j].xoff = (int32_t)xoff;
+      a.seq[j].foff = r.seq[j].foff = foff;
+      if (fresh_active(q)) {
+        xoff += q.X;
+        foff += q.nb;
+      }
+      a.seq[j].item0 = it;
+      it += LH * std::max<int64_t>(1, ceil_div(q.m, kFreshMovesHost));
+    }
+    a.items = it;
+    mv->push_back(a);
+    rows->push_back(r);
+  }
+}
+
+kvc_status check_allocator(const kvc_allocator* alloc) {
+  if (alloc == nullptr || alloc->free_ids == nullptr || alloc->free_top == nullptr || alloc->capacity < 0)
+    return fail(KVC_ERR_INVALID_ARG, "allocator is NULL or incomplete");
+  return KVC_OK;
+}
+
+}  // namespace
+
+kvc_status kvc_evict_sentinel(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                              const int32_t* keep, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedTags | kNeedBT);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  if (p.Mtot > 0 && keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  std::vector<LaunchMeta> metas;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta a = base_meta(cache, p);
+    a.nseq = (int)(hi - lo);
+    int64_t it = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      fill_seq(&a.seq[i - lo], p, i);
+      a.seq[i - lo].item0 = it;
+      it += LH * std::max<int64_t>(1, ceil_div(p.seqs[i].n, kSentinelChunkHost));
+    }
+    a.items = it;
+    metas.push_back(a);
+  }
+  LayoutLaunch ll;
+  ll.chunks = metas.size();
+  ll.meta = metas.data();
+  ll.block_table = cache->block_table;
+  ll.keep = keep;
+  ll.k_pool = cache->k_pool;
+  ll.v_pool = cache->v_pool;
+  ll.tags = cache->tags;
+  ll.status = di.status;
+  const cudaError_t e = launch_sentinel(ll, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_evict_sentinel launch");
+  return ok();
+}
+
+kvc_status kvc_plan_fresh_buffer_sizes(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                                       kvc_plan_sizes* out) {
+  kvc_status st = kvc_plan_buffer_sizes(cache, segs, m, out);
+  if (st != KVC_OK) return st;
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  out->freed_len = fresh_returned(p);
+  return ok();
+}
+
+kvc_status kvc_plan_fresh(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                          const int32_t* keep, const kvc_allocator* alloc, const kvc_plan* plan,
+                          kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  if ((st = check_allocator(alloc)) != KVC_OK) return st;
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if ((st = check_fresh_plan(cache, p, plan)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  if (p.Mtot > 0 && keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  std::vector<LaunchMeta> mv, rows;
+  fresh_metas(cache, p, &mv, &rows);
+  LayoutLaunch ll;
+  ll.chunks = mv.size();
+  ll.meta = mv.data();
+  ll.rows = rows.data();
+  ll.block_table = cache->block_table;
+  ll.nblocks = cache->nblocks;
+  ll.keep = keep;
+  ll.moves = plan->moves;
+  ll.move_count = plan->move_count;
+  ll.dead = plan->dead;
+  ll.dead_count = plan->dead_count;
+  ll.freed = plan->freed;
+  ll.new_rows = plan->new_rows;
+  ll.free_ids = alloc->free_ids;
+  ll.free_top = alloc->free_top;
+  ll.status = di.status;
+  const cudaError_t e = launch_fresh_plan(ll, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_plan_fresh launch");
+  return ok();
+}
+
+kvc_status kvc_commit_fresh(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
+                            const kvc_allocator* alloc, const kvc_plan* plan, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  if ((st = check_allocator(alloc)) != KVC_OK) return st;
+  Plan p;
+  if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
+  if ((st = check_fresh_plan(cache, p, plan)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  std::vector<LaunchMeta> mv, rows;
+  fresh_metas(cache, p, &mv, &rows);
+  LayoutLaunch ll;
+  ll.chunks = rows.size();
+  ll.rows = rows.data();
+  ll.block_table_mut = cache->block_table;
+  ll.nblocks = cache->nblocks;
+  ll.freed = plan->freed;
+  ll.new_rows = plan->new_rows;
+  ll.free_ids = alloc->free_ids;
+  ll.free_top = alloc->free_top;
+  ll.capacity = alloc->capacity;
+  ll.Ftot_all = fresh_returned(p);
+  ll.status = di.status;
+  const cudaError_t e = launch_fresh_commit(ll, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_commit_fresh launch");
+  return ok();
+}
+
 kvc_status kvc_read_device_status(uint32_t* out, int32_t clear, kvc_stream_t stream) {
   if (out == nullptr) return fail(KVC_ERR_INVALID_ARG, "out is NULL");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -22,7 +22,7 @@ struct SeqMeta {
   int32_t nb;     // ceil(n / P): blocks of the segment
   int32_t X;      // ceil(m / P): blocks of the target region
   int32_t split;  // score pass 1: key splits per unit
-  int32_t pad;
+  int32_t xoff;   // fresh-page compaction: first of the sequence's popped pages
   int64_t off;    // offset of the sequence in the [L][H][Ntot] score rows
   int64_t moff;   // offset in the [L][H][Mtot] keep / move rows
   int64_t foff;   // offset in the freed-page list
@@ -48,6 +48,7 @@ struct LaunchMeta {
   float scale;      // logit scale
   float pad2;
   int64_t Ntot, Mtot, Ftot;
+  int64_t Xtot;     // fresh-page compaction: pages popped by the whole call
   int64_t items;    // work items of this launch
   SeqMeta seq[kMaxSeqPerLaunch];
 };

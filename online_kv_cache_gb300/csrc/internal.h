@@ -91,6 +91,36 @@ struct CompactLaunch {
   unsigned* status = nullptr;
 };
 
+// Layout variants of eviction (layout.cu): sentinel dead slots, and the plan
+// and commit of the order-preserving compaction into fresh pages.
+struct LayoutLaunch {
+  size_t chunks = 0;
+  const LaunchMeta* meta = nullptr;  // [chunks]
+  const LaunchMeta* rows = nullptr;  // [chunks] one item per sequence (fresh plan / commit)
+  const int32_t* block_table = nullptr;
+  int32_t* block_table_mut = nullptr;
+  int32_t* nblocks = nullptr;
+  const int32_t* keep = nullptr;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  int32_t* tags = nullptr;
+  int32_t* moves = nullptr;
+  int32_t* move_count = nullptr;
+  int32_t* dead = nullptr;
+  int32_t* dead_count = nullptr;
+  int32_t* freed = nullptr;
+  int32_t* new_rows = nullptr;
+  int32_t* free_ids = nullptr;
+  int32_t* free_top = nullptr;
+  int32_t capacity = 0;
+  int64_t Ftot_all = 0;  // pages returned by the whole call (fresh commit)
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_sentinel(const LayoutLaunch& ll, cudaStream_t stream);
+cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream);
+cudaError_t launch_fresh_commit(const LayoutLaunch& ll, cudaStream_t stream);
+
 cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream);
 cudaError_t launch_compact(const CompactLaunch& cl, cudaStream_t stream);
 cudaError_t launch_free(const CompactLaunch& cl, cudaStream_t stream);

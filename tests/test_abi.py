@@ -200,3 +200,31 @@ def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
     st = lib.kvc_score_noalloc(ctypes.byref(c), ctypes.byref(s), 0x60000, 4096, 0.1, 0x70000, None, None)
     assert st == kvc.KVC_ERR_WORKSPACE
     assert "scratch" in kvc.kvc_last_error()
+
+
+def test_layout_variant_validation(lib):
+    """The sentinel and fresh-page entry points validate before any launch; the fresh plan's
+    return list holds every block of the segments that keep fewer than all positions."""
+    c = fake_cache()
+    s, _ = segs([0, 16], [100, 64], [100, 80])
+    m = np.array([20, 48], np.int32)  # sequence 1 keeps all 48 of its positions
+    assert lib.kvc_evict_sentinel(ctypes.byref(c), ctypes.byref(s), m.ctypes.data, None,
+                                  None) == kvc.KVC_ERR_INVALID_ARG
+    out = kvc.kvc_plan_sizes()
+    assert lib.kvc_plan_fresh_buffer_sizes(ctypes.byref(c), ctypes.byref(s), m.ctypes.data,
+                                           ctypes.byref(out)) == kvc.KVC_OK
+    assert out.freed_len == 7  # ceil(100/16) blocks of sequence 0; sequence 1 is untouched
+    assert out.moves_len == 2 * 2 * 2 * 68
+    plan = kvc.kvc_plan(0x100, 0x200, 0x300, 0x400, 0x500, 0x600, out.moves_len, out.units_len,
+                        out.dead_len, out.freed_len - 1, out.new_rows_len)
+    alloc = kvc.kvc_allocator(0x800, 0x900, 10)
+    assert lib.kvc_plan_fresh(ctypes.byref(c), ctypes.byref(s), m.ctypes.data, 0x700, None,
+                              ctypes.byref(plan), None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_plan_fresh(ctypes.byref(c), ctypes.byref(s), m.ctypes.data, 0x700,
+                              ctypes.byref(alloc), ctypes.byref(plan), None) == kvc.KVC_ERR_WORKSPACE
+    assert "freed" in kvc.kvc_last_error()
+    assert lib.kvc_commit_fresh(ctypes.byref(c), ctypes.byref(s), m.ctypes.data, ctypes.byref(alloc),
+                                ctypes.byref(plan), None) == kvc.KVC_ERR_WORKSPACE
+    bad = np.array([20, -1], np.int32)
+    assert lib.kvc_evict_sentinel(ctypes.byref(c), ctypes.byref(s), bad.ctypes.data, 0x700,
+                                  None) == kvc.KVC_ERR_BUDGET
