@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--variant", choices=["inplace", "sentinel", "fresh"], default="inplace",
+                    help="eviction layout after selection: the in-place tail-region compaction "
+                         "(default), sentinel dead slots, or compaction into fresh pages")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -282,10 +285,12 @@ def our_arm(args):
     import online_kv_cache_gb300 as kvc
     import workloads
 
+    import dataclasses
     sp = workloads.spec(args.workload, args.seed)
     if args.layers:
-        import dataclasses
         sp = dataclasses.replace(sp, L=args.layers)
+    if args.variant == "fresh":  # the fresh pages come from the free stack: leave room for them
+        sp = dataclasses.replace(sp, headroom=max(sp.headroom, 0.35))
     case = workloads.build(sp, args.seed + rank, dev)
     m = budgets_lib(case)
     cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks,
@@ -305,11 +310,22 @@ def our_arm(args):
         ev[2].record(stream)
         cp.select()
         ev[3].record(stream)
-        cp.plan_compact()
-        ev[4].record(stream)
-        cp.compact()
-        ev[5].record(stream)
-        cp.free_pages()
+        if args.variant == "inplace":
+            cp.plan_compact()
+            ev[4].record(stream)
+            cp.compact()
+            ev[5].record(stream)
+            cp.free_pages()
+        elif args.variant == "fresh":
+            fplan = cp.plan_fresh()
+            ev[4].record(stream)
+            cp.compact(plan=fplan)
+            ev[5].record(stream)
+            cp.commit_fresh()
+        else:  # sentinel: the whole layout step is the "compact" stage
+            ev[4].record(stream)
+            cp.evict_sentinel()
+            ev[5].record(stream)
         ev[6].record(stream)
 
     for _ in range(args.warmup):
@@ -349,7 +365,8 @@ def our_arm(args):
         clocks.stop()
 
     # algorithmic work of the step
-    moves = int(cp.plan.move_count[:sp.L * sp.H * sp.B].sum().item()) if cp.Mtot else 0
+    plan_used = cp.fresh_plan if args.variant == "fresh" else cp.plan
+    moves = int(plan_used.move_count[:sp.L * sp.H * sp.B].sum().item()) if cp.Mtot else 0
     R, d = sp.R, sp.d
     F_alg = 2.0 * R * d * entries  # one Q K^T contraction (each pass executes it once)
     Xp = sum(((min(a, b) + sp.P - 1) // sp.P) * sp.P for a, b in zip(m, n))
@@ -381,7 +398,10 @@ def our_arm(args):
                     "tensor_frac": F_alg / t_dom / 1e12 / pk["bf16_tflops"]}
     roofline.update({"traffic": profile_traffic(dom_kernel, sp.name), "peak_source": pk["source"],
                      "algorithmic_flops_per_launch": F_alg, "algorithmic_bytes_per_launch": B_pass})
-    compact_bytes = moves * 8.0 * d + 4.0 * moves
+    if args.variant == "sentinel":  # evicted rows written: K and V rows (2d bytes each) and a tag
+        compact_bytes = (entries - sp.L * sp.H * Mtot) * (4.0 * d + 4.0)
+    else:
+        compact_bytes = moves * 8.0 * d + 4.0 * moves
     gbs = compact_bytes / (per_stage["compact"] * 1e-3) / 1e9 if per_stage["compact"] > 0 else 0.0
 
     line = {
@@ -392,7 +412,8 @@ def our_arm(args):
                    "l2": "inputs larger than L2 (pools %.1f GB); cache restored from a device "
                          "snapshot between steps, outside the timed events"
                          % (2 * case.k_pool.numel() * 2 / 1e9),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "eviction_layout": args.variant},
         "roofline": roofline,
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
                           "F_alg": F_alg, "B_alg": B_alg, "moves": moves},
@@ -404,9 +425,10 @@ def our_arm(args):
     if clocks:
         line["clocks"] = clocks.summary(w0, w1)
 
-    if not args.no_e2e:
+    # the end-to-end and CPU-baseline legs measure the default in-place chain only
+    if not args.no_e2e and args.variant == "inplace":
         line["e2e"] = e2e_run(args, case, cp, snap, entries, world, dev)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "inplace":
         case.restore(snap)  # the oracle reads the pristine cache
         torch.cuda.synchronize()
         line["cpu_baseline"] = cpu_baseline(case, budgets_oracle(case))
