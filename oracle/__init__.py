@@ -17,6 +17,8 @@ function cites the page passage it restates:
   sequentially, and the return of the emptied blocks to the allocator;
 * logical view -- the order-preserving out-of-place view (Chain Cache's
   logical-vs-physical split on the SparseEngine page);
+* action attention / LRFU -- ActKV's action-critical entries (top 90% of the
+  action attention mass) smoothed by LRFU (lambda = 0.5) into the eviction score;
 * sentinel eviction / fresh-page compaction -- the layout-preserving dead
   slot (K = -10^4, V = 0) of the IntentKV page, and an order-preserving
   compaction into freshly allocated pages.
@@ -85,6 +87,14 @@ def _load():
         lib.oracle_free_blocks.restype = I
         lib.oracle_logical_view.argtypes = [P, P, P, I, I, I, I, I, I, P, I, P, I, P, P, P]
         lib.oracle_logical_view.restype = I
+        lib.oracle_action_dense.argtypes = [P, P, I, I, I, D, P, P]
+        lib.oracle_action_dense.restype = I
+        lib.oracle_action_cache.argtypes = lib.oracle_score_cache.argtypes
+        lib.oracle_action_cache.restype = I
+        lib.oracle_action_hits.argtypes = [P, I, D, P]
+        lib.oracle_action_hits.restype = I
+        lib.oracle_lrfu_cache.argtypes = [P, I, I, I, I, P, I, P, P, I, P, D, D, P, P]
+        lib.oracle_lrfu_cache.restype = I
         lib.oracle_sentinel_k_bits.argtypes = []
         lib.oracle_sentinel_k_bits.restype = ctypes.c_uint16
         lib.oracle_evict_sentinel.argtypes = [P, P, P, I, I, I, I, I, I, I, P, I, P, P, I, P, P]
@@ -165,9 +175,49 @@ def _i32(a) -> np.ndarray:
     return _c(np.asarray(a), np.int32)
 
 
+def action_dense(Q: np.ndarray, K: np.ndarray, scale: float):
+    """(a [n], lse [R]) in fp64: a_j = sum_i alpha_ij."""
+    Q = _c(Q, np.float64)
+    K = _c(K, np.float64)
+    R, d = Q.shape
+    n = K.shape[0]
+    a = np.zeros(n, np.float64)
+    lse = np.zeros(R, np.float64)
+    _check(_load().oracle_action_dense(_ptr(Q), _ptr(K), R, n, d, float(scale), _ptr(a), _ptr(lse)),
+           "action_dense")
+    return a, lse
+
+
+def action_hits(a: np.ndarray, frac: float = 0.9) -> np.ndarray:
+    """0/1 flags of the action-critical entries of one unit."""
+    a = _c(a, np.float64)
+    hit = np.zeros(max(1, a.size), np.uint8)
+    _check(_load().oracle_action_hits(_ptr(a), a.size, float(frac), _ptr(hit)), "action_hits")
+    return hit[:a.size].astype(bool)
+
+
+def lrfu_cache(crf_pool: np.ndarray, block_table, seg_start, seg_end, a: np.ndarray,
+               frac: float = 0.9, lam: float = 0.5):
+    """One LRFU step; crf_pool fp64 [L][num_pages][H][P] updated in place.  Returns (crf [L][H][Ntot],
+    hits [L][H][Ntot] bool)."""
+    if crf_pool.dtype != np.float64 or not crf_pool.flags.c_contiguous:
+        raise TypeError("crf_pool must be a contiguous float64 array")
+    L, num_pages, H, P = crf_pool.shape
+    bt = _i32(block_table)
+    s0, s1 = _i32(seg_start), _i32(seg_end)
+    a = _c(a, np.float64)
+    crf = np.zeros(a.shape, np.float64)
+    hits = np.zeros(a.shape, np.uint8)
+    _check(_load().oracle_lrfu_cache(_ptr(crf_pool), L, num_pages, H, P, _ptr(bt), bt.shape[1],
+                                     _ptr(s0), _ptr(s1), len(s0), _ptr(a), float(frac), float(lam),
+                                     _ptr(crf), _ptr(hits)), "lrfu_cache")
+    return crf, hits.astype(bool)
+
+
 def score_cache(k_pool, block_table, nblocks, seg_start, seg_end, seq_len, q, scale,
-                unit_mask=None, threads=None):
-    """Scores [L][H][Ntot] (fp64) and LSE [B][L][H][R] of every unit of a paged cache.
+                unit_mask=None, threads=None, action=False):
+    """Scores [L][H][Ntot] (fp64) and LSE [B][L][H][R] of every unit of a paged cache (with
+    action=True the action attention a_j = sum_i alpha_ij instead of the score).
 
     k_pool: bf16 [L][num_pages][H][P][d]; q: bf16 [B][L][H][R][d]; the segment of
     sequence b is [seg_start[b], seg_end[b]) in its slot coordinates.  unit_mask
@@ -188,10 +238,10 @@ def score_cache(k_pool, block_table, nblocks, seg_start, seg_end, seq_len, q, sc
     lse = np.full((B, L, H, R), np.nan, np.float64)
     mask = None if unit_mask is None else _c(np.asarray(unit_mask, dtype=bool).reshape(B, L, H),
                                              np.uint8)
-    st = _load().oracle_score_cache(_ptr(kb), _ptr(bt), _ptr(nbk), bt.shape[1], L, num_pages, H,
-                                    P, d, _ptr(s0), _ptr(s1), _ptr(sl), B, _ptr(qb), R,
-                                    float(scale), _ptr(mask), _ptr(scores), _ptr(lse),
-                                    threads or default_threads())
+    fn = _load().oracle_action_cache if action else _load().oracle_score_cache
+    st = fn(_ptr(kb), _ptr(bt), _ptr(nbk), bt.shape[1], L, num_pages, H, P, d, _ptr(s0), _ptr(s1),
+            _ptr(sl), B, _ptr(qb), R, float(scale), _ptr(mask), _ptr(scores), _ptr(lse),
+            threads or default_threads())
     _check(st, "score_cache")
     return scores, lse
 

@@ -148,6 +148,47 @@ int oracle_score_dense(const double *Q, const double *K, int R, int n, int d,
     return status;
 }
 
+/* Action attention of every key (ActKV analysis page, first component: the
+ * attention that all action tokens pay to a KV entry, gathered per entry):
+ *   a_j = sum_i alpha_ij,  alpha_ij = exp(L_ij - LSE_i) as in
+ *   oracle_score_dense; the rows of Q are the action tokens' queries.
+ * Writes a[n] and, if lse != NULL, lse[R]. */
+int oracle_action_dense(const double *Q, const double *K, int R, int n, int d, double scale,
+                        double *a, double *lse)
+{
+    if (R <= 0 || n < 0 || d <= 0 || !Q || (n > 0 && (!K || !a))) return ORC_ERR_ARG;
+    if (n == 0) {
+        if (lse)
+            for (int i = 0; i < R; ++i) lse[i] = -INFINITY;
+        return ORC_OK;
+    }
+    double *row = (double *)malloc((size_t)n * sizeof(double));
+    if (!row) return ORC_ERR_NOMEM;
+    for (int j = 0; j < n; ++j) a[j] = 0.0;
+    int status = ORC_OK;
+    for (int i = 0; i < R && status == ORC_OK; ++i) {
+        const double *qi = Q + (size_t)i * d;
+        for (int j = 0; j < n; ++j) {
+            const double *kj = K + (size_t)j * d;
+            double dot = 0.0;
+            for (int t = 0; t < d; ++t) dot += qi[t] * kj[t];
+            row[j] = scale * dot;
+            if (!isfinite(row[j])) status = ORC_ERR_NONFINITE;
+        }
+        if (status != ORC_OK) break;
+        double mx = row[0];
+        for (int j = 1; j < n; ++j)
+            if (row[j] > mx) mx = row[j];
+        double sum = 0.0;
+        for (int j = 0; j < n; ++j) sum += exp(row[j] - mx);
+        double lse_i = mx + log(sum);
+        if (lse) lse[i] = lse_i;
+        for (int j = 0; j < n; ++j) a[j] += exp(row[j] - lse_i);
+    }
+    free(row);
+    return status;
+}
+
 /* Slot s of sequence b, layer l, head h -> index of its first element in a
  * pool laid out [L][num_pages][H][P][d]. */
 static size_t pool_elem(const int32_t *bt_row, int slot, int layer, int head,
@@ -189,11 +230,11 @@ static int check_segment(const int32_t *bt_row, int nblocks_b, int max_blocks, i
  *   scores   out [L][H][Ntot], Ntot = sum_b n_b, sequence b at offset
  *            sum_{b'<b} n_b'   (entries of skipped units are left untouched)
  *   lse      out [B][L][H][R] or NULL */
-int oracle_score_cache(const uint16_t *k_pool, const int32_t *block_table, const int32_t *nblocks,
+static int cache_units(const uint16_t *k_pool, const int32_t *block_table, const int32_t *nblocks,
                        int max_blocks, int L, int num_pages, int H, int P, int d,
                        const int32_t *seg_start, const int32_t *seg_end, const int32_t *seq_len,
                        int B, const uint16_t *q, int R, double scale, const uint8_t *unit_mask,
-                       double *scores, double *lse, int nthreads)
+                       double *scores, double *lse, int nthreads, int action)
 {
     if (!k_pool || !block_table || !nblocks || !seg_start || !seg_end || !seq_len || !q ||
         !scores || L <= 0 || H <= 0 || P <= 0 || d <= 0 || R <= 0 || B <= 0)
@@ -241,7 +282,8 @@ int oracle_score_cache(const uint16_t *k_pool, const int32_t *block_table, const
             for (int t = 0; t < d; ++t) Kd[(size_t)j * d + t] = bf16_to_double(k_pool[base + t]);
         }
         double *s_u = scores + ((size_t)l * H + h) * Ntot + off[b];
-        int st = oracle_score_dense(Qd, Kd, R, n, d, scale, s_u, lse_u);
+        int st = action ? oracle_action_dense(Qd, Kd, R, n, d, scale, s_u, lse_u)
+                        : oracle_score_dense(Qd, Kd, R, n, d, scale, s_u, lse_u);
         if (st != ORC_OK) {
 #pragma omp critical
             status = st;
@@ -251,6 +293,28 @@ int oracle_score_cache(const uint16_t *k_pool, const int32_t *block_table, const
     }
     free(off);
     return status;
+}
+
+int oracle_score_cache(const uint16_t *k_pool, const int32_t *block_table, const int32_t *nblocks,
+                       int max_blocks, int L, int num_pages, int H, int P, int d,
+                       const int32_t *seg_start, const int32_t *seg_end, const int32_t *seq_len,
+                       int B, const uint16_t *q, int R, double scale, const uint8_t *unit_mask,
+                       double *scores, double *lse, int nthreads)
+{
+    return cache_units(k_pool, block_table, nblocks, max_blocks, L, num_pages, H, P, d, seg_start,
+                       seg_end, seq_len, B, q, R, scale, unit_mask, scores, lse, nthreads, 0);
+}
+
+/* Action attention a_j (oracle_action_dense) of every unit of a paged cache,
+ * laid out like oracle_score_cache's scores. */
+int oracle_action_cache(const uint16_t *k_pool, const int32_t *block_table, const int32_t *nblocks,
+                        int max_blocks, int L, int num_pages, int H, int P, int d,
+                        const int32_t *seg_start, const int32_t *seg_end, const int32_t *seq_len,
+                        int B, const uint16_t *q, int R, double scale, const uint8_t *unit_mask,
+                        double *a, double *lse, int nthreads)
+{
+    return cache_units(k_pool, block_table, nblocks, max_blocks, L, num_pages, H, P, d, seg_start,
+                       seg_end, seq_len, B, q, R, scale, unit_mask, a, lse, nthreads, 1);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -664,6 +728,94 @@ int oracle_commit_fresh(int32_t *block_table, int32_t *nblocks, int max_blocks, 
         for (int i = old - f; i < old; ++i) row[i] = -1;
         nblocks[b] = old - f;
         xoff += X;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* ActKV action-critical entries and LRFU.                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Action-critical entries of one unit (ActKV analysis page, first component:
+ * entries whose action attention falls within the top 90% count as action-
+ * critical).  Reading: order the entries by a_j (descending, ties to the
+ * lower position), take the shortest prefix whose cumulative a reaches
+ * frac * sum_j a_j, and mark every entry whose a_j is at least the last
+ * value of that prefix (ties at the boundary included).  hit[n] gets 0/1.
+ * An all-zero a marks nothing. */
+int oracle_action_hits(const double *a, int n, double frac, uint8_t *hit)
+{
+    if (n < 0 || (n > 0 && (!a || !hit)) || !(frac >= 0.0 && frac <= 1.0)) return ORC_ERR_ARG;
+    if (n == 0) return ORC_OK;
+    scored_pos *v = (scored_pos *)malloc((size_t)n * sizeof(scored_pos));
+    if (!v) return ORC_ERR_NOMEM;
+    double total = 0.0;
+    for (int j = 0; j < n; ++j) {
+        v[j].s = a[j];
+        v[j].j = j;
+        total += a[j];
+        hit[j] = 0;
+    }
+    if (total > 0.0 && frac > 0.0) {
+        qsort(v, (size_t)n, sizeof(scored_pos), by_score_then_position);
+        double cum = 0.0, tau = v[n - 1].s;
+        for (int r = 0; r < n; ++r) {
+            cum += v[r].s;
+            if (cum >= frac * total) {
+                tau = v[r].s;
+                break;
+            }
+        }
+        for (int j = 0; j < n; ++j) hit[j] = (uint8_t)(a[j] >= tau);
+    }
+    free(v);
+    return ORC_OK;
+}
+
+/* One LRFU step over every unit of a paged cache (ActKV analysis page: LRFU
+ * with its hit signal replaced by "hit by action attention", decay lambda =
+ * 0.5).  LRFU's combined recency-frequency value of an entry referenced at
+ * times t_k is sum_k (1/2)^(lambda (t - t_k)); evaluated once per compaction
+ * step it is  crf <- 2^(-lambda) crf + hit.  crf_pool holds one value per
+ * slot [L][num_pages][H][P] and is updated in place for the positions of
+ * each segment; crf_out [L][H][Ntot] receives the new values (the eviction
+ * scores) and hits [L][H][Ntot] (may be NULL) the hit flags. */
+int oracle_lrfu_cache(double *crf_pool, int L, int num_pages, int H, int P,
+                      const int32_t *block_table, int max_blocks, const int32_t *seg_start,
+                      const int32_t *seg_end, int B, const double *a, double frac, double lambda,
+                      double *crf_out, uint8_t *hits)
+{
+    if (!crf_pool || !block_table || !seg_start || !seg_end || !a || !crf_out || L <= 0 ||
+        H <= 0 || P <= 0 || B <= 0)
+        return ORC_ERR_ARG;
+    int64_t Ntot = 0;
+    for (int b = 0; b < B; ++b) Ntot += seg_end[b] - seg_start[b];
+    const double decay = pow(2.0, -lambda);
+    for (int l = 0; l < L; ++l) {
+        for (int h = 0; h < H; ++h) {
+            int64_t off = 0;
+            for (int b = 0; b < B; ++b) {
+                int s0 = seg_start[b], n = seg_end[b] - seg_start[b];
+                const size_t row = ((size_t)l * H + h) * (size_t)Ntot + (size_t)off;
+                off += n;
+                if (n == 0) continue;
+                uint8_t *hit = (uint8_t *)malloc((size_t)n);
+                if (!hit) return ORC_ERR_NOMEM;
+                int st = oracle_action_hits(a + row, n, frac, hit);
+                if (st != ORC_OK) {
+                    free(hit);
+                    return st;
+                }
+                const int32_t *bt_row = block_table + (size_t)b * max_blocks;
+                for (int j = 0; j < n; ++j) {
+                    size_t e = tag_elem(bt_row, s0 + j, l, h, num_pages, H, P);
+                    crf_pool[e] = decay * crf_pool[e] + (double)hit[j];
+                    crf_out[row + j] = crf_pool[e];
+                    if (hits) hits[row + j] = hit[j];
+                }
+                free(hit);
+            }
+        }
     }
     return ORC_OK;
 }
