@@ -99,6 +99,9 @@ typedef struct kvc_cache {
     int32_t head_dim;     /* d */
     int32_t max_blocks;
     int32_t batch;        /* B */
+    float *aux;           /* fp32 [L][num_pages][H][P]: per-slot state that
+                           * travels with its entry through kvc_compact (the
+                           * LRFU values of kvc_lrfu_update), or NULL */
 } kvc_cache;
 
 /* One segment per sequence, all host memory ([SE]: the application names the
@@ -276,6 +279,36 @@ kvc_status kvc_compact(const kvc_cache *cache, const kvc_segments *segs, const i
  * KVC_DEV_FREE_STACK and pushes nothing. */
 kvc_status kvc_free_pages(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                           const kvc_allocator *alloc, const kvc_plan *plan, kvc_stream_t stream);
+
+/* ------------------------------------------------------------ ActKV scoring */
+
+/* Action attention of every cached key ("ActKV 解剖", zhichai.net analysis of
+ * ActKV, first component: the attention scores of all action tokens toward a
+ * KV entry, gathered per entry):
+ *   a_j = sum_i alpha_ij,  alpha_ij = exp(L_ij - LSE_i) over the segment,
+ * with q holding the action tokens' query rows in the layout of kvc_score.
+ * attn out fp32 [L][H][Ntot] (layout of kvc_score's scores); lse as in
+ * kvc_score.  Same two tensor-core passes and workspace size as kvc_score. */
+kvc_status kvc_score_action(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
+                            int32_t R, float scale, float *attn, float *lse, void *ws,
+                            size_t ws_bytes, kvc_stream_t stream);
+
+/* One LRFU step of ActKV's eviction score (same page: entries within the top
+ * 90% of action attention are action-critical; LRFU takes "hit by action
+ * attention" as its reference signal, decay lambda = 0.5).  Per unit:
+ * the action-critical entries are those with a_j >= tau, tau the largest
+ * value whose entries a >= tau hold at least frac of the unit's total action
+ * mass (the shortest prefix of the a-descending order reaching frac, boundary
+ * ties included; nothing if the mass is 0 or frac = 0).  Then for every slot
+ * of the segment: crf <- 2^-lambda * crf + hit in cache->aux (required), and
+ * crf_out [L][H][Ntot] receives the new values (the eviction scores for
+ * kvc_select_topm).  hits (uint8 [L][H][Ntot], may be NULL) receives the
+ * flags.  Masses are summed in 2^-40 fixed point (64-bit integers), so the
+ * result does not depend on the order of the sums.  frac in [0, 1], lambda
+ * finite and >= 0. */
+kvc_status kvc_lrfu_update(const kvc_cache *cache, const kvc_segments *segs, const float *attn,
+                           float frac, float lambda, float *crf_out, uint8_t *hits,
+                           kvc_stream_t stream);
 
 /* ------------------------------------------------- layout variants of eviction */
 

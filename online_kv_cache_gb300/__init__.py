@@ -45,7 +45,8 @@ EXPORTED = (
     "kvc_compact", "kvc_free_pages", "kvc_status_string", "kvc_last_error",
     "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
     "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc", "kvc_evict_sentinel",
-    "kvc_plan_fresh_buffer_sizes", "kvc_plan_fresh", "kvc_commit_fresh",
+    "kvc_plan_fresh_buffer_sizes", "kvc_plan_fresh", "kvc_commit_fresh", "kvc_score_action",
+    "kvc_lrfu_update",
 )
 
 
@@ -65,7 +66,7 @@ class kvc_cache(ctypes.Structure):
                 ("num_layers", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
-                ("batch", ctypes.c_int32)]
+                ("batch", ctypes.c_int32), ("aux", ctypes.c_void_p)]
 
 
 class kvc_segments(ctypes.Structure):
@@ -139,6 +140,8 @@ def lib():
             "kvc_plan_fresh_buffer_sizes": (I32, [C, SG, P, ctypes.POINTER(kvc_plan_sizes)]),
             "kvc_plan_fresh": (I32, [C, SG, P, P, A, PL, P]),
             "kvc_commit_fresh": (I32, [C, SG, P, A, PL, P]),
+            "kvc_score_action": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
+            "kvc_lrfu_update": (I32, [C, SG, P, F, F, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -184,14 +187,14 @@ class Cache:
     """kvc_cache over torch tensors (pools [L][num_pages][H][P][d] bf16, tags int32,
     block_table [B][max_blocks] int32, nblocks [B] int32)."""
 
-    def __init__(self, k_pool, v_pool, tags, block_table, nblocks):
+    def __init__(self, k_pool, v_pool, tags, block_table, nblocks, aux=None):
         L, num_pages, H, P, d = k_pool.shape
-        self.tensors = (k_pool, v_pool, tags, block_table, nblocks)
+        self.tensors = (k_pool, v_pool, tags, block_table, nblocks, aux)
         self.c = kvc_cache(
             _dev_ptr(k_pool, "k_pool", torch.bfloat16), _dev_ptr(v_pool, "v_pool", torch.bfloat16),
             _dev_ptr(tags, "tags", torch.int32), _dev_ptr(block_table, "block_table", torch.int32),
             _dev_ptr(nblocks, "nblocks", torch.int32), L, num_pages, H, P, d,
-            block_table.shape[1], block_table.shape[0])
+            block_table.shape[1], block_table.shape[0], _dev_ptr(aux, "aux", torch.float32))
 
     @property
     def ref(self):
@@ -382,6 +385,22 @@ def kvc_commit_fresh(cache: Cache, segs: Segments, m, alloc: Allocator, plan: Pl
                                   _stream(stream)), "kvc_commit_fresh")
 
 
+def kvc_score_action(cache: Cache, segs: Segments, q: torch.Tensor, R: int, scale: float,
+                     attn: torch.Tensor, lse: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    _check(lib().kvc_score_action(cache.ref, segs.ref, _dev_ptr(q, "q", torch.bfloat16), int(R),
+                                  float(scale), _dev_ptr(attn, "attn", torch.float32),
+                                  _dev_ptr(lse, "lse", torch.float32), _dev_ptr(ws, "ws"),
+                                  ws.numel() * ws.element_size(), _stream(stream)), "kvc_score_action")
+
+
+def kvc_lrfu_update(cache: Cache, segs: Segments, attn: torch.Tensor, frac: float, lam: float,
+                    crf_out: torch.Tensor, hits: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().kvc_lrfu_update(cache.ref, segs.ref, _dev_ptr(attn, "attn", torch.float32),
+                                 float(frac), float(lam), _dev_ptr(crf_out, "crf_out", torch.float32),
+                                 _dev_ptr(hits, "hits", torch.uint8), _stream(stream)),
+           "kvc_lrfu_update")
+
+
 def kvc_status_string(status: int) -> str:
     return lib().kvc_status_string(int(status)).decode()
 
@@ -421,8 +440,8 @@ class Compactor:
     segments: host lists seg_start / seg_end / seq_len; m: host budgets per sequence."""
 
     def __init__(self, k_pool, v_pool, tags, block_table, nblocks, free_ids, free_top,
-                 seg_start, seg_end, seq_len, m, R: int):
-        self.cache = Cache(k_pool, v_pool, tags, block_table, nblocks)
+                 seg_start, seg_end, seq_len, m, R: int, aux=None):
+        self.cache = Cache(k_pool, v_pool, tags, block_table, nblocks, aux)
         self.alloc = Allocator(free_ids, free_top)
         self.segs = Segments(seg_start, seg_end, seq_len)
         self.m = _host_i32(m)
@@ -453,6 +472,17 @@ class Compactor:
                     stream=None):
         kvc_score_alpha(self.cache, self.segs, q, self.R, scale, lse, self.scores, self.ws_view,
                         stream)
+
+    def score_action(self, q: torch.Tensor, scale: float, stream=None):
+        """Action attention a_j of every key into self.attn (ActKV's hit signal)."""
+        if getattr(self, "attn", None) is None:
+            self.attn = torch.empty_like(self.scores)
+        kvc_score_action(self.cache, self.segs, q, self.R, scale, self.attn, None, self.ws_view, stream)
+
+    def lrfu(self, frac: float = 0.9, lam: float = 0.5, hits: Optional[torch.Tensor] = None,
+             stream=None):
+        """One LRFU step on the cache's aux values; the new values become self.scores."""
+        kvc_lrfu_update(self.cache, self.segs, self.attn, frac, lam, self.scores, hits, stream)
 
     def select(self, stream=None):
         kvc_select_topm(self.cache, self.segs, self.scores, self.m, self.keep, None, stream)

@@ -290,7 +290,7 @@ struct ScorePlan {
   size_t part_bytes = 0, obias_bytes = 0, part2_bytes = 0;
 };
 
-void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, float scale, int num_sms,
+void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, float scale, float pw, int num_sms,
                       ScorePlan* sp) {
   const int64_t LH = (int64_t)c->num_layers * c->num_kv_heads;
   const int tpi1 = tiles_per_item(c, p, g.ngroups1, num_sms);
@@ -306,6 +306,7 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
       lm->nchunks = g.nchunks;
       lm->rowtiles = g.rowtiles;
       lm->scale = scale;
+      lm->pw = pw;
     }
     a.ngroups = g.ngroups1;
     a.gsub = g.gsub1;
@@ -452,7 +453,7 @@ kvc_status kvc_score_workspace_size(const kvc_cache* cache, const kvc_segments* 
   DeviceInfo di;
   if ((st = device_info_or_default(&di)) != KVC_OK) return st;
   ScorePlan sp;
-  build_score_plan(cache, p, score_geom(R, cache->head_dim), 1.0f, di.num_sms, &sp);
+  build_score_plan(cache, p, score_geom(R, cache->head_dim), 1.0f, 2.0f, di.num_sms, &sp);
   *bytes = align256(sp.part_bytes) + align256(sp.obias_bytes) + align256(sp.part2_bytes);
   return ok();
 }
@@ -463,7 +464,7 @@ namespace kvc {
 namespace {
 
 // Validation, descriptors and launches shared by kvc_score, kvc_score_lse and kvc_score_alpha.
-kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cache,
+kvc_status score_common(const char* where, unsigned phases, float pw, const kvc_cache* cache,
                         const kvc_segments* segs, const uint16_t* q, int32_t R, float scale,
                         const float* lse_in, float* lse_out, float* scores, void* ws, size_t ws_bytes,
                         kvc_stream_t stream) {
@@ -481,7 +482,7 @@ kvc_status score_common(const char* where, unsigned phases, const kvc_cache* cac
   if ((st = device_info_or_default(&di)) != KVC_OK) return st;
   const ScoreGeom g = score_geom(R, cache->head_dim);
   ScorePlan sp;
-  build_score_plan(cache, p, g, scale, di.num_sms, &sp);
+  build_score_plan(cache, p, g, scale, pw, di.num_sms, &sp);
   const size_t need = align256(sp.part_bytes) + align256(sp.obias_bytes) + align256(sp.part2_bytes);
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
@@ -534,13 +535,13 @@ extern "C" {
 kvc_status kvc_score(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
                      float scale, float* scores, float* lse, void* ws, size_t ws_bytes,
                      kvc_stream_t stream) {
-  return score_common("kvc_score", kPhaseLse | kPhaseAlpha, cache, segs, q, R, scale, nullptr, lse,
+  return score_common("kvc_score", kPhaseLse | kPhaseAlpha, 2.0f, cache, segs, q, R, scale, nullptr, lse,
                       scores, ws, ws_bytes, stream);
 }
 
 kvc_status kvc_score_lse(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
                          float scale, float* lse, void* ws, size_t ws_bytes, kvc_stream_t stream) {
-  return score_common("kvc_score_lse", kPhaseLse, cache, segs, q, R, scale, nullptr, lse, nullptr, ws,
+  return score_common("kvc_score_lse", kPhaseLse, 2.0f, cache, segs, q, R, scale, nullptr, lse, nullptr, ws,
                       ws_bytes, stream);
 }
 
@@ -548,8 +549,15 @@ kvc_status kvc_score_alpha(const kvc_cache* cache, const kvc_segments* segs, con
                            float scale, const float* lse, float* scores, void* ws, size_t ws_bytes,
                            kvc_stream_t stream) {
   const unsigned phases = kPhaseAlpha | (lse != nullptr ? kPhaseLseIn : 0u);
-  return score_common("kvc_score_alpha", phases, cache, segs, q, R, scale, lse, nullptr, scores, ws,
+  return score_common("kvc_score_alpha", phases, 2.0f, cache, segs, q, R, scale, lse, nullptr, scores, ws,
                       ws_bytes, stream);
+}
+
+kvc_status kvc_score_action(const kvc_cache* cache, const kvc_segments* segs, const uint16_t* q, int32_t R,
+                            float scale, float* attn, float* lse, void* ws, size_t ws_bytes,
+                            kvc_stream_t stream) {
+  return score_common("kvc_score_action", kPhaseLse | kPhaseAlpha, 1.0f, cache, segs, q, R, scale, nullptr,
+                      lse, attn, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- no-alloc scoring
@@ -791,6 +799,7 @@ kvc_status kvc_compact(const kvc_cache* cache, const kvc_segments* segs, const i
   cl.k_pool = cache->k_pool;
   cl.v_pool = cache->v_pool;
   cl.tags = cache->tags;
+  cl.aux = cache->aux;
   cl.moves = plan->moves;
   cl.move_count = plan->move_count;
   cl.dead = plan->dead;
@@ -1025,6 +1034,51 @@ kvc_status kvc_commit_fresh(const kvc_cache* cache, const kvc_segments* segs, co
   ll.status = di.status;
   const cudaError_t e = launch_fresh_commit(ll, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_commit_fresh launch");
+  return ok();
+}
+
+// ------------------------------------------------------------- ActKV LRFU
+
+kvc_status kvc_lrfu_update(const kvc_cache* cache, const kvc_segments* segs, const float* attn, float frac,
+                           float lambda, float* crf_out, uint8_t* hits, kvc_stream_t stream) {
+  kvc_status st = check_cache(cache, kNeedBT);
+  if (st != KVC_OK) return st;
+  if (cache->aux == nullptr) return fail(KVC_ERR_INVALID_ARG, "cache->aux (the per-slot LRFU values) is NULL");
+  if (attn == nullptr || crf_out == nullptr) return fail(KVC_ERR_INVALID_ARG, "attn or crf_out is NULL");
+  if (!(frac >= 0.0f && frac <= 1.0f)) return fail(KVC_ERR_INVALID_ARG, "frac must lie in [0, 1]");
+  if (!std::isfinite(lambda) || lambda < 0.0f) return fail(KVC_ERR_INVALID_ARG, "lambda must be finite and >= 0");
+  Plan p;
+  if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
+  if (p.seqs.empty()) return ok();
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
+  std::vector<LaunchMeta> metas;
+  for (auto [lo, hi] : chunks_of(p)) {
+    LaunchMeta a = base_meta(cache, p);
+    a.nseq = (int)(hi - lo);
+    int64_t it = 0;
+    for (size_t i = lo; i < hi; ++i) {
+      fill_seq(&a.seq[i - lo], p, i);
+      a.seq[i - lo].item0 = it;
+      it += LH;
+    }
+    a.items = it;
+    metas.push_back(a);
+  }
+  LrfuLaunch ll;
+  ll.chunks = metas.size();
+  ll.meta = metas.data();
+  ll.block_table = cache->block_table;
+  ll.attn = attn;
+  ll.crf_pool = cache->aux;
+  ll.crf_out = crf_out;
+  ll.hits = hits;
+  ll.frac = frac;
+  ll.decay = (float)std::exp2(-(double)lambda);
+  ll.status = di.status;
+  const cudaError_t e = launch_lrfu(ll, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_lrfu_update launch");
   return ok();
 }
 

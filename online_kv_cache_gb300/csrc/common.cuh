@@ -46,7 +46,7 @@ struct LaunchMeta {
   int32_t log2P;    // log2(P)
   int32_t words;    // plan: 32-bit bitmap words covering the largest target region
   float scale;      // logit scale
-  float pad2;
+  float pw;         // score pass 2: power of alpha summed per key (2: eviction score, 1: action attention)
   int64_t Ntot, Mtot, Ftot;
   int64_t Xtot;     // fresh-page compaction: pages popped by the whole call
   int64_t items;    // work items of this launch

@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(256)
 
 // One parallel copy.  A block copies up to kMovesPerBlock moves of one unit
 // (the unit is decoded once per block): each move moves a K row and a V row
-// (d bf16 each, 16-byte vectors, D/4 lanes per move) and the tag; U moves are
+// (d bf16 each, 16-byte vectors, D/4 lanes per move), the tag and, when the
+// cache has one, the per-slot aux value; U moves are
 // in flight per lane group.  The unit's first block also writes tag -1 to its
 // dead holes.
 template <int D>
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(256)
     copy_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ moves,
                 const int32_t* __restrict__ move_count, const int32_t* __restrict__ dead,
                 const int32_t* __restrict__ dead_count, uint8_t* __restrict__ k_pool,
-                uint8_t* __restrict__ v_pool, int32_t* __restrict__ tags) {
+                uint8_t* __restrict__ v_pool, int32_t* __restrict__ tags, float* __restrict__ aux) {
   constexpr int LPM = D / 4;     // lanes per move
   constexpr int MPW = 32 / LPM;  // moves per warp step
   constexpr int CH = D / 8;      // 16-byte chunks per row
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(256)
     int4 val[U];
     int64_t drow[U];
     int32_t tag[U];
+    float ax[U];
 #pragma unroll
     for (int q = 0; q < U; ++q) {
       const int k = kb + q * kStride;
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(256)
           const int64_t srow = lbase + (int64_t)(m2.x >> lp) * HP + (m2.x & (P - 1));
           drow[q] = lbase + (int64_t)(m2.y >> lp) * HP + (m2.y & (P - 1));
           val[q] = *reinterpret_cast<const int4*>(pool + srow * kRowBytes + ch * 16);
-          if (c == 0) tag[q] = tags[srow];
+          if (c == 0) {
+            tag[q] = tags[srow];
+            if (aux) ax[q] = aux[srow];
+          }
         }
       }
     }
@@ -256,7 +261,10 @@ __global__ void __launch_bounds__(256)
     for (int q = 0; q < U; ++q) {
       if (drow[q] < 0) continue;
       *reinterpret_cast<int4*>(pool + drow[q] * kRowBytes + ch * 16) = val[q];
-      if (c == 0) tags[drow[q]] = tag[q];
+      if (c == 0) {
+        tags[drow[q]] = tag[q];
+        if (aux) aux[drow[q]] = ax[q];
+      }
     }
   }
   if (chunk == 0) {
@@ -339,11 +347,11 @@ cudaError_t launch_compact(const CompactLaunch& cl, cudaStream_t stream) {
     if (m.d == 128)
       copy_kernel<128><<<(unsigned)m.items, 256, 0, stream>>>(
           m, cl.moves, cl.move_count, cl.dead, cl.dead_count, static_cast<uint8_t*>(cl.k_pool),
-          static_cast<uint8_t*>(cl.v_pool), cl.tags);
+          static_cast<uint8_t*>(cl.v_pool), cl.tags, cl.aux);
     else
       copy_kernel<64><<<(unsigned)m.items, 256, 0, stream>>>(
           m, cl.moves, cl.move_count, cl.dead, cl.dead_count, static_cast<uint8_t*>(cl.k_pool),
-          static_cast<uint8_t*>(cl.v_pool), cl.tags);
+          static_cast<uint8_t*>(cl.v_pool), cl.tags, cl.aux);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch();

@@ -79,6 +79,7 @@ struct CompactLaunch {
   void* k_pool = nullptr;
   void* v_pool = nullptr;
   int32_t* tags = nullptr;
+  float* aux = nullptr;  // per-slot state moved with the tags, or null
   int32_t* moves = nullptr;
   int32_t* move_count = nullptr;
   int32_t* dead = nullptr;
@@ -117,6 +118,21 @@ struct LayoutLaunch {
   unsigned* status = nullptr;
 };
 
+// ActKV's LRFU step (actkv.cu): one block per unit.
+struct LrfuLaunch {
+  size_t chunks = 0;
+  const LaunchMeta* meta = nullptr;  // [chunks], one item per unit
+  const int32_t* block_table = nullptr;
+  const float* attn = nullptr;       // [L][H][Ntot] action attention
+  float* crf_pool = nullptr;         // [L][num_pages][H][P] per-slot LRFU values
+  float* crf_out = nullptr;          // [L][H][Ntot] eviction scores
+  uint8_t* hits = nullptr;           // [L][H][Ntot] or null
+  float frac = 0.9f;
+  float decay = 0.70710678f;
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_lrfu(const LrfuLaunch& ll, cudaStream_t stream);
 cudaError_t launch_sentinel(const LayoutLaunch& ll, cudaStream_t stream);
 cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream);
 cudaError_t launch_fresh_commit(const LayoutLaunch& ll, cudaStream_t stream);

@@ -24,12 +24,15 @@
 //                      sum) per row in the log2 domain; each warpgroup writes
 //                      one partial per (item, row).
 // Combine:             merges the partials of a row into the pass-2 offset
-//                      nob_i = kBias - 2 log2 sum_j 2^(c q_i.k_j)  (c = scale log2 e).
+//                      nob_i = kBias - pw log2 sum_j 2^(c q_i.k_j)  (c = scale log2 e).
 // Pass 2 (alpha pass): D[128 keys x W rows] = K_tile Q_chunk^T; every TMEM lane
-//                      is one key, so sum_i 2^(2c L_ij + nob_i) = 2^kBias sum_i
-//                      alpha_ij^2 is a per-thread running sum; s_j = sqrt(sum/R)
-//                      2^(-kBias/2), or a per-group partial sum when R spans
-//                      several row groups (finished by score_finalize).
+//                      is one key, so sum_i 2^(pw c L_ij + nob_i) = 2^kBias sum_i
+//                      alpha_ij^pw is a per-thread running sum; with pw = 2 the
+//                      score s_j = sqrt(sum/R) 2^(-kBias/2), with pw = 1 the
+//                      action attention a_j = sum 2^(-kBias) (the attention all
+//                      rows pay to key j, "ActKV 解剖", first component); or a
+//                      per-group partial sum when R spans several row groups
+//                      (finished by score_finalize).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_run[q] = snew;
               }
           } else {
-            const float2 c2 = make_float2(2.0f * c, 2.0f * c);
+            const float2 c2 = make_float2(meta.pw * c, meta.pw * c);
             const float* ob = nob + u * meta.R_pad + (it.u.g * meta.gsub + j) * meta.W;
             for (int col0 = 0; col0 < meta.W; col0 += 128) {
               tmem_ld128(taddr + col0, v);
@@ -544,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (writer && key < it.u.n) {
             const int64_t o = ((int64_t)it.u.l * meta.H + it.u.h) * meta.Ntot + it.u.off + key;
             if (meta.ngroups == 1)
-              out2[o] = sqrtf(acc / (float)meta.R) * exp2f(-0.5f * kBias);
+              out2[o] = (meta.pw == 2.0f) ? sqrtf(acc / (float)meta.R) * exp2f(-0.5f * kBias)
+                                          : acc * exp2f(-kBias);
             else
               out2[(int64_t)it.u.g * meta.L * meta.H * meta.Ntot + o] = acc;
           }
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================== combine / offsets
 
 // Merges the pass-1 partials of each row into the pass-2 offset
-// nob_i = kBias - 2 log2 sum_j 2^(c L_ij) (rows >= R: -inf) and the natural-log
+// nob_i = kBias - pw log2 sum_j 2^(c L_ij) (rows >= R: -inf) and the natural-log
 // LSE.  One thread per (unit, row); the items of the companion pass-1 launch
 // start at seq.item1.
 __global__ void lse_combine_kernel(const __grid_constant__ LaunchMeta meta,
@@ -605,7 +609,7 @@ __global__ void lse_combine_kernel(const __grid_constant__ LaunchMeta meta,
         if (p.y > 0.0f) S += p.y * exp2f(p.x - M);
       }
     const float lg = M + log2f(S);  // log2 sum_j 2^(c L_ij)
-    nob[u * meta.R_pad + i] = kBias - 2.0f * lg;
+    nob[u * meta.R_pad + i] = kBias - meta.pw * lg;
     if (lse_out != nullptr) lse_out[u * meta.R + i] = lg * ln2;
   }
 }
@@ -625,21 +629,23 @@ __global__ void nob_from_lse_kernel(const __grid_constant__ LaunchMeta meta,
     const int l = (int)(local / meta.H);
     const int64_t u = ((int64_t)s.b * meta.L + l) * meta.H + h;
     nob[u * meta.R_pad + i] =
-        (i < meta.R) ? kBias - 2.0f * kLog2e * lse_in[u * meta.R + i] : -INFINITY;
+        (i < meta.R) ? kBias - meta.pw * kLog2e * lse_in[u * meta.R + i] : -INFINITY;
   }
 }
 
 // Scores from the per-row-group partial sums of pass 2 (R spanning several
-// groups): s = sqrt(sum_g part_g / R) 2^(-kBias/2).
+// groups): s = sqrt(sum_g part_g / R) 2^(-kBias/2) (pw = 2) or the action
+// attention sum_g part_g 2^(-kBias) (pw = 1).
 __global__ void score_finalize_kernel(const __grid_constant__ LaunchMeta meta,
                                       const float* __restrict__ part2, float* __restrict__ scores) {
   const int64_t LHN = (int64_t)meta.L * meta.H * meta.Ntot;
   const float unbias = exp2f(-0.5f * kBias);
+  const bool te = meta.pw == 2.0f;
   for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < LHN;
        g += (int64_t)gridDim.x * blockDim.x) {
     float acc = 0.0f;
     for (int q = 0; q < meta.ngroups; ++q) acc += part2[q * LHN + g];
-    scores[g] = sqrtf(acc / (float)meta.R) * unbias;
+    scores[g] = te ? sqrtf(acc / (float)meta.R) * unbias : acc * unbias * unbias;
   }
 }
 
