@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--scorer", choices=["te", "actkv"], default="te",
+                    help="eviction score: the token-eviction attention-mass score (default) or "
+                         "ActKV's action attention smoothed by LRFU")
     ap.add_argument("--variant", choices=["inplace", "sentinel", "fresh"], default="inplace",
                     help="eviction layout after selection: the in-place tail-region compaction "
                          "(default), sentinel dead slots, or compaction into fresh pages")
@@ -293,10 +296,21 @@ def our_arm(args):
         sp = dataclasses.replace(sp, headroom=max(sp.headroom, 0.35))
     case = workloads.build(sp, args.seed + rank, dev)
     m = budgets_lib(case)
+    aux = None
+    if args.scorer == "actkv":  # per-slot LRFU values, moved with their entries
+        aux = torch.zeros(case.tags.shape, dtype=torch.float32, device=dev)
     cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks,
                        case.free_ids, case.free_top, case.seg_start, case.seg_end, case.seq_len, m,
-                       sp.R)
+                       sp.R, aux=aux)
     snap = case.snapshot()
+    if aux is not None:
+        snap.append(aux.clone())
+        restore_core = case.restore
+
+        def restore_all(sn):
+            restore_core(sn[:-1])
+            aux.copy_(sn[-1])
+        case.restore = restore_all
     n = [e - s for s, e in zip(case.seg_start, case.seg_end)]
     entries = sp.L * sp.H * sum(n)
     stream = torch.cuda.current_stream()
@@ -304,9 +318,14 @@ def our_arm(args):
 
     def step(ev):
         ev[0].record(stream)
-        cp.score_lse(case.q, sp.scale)
-        ev[1].record(stream)
-        cp.score_alpha(case.q, sp.scale)
+        if args.scorer == "actkv":  # both scoring passes, then the LRFU step, in "score_alpha"
+            cp.score_action(case.q, sp.scale)
+            ev[1].record(stream)
+            cp.lrfu(0.9, 0.5)
+        else:
+            cp.score_lse(case.q, sp.scale)
+            ev[1].record(stream)
+            cp.score_alpha(case.q, sp.scale)
         ev[2].record(stream)
         cp.select()
         ev[3].record(stream)
@@ -383,6 +402,11 @@ def our_arm(args):
     dom_kernel = ("score_pass_kernel<128,2> (alpha pass)" if dom == "score_alpha"
                   else "score_pass_kernel<128,1> (LSE pass)")
     t_dom = per_stage[dom] * 1e-3
+    if args.scorer == "actkv":
+        # the "score_lse" stage holds both passes of the action attention: time them as one
+        # pass each (half the stage) against one Q K^T each
+        dom, dom_kernel = "score_lse", "score_pass_kernel<128,1>+<128,2> (action attention, per pass)"
+        t_dom = per_stage["score_lse"] * 1e-3 / 2.0
     # a pass reads every K row once and its Q group(s); the alpha pass also writes the scores.
     # The pass is bound by whichever of its flops (at the bf16 peak) or bytes (at the copy
     # peak) takes longer.
@@ -413,7 +437,7 @@ def our_arm(args):
                          "snapshot between steps, outside the timed events"
                          % (2 * case.k_pool.numel() * 2 / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "eviction_layout": args.variant},
+                   "eviction_layout": args.variant, "eviction_score": args.scorer},
         "roofline": roofline,
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
                           "F_alg": F_alg, "B_alg": B_alg, "moves": moves},
@@ -426,9 +450,10 @@ def our_arm(args):
         line["clocks"] = clocks.summary(w0, w1)
 
     # the end-to-end and CPU-baseline legs measure the default in-place chain only
-    if not args.no_e2e and args.variant == "inplace":
+    if not args.no_e2e and args.variant == "inplace" and args.scorer == "te":
         line["e2e"] = e2e_run(args, case, cp, snap, entries, world, dev)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "inplace":
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "inplace"
+            and args.scorer == "te"):
         case.restore(snap)  # the oracle reads the pristine cache
         torch.cuda.synchronize()
         line["cpu_baseline"] = cpu_baseline(case, budgets_oracle(case))

@@ -305,7 +305,8 @@ kvc_status kvc_score_action(const kvc_cache *cache, const kvc_segments *segs, co
  * kvc_select_topm).  hits (uint8 [L][H][Ntot], may be NULL) receives the
  * flags.  Masses are summed in 2^-40 fixed point (64-bit integers), so the
  * result does not depend on the order of the sums.  frac in [0, 1], lambda
- * finite and >= 0. */
+ * finite and >= 0; segments of at most 2^20 positions (KVC_ERR_UNSUPPORTED
+ * beyond). */
 kvc_status kvc_lrfu_update(const kvc_cache *cache, const kvc_segments *segs, const float *attn,
                            float frac, float lambda, float *crf_out, uint8_t *hits,
                            kvc_stream_t stream);

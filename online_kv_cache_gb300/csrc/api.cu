@@ -1050,6 +1050,10 @@ kvc_status kvc_lrfu_update(const kvc_cache* cache, const kvc_segments* segs, con
   Plan p;
   if ((st = build_plan(cache, segs, nullptr, &p)) != KVC_OK) return st;
   if (p.seqs.empty()) return ok();
+  for (const Seq& q : p.seqs)
+    if (q.n > kLrfuMaxSegment)
+      return fail(KVC_ERR_UNSUPPORTED, "segment of %d positions exceeds %d (LRFU mass histograms)", q.n,
+                  kLrfuMaxSegment);
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
   const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;

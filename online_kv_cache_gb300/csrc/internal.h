@@ -132,6 +132,10 @@ struct LrfuLaunch {
   unsigned* status = nullptr;
 };
 
+// Longest segment the LRFU kernel takes: its per-warp 16-bit mass parts stay
+// below 2^32 for up to 2^16 elements per warp (16 warps).
+constexpr int kLrfuMaxSegment = 1 << 20;
+
 cudaError_t launch_lrfu(const LrfuLaunch& ll, cudaStream_t stream);
 cudaError_t launch_sentinel(const LayoutLaunch& ll, cudaStream_t stream);
 cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream);

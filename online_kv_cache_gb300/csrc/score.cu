@@ -172,7 +172,10 @@ __device__ __forceinline__ void alpha2_cols(const float (&v)[128], const float* 
 // kst tiles keeps kst - 1 tiles in flight.  The block-table entries of the
 // next kPageRing - 1 tiles travel ahead of the K ring through cp.async into a
 // shared-memory ring, so no TMA issue waits on a global load.
-template <int D, int PASS>
+// PW (pass 2): the power of alpha summed per key -- 2 for the eviction score,
+// 1 for the action attention (a compile-time constant: the pass-2 epilogue
+// is sensitive to every instruction of its inner loop).
+template <int D, int PASS, int PW = 2>
 __global__ void __launch_bounds__(kThreads, 1)
     score_pass_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_run[q] = snew;
               }
           } else {
-            const float2 c2 = make_float2(meta.pw * c, meta.pw * c);
+            const float2 c2 = make_float2((float)PW * c, (float)PW * c);
             const float* ob = nob + u * meta.R_pad + (it.u.g * meta.gsub + j) * meta.W;
             for (int col0 = 0; col0 < meta.W; col0 += 128) {
               tmem_ld128(taddr + col0, v);
@@ -547,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (writer && key < it.u.n) {
             const int64_t o = ((int64_t)it.u.l * meta.H + it.u.h) * meta.Ntot + it.u.off + key;
             if (meta.ngroups == 1)
-              out2[o] = (meta.pw == 2.0f) ? sqrtf(acc / (float)meta.R) * exp2f(-0.5f * kBias)
-                                          : acc * exp2f(-kBias);
+              out2[o] = (PW == 2) ? sqrtf(acc / (float)meta.R) * exp2f(-0.5f * kBias)
+                                  : acc * exp2f(-kBias);
             else
               out2[(int64_t)it.u.g * meta.L * meta.H * meta.Ntot + o] = acc;
           }
@@ -658,16 +661,17 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
   if (dev < 64 && !attr_set[dev]) {
     // the register split inside the kernel assumes this launch allocation; a
     // build with any other count is refused rather than launched
-    cudaFuncAttributes fa1, fa2;
-    if ((e = cudaFuncGetAttributes(&fa1, score_pass_kernel<D, 1>)) != cudaSuccess) return e;
-    if ((e = cudaFuncGetAttributes(&fa2, score_pass_kernel<D, 2>)) != cudaSuccess) return e;
-    if (fa1.numRegs != kRegsLaunch || fa2.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(score_pass_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kScoreSmemLimit);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_pass_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kScoreSmemLimit);
-    if (e != cudaSuccess) return e;
+    const void* kernels[3] = {reinterpret_cast<const void*>(score_pass_kernel<D, 1>),
+                              reinterpret_cast<const void*>(score_pass_kernel<D, 2, 2>),
+                              reinterpret_cast<const void*>(score_pass_kernel<D, 2, 1>)};
+    for (const void* k : kernels) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
+      if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmemLimit)) !=
+          cudaSuccess)
+        return e;
+    }
     attr_set[dev] = true;
   }
   for (size_t c = 0; c < sl.chunks; ++c) {
@@ -705,8 +709,12 @@ cudaError_t launch_score_d(const ScoreLaunch& sl, cudaStream_t stream) {
         const int grid = (int)std::min<int64_t>(m2.items, sl.grid_limit);
         const int smem = score_smem_bytes(m2.qbytes, m2.kst, D);
         float* out = (m2.ngroups == 1) ? sl.scores : sl.part2;
-        score_pass_kernel<D, 2><<<grid, kThreads, smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,
-                                                                  nullptr, sl.obias, out, sl.status);
+        if (m2.pw == 1.0f)
+          score_pass_kernel<D, 2, 1><<<grid, kThreads, smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,
+                                                                       nullptr, sl.obias, out, sl.status);
+        else
+          score_pass_kernel<D, 2, 2><<<grid, kThreads, smem, stream>>>(*sl.tmK, *sl.tmQ2, m2, sl.block_table,
+                                                                       nullptr, sl.obias, out, sl.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
       }
