@@ -640,6 +640,10 @@ kvc_status kvc_select_topm(const kvc_cache* cache, const kvc_segments* segs, con
   if ((st = build_plan(cache, segs, m, &p)) != KVC_OK) return st;
   if (p.seqs.empty() || p.Mtot == 0) return ok();
   if (scores == nullptr || keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores or keep is NULL");
+  for (const Seq& q : p.seqs)
+    if (q.n >= kSelectMaxSegment)
+      return fail(KVC_ERR_UNSUPPORTED, "segment of %d positions: selection takes fewer than %d", q.n,
+                  kSelectMaxSegment);
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
   const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;

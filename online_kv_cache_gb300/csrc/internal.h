@@ -132,6 +132,10 @@ struct LrfuLaunch {
   unsigned* status = nullptr;
 };
 
+// Segments the selection kernel takes: its per-warp 16-bit bin counts see at
+// most n / 16 elements per pass.
+constexpr int kSelectMaxSegment = 1 << 20;
+
 // Longest segment the LRFU kernel takes: its per-warp 16-bit mass parts stay
 // below 2^32 for up to 2^16 elements per warp (16 warps).
 constexpr int kLrfuMaxSegment = 1 << 20;

@@ -8,7 +8,9 @@
 // One 512-thread CTA per unit.  Scores are >= 0, so their fp32 bit patterns
 // order like the values.  Three radix passes over the bits (11, 11, 10 from
 // the top) find the exact bit pattern T of the m-th largest score and how many
-// elements equal to T are kept (k_eq).  A final pass keeps every element > T
+// elements equal to T are kept (k_eq); each pass counts into warp-private
+// histograms with plain shared atomics (scores bunch into few bins, and
+// per-warp bins keep those updates from queueing across the block).  A final pass keeps every element > T
 // and the first k_eq elements == T, and writes each kept position at its rank
 // (warp ballots + a block scan of the warp counts).
 #include <cuda_runtime.h>
@@ -27,6 +29,10 @@ constexpr int kWarps = kSelThreads / 32;
 constexpr int kU = 8;                         // elements per thread per tile
 constexpr int kTileElems = kSelThreads * kU;  // element e of a tile: q * kSelThreads + tid
 constexpr int kBins = 2048;
+// warp-private count histograms: two 16-bit bin counts per 32-bit word (a warp
+// sees at most 2^16 - 1 elements of a unit per pass for n < 2^20)
+constexpr int kWarpWords = kBins / 2;
+constexpr size_t kSelSmem = (size_t)kWarps * kWarpWords * sizeof(uint32_t);
 
 // One CTA per unit.  Element i of a tile sits at tile + q * kSelThreads + tid, so
 // every load instruction is coalesced and the (q, warp, lane) order is the index
@@ -35,6 +41,7 @@ __global__ void __launch_bounds__(kSelThreads)
     select_topm_kernel(const __grid_constant__ LaunchMeta meta, const float* __restrict__ scores,
                        int32_t* __restrict__ keep) {
   __shared__ uint32_t hist[kBins];
+  extern __shared__ uint32_t whist[];  // [kWarps][kWarpWords]
   __shared__ uint32_t pre_gt[kU * kWarps], pre_eq[kU * kWarps];
   __shared__ uint32_t sh_digit, sh_k, sh_tot_gt, sh_tot_eq;
 
@@ -63,8 +70,9 @@ __global__ void __launch_bounds__(kSelThreads)
     const int width = pass == 2 ? 10 : 11;
     const uint32_t dmask = (1u << width) - 1u;
     const int nbins = 1 << width;
-    for (int i = tid; i < kBins; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
+    uint32_t* wh = whist + warp * kWarpWords;
+    for (int i = lane; i < kWarpWords; i += 32) wh[i] = 0;
+    __syncwarp();
 #pragma unroll 1
     for (int tile = 0; tile < n; tile += kTileElems) {
       uint32_t u[kU];
@@ -76,10 +84,18 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
       for (int q = 0; q < kU; ++q) {
         const int i = tile + q * kSelThreads + tid;
-        const uint32_t d = (i < n && (u[q] & pmask) == prefix) ? ((u[q] >> sh) & dmask) : 0xFFFFFFFFu;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+        if (i < n && (u[q] & pmask) == prefix) {
+          const uint32_t d = (u[q] >> sh) & dmask;
+          atomicAdd(&wh[d >> 1], (d & 1u) ? 0x10000u : 1u);
+        }
       }
+    }
+    __syncthreads();
+    for (int b = tid; b < nbins; b += kSelThreads) {
+      uint32_t c = 0;
+#pragma unroll 4
+      for (int w = 0; w < kWarps; ++w) c += (whist[w * kWarpWords + (b >> 1)] >> ((b & 1) * 16)) & 0xFFFFu;
+      hist[b] = c;
     }
     __syncthreads();
     if (warp == 0) {
@@ -186,10 +202,19 @@ __global__ void __launch_bounds__(kSelThreads)
 }  // namespace
 
 cudaError_t launch_select(const SelectLaunch& sl, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return e0;
+  if (dev >= 64 || !attr_set[dev]) {
+    e0 = cudaFuncSetAttribute(select_topm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmem);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 64) attr_set[dev] = true;
+  }
   for (size_t c = 0; c < sl.chunks; ++c) {
     const LaunchMeta& m = sl.meta[c];
     if (m.items <= 0) continue;
-    select_topm_kernel<<<(unsigned)m.items, kSelThreads, 0, stream>>>(m, sl.scores, sl.keep);
+    select_topm_kernel<<<(unsigned)m.items, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch();
