@@ -268,6 +268,33 @@ def profile_traffic(kernel: str, workload: str):
     return ent.get("dram_bytes_per_launch") if digest == ent.get("source_sha256_16") else None
 
 
+# ----------------------------------------------------------------------------- ranks
+#
+# Units (sequence, layer, KV head) are independent, so N GPUs run N replicas of the
+# workload (one per rank, seeded seed + rank) with no exchange on the data path.
+# The job ends when the slowest rank does: the step time is the maximum over ranks,
+# and the whole-job throughput counts every rank's entries.
+
+def replica_seed(seed: int, rank: int) -> int:
+    return seed + rank
+
+
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """Maximum over the ranks of a per-rank time (ms); world == 1 returns it unchanged."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(entries_per_rank: int, world: int, ms: float) -> float:
+    """Entries per second of the whole job: every rank's entries over the slowest step."""
+    return entries_per_rank * world / (ms * 1e-3)
+
+
 def our_arm(args):
     import torch
     import torch.distributed as dist
@@ -294,7 +321,7 @@ def our_arm(args):
         sp = dataclasses.replace(sp, L=args.layers)
     if args.variant == "fresh":  # the fresh pages come from the free stack: leave room for them
         sp = dataclasses.replace(sp, headroom=max(sp.headroom, 0.35))
-    case = workloads.build(sp, args.seed + rank, dev)
+    case = workloads.build(sp, replica_seed(args.seed, rank), dev)
     m = budgets_lib(case)
     aux = None
     if args.scorer == "actkv":  # per-slot LRFU values, moved with their entries
@@ -374,11 +401,7 @@ def our_arm(args):
     per_step = [events[k][0].elapsed_time(events[k][6]) for k in range(args.steps)]
     per_stage = {s: statistics.mean(events[k][i].elapsed_time(events[k][i + 1])
                                     for k in range(args.steps)) for i, s in enumerate(stages)}
-    ms = statistics.mean(per_step)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(statistics.mean(per_step), world, dev)
     if clocks:
         time.sleep(0.15)
         clocks.stop()
@@ -429,7 +452,7 @@ def our_arm(args):
     gbs = compact_bytes / (per_stage["compact"] * 1e-3) / 1e9 if per_stage["compact"] > 0 else 0.0
 
     line = {
-        "metric": METRIC, "value": entries * world / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(entries, world, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(sp), "entries_per_step": entries,
@@ -501,12 +524,8 @@ def e2e_run(args, case, cp, snap, entries, world, dev):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": entries * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms = slowest_rank_ms(e0.elapsed_time(e1) / steps, world, dev)
+    return {"value": job_throughput(entries, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
 
 
