@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(256)
   constexpr int LPM = D / 4;     // lanes per move
   constexpr int MPW = 32 / LPM;  // moves per warp step
   constexpr int CH = D / 8;      // 16-byte chunks per row
-  constexpr int U = 4;           // moves in flight per lane group
+  constexpr int U = 1;           // moves in flight per lane group (more resident warps beat more per thread)
   constexpr int64_t kRowBytes = (int64_t)D * 2;
   const int64_t item = blockIdx.x;
   const int si = find_seq(meta, item);
