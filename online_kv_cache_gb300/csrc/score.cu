@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Load order per item: its first min(kst-1, tiles) K tiles, then its Q group
     // (sub-tile by sub-tile as the previous item releases them), then the rest.
     uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0}, qc = 0;
+    int pks = 0;        // K ring stage of the next tile and its phase parity
+    uint32_t pkph = 0;
     bool ok = true;
     const int ppt = kTile / meta.P;  // pages per key tile (<= kPagesPerTileMax)
     // Page-ring cursor: one commit group per key tile of this CTA, in K order;
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           prow = ((kit_.u.l * meta.num_pages + page) * meta.H + kit_.u.h) * meta.P;
       }
 
-      const int ks = kcount % kst;
-      if (lane == 0) ok = mbar_wait(&k_empty[ks], ((kcount / kst) & 1) ^ 1, abort_flag, status);
+      const int ks = pks;
+      if (lane == 0) ok = mbar_wait(&k_empty[ks], pkph ^ 1u, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const unsigned valid = __ballot_sync(0xffffffffu, prow >= 0);
@@ -326,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(dst + p * meta.P * C::kKPageBytesPerRow, &tmK, &k_full[ks], 0, 0, 0, row >> 3);
       }
       ++kcount;
+      if (++pks == kst) {
+        pks = 0;
+        pkph ^= 1u;
+      }
       if (++kt >= kit_.t1) {
         k_item += gridDim.x;
         if (k_item < meta.items) {
@@ -353,8 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the 16-byte-unit offset of each k-step to the start-address field.
     if (lane == 0) {
       const uint32_t idesc = (PASS == 1) ? idesc_bf16_f32(kTile, kTile) : idesc_bf16_f32(kTile, meta.W);
-      uint32_t kcount = 0, q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
+      uint32_t q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
       uint32_t slot = 0, use = 0;  // accumulator slot of the next job and its use count
+      int ks = 0;                  // K ring stage of the next tile and its phase parity
+      uint32_t kph = 0;
       uint32_t qc = 0, dc = 0;
       bool issued = false, ok = true;
       const uint32_t q_base = smem_u32(sQ);
@@ -387,8 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         for (int t = it.t0; t < it.t1 && ok; ++t) {
-          const int ks = kcount % kst;
-          if (!(ok = mbar_wait(&k_full[ks], (kcount / kst) & 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait(&k_full[ks], kph, abort_flag, status))) break;
           const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + ks * C::kTileBytes), C::kKGroup);
           for (int j = 0; j < it.J; ++j) {
             if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status))) break;
@@ -419,7 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(&k_empty[ks]);
-          ++kcount;
+          if (++ks == kst) {
+            ks = 0;
+            kph ^= 1u;
+          }
         }
         for (int j = 0; j < it.J; ++j) ++q_use[j];
       }
