@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (small profiling cases)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="keep the workload's first N sequences (small profiling cases)")
     return ap.parse_args()
 
 
@@ -322,6 +324,9 @@ def our_arm(args):
     sp = workloads.spec(args.workload, args.seed)
     if args.layers:
         sp = dataclasses.replace(sp, L=args.layers)
+    if args.seqs:
+        bud = sp.budget if sp.budget[0] != "actkv" else ("actkv", sp.budget[1][:args.seqs])
+        sp = dataclasses.replace(sp, lengths=sp.lengths[:args.seqs], budget=bud)
     if args.variant == "fresh":  # the fresh pages come from the free stack: leave room for them
         sp = dataclasses.replace(sp, headroom=max(sp.headroom, 0.35))
     case = workloads.build(sp, replica_seed(args.seed, rank), dev)

@@ -288,15 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qpar = (PASS == 1) ? ((qc >> 1) & 1) : (q_use[j] & 1);
           if (lane == 0) {
             ok = mbar_wait(&q_empty[qs], qpar ^ 1, abort_flag, status);
-            if (ok) {
-              mbar_arrive_expect_tx(&q_full[qs], sub_bytes);
-#pragma unroll
-              for (int kb = 0; kb < C::KB; ++kb)
-                tma_load_2d(sQ + (qs * C::KB + kb) * sub_rows * 128, &tmQ, &q_full[qs], kb * 64,
-                            qrow + j * sub_rows);
-            }
+            if (ok) mbar_arrive_expect_tx(&q_full[qs], sub_bytes);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok && lane < C::KB)  // lane kb: k-block kb of the sub-tile
+            tma_load_2d(sQ + (qs * C::KB + lane) * sub_rows * 128, &tmQ, &q_full[qs], lane * 64,
+                        qrow + j * sub_rows);
           ++q_use[j];
           ++qc;
         }
@@ -321,12 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const unsigned valid = __ballot_sync(0xffffffffu, prow >= 0);
       if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], __popc(valid) * C::KB * meta.P * 128);
-      uint8_t* dst = sK + ks * C::kTileBytes;
-      for (int p = 0; p < ppt; ++p) {
-        const int32_t row = __shfl_sync(0xffffffffu, prow, p);
-        if (lane == 0 && row >= 0)  // the page's P keys, every k-block, in one copy
-          tma_load_4d(dst + p * meta.P * C::kKPageBytesPerRow, &tmK, &k_full[ks], 0, 0, 0, row >> 3);
-      }
+      __syncwarp();
+      // Lane p copies page p of the tile (its P keys, every k-block) and all the
+      // lanes issue in one instruction: a single issuing lane tops out near
+      // 2.6 TB/s of 4 KB pages on the whole GPU, one page per lane near 5.5 TB/s.
+      if (prow >= 0)
+        tma_load_4d(sK + ks * C::kTileBytes + lane * meta.P * C::kKPageBytesPerRow, &tmK, &k_full[ks], 0, 0, 0,
+                    prow >> 3);
       ++kcount;
       if (++pks == kst) {
         pks = 0;
