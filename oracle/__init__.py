@@ -21,7 +21,10 @@ function cites the page passage it restates:
   action attention mass) smoothed by LRFU (lambda = 0.5) into the eviction score;
 * sentinel eviction / fresh-page compaction -- the layout-preserving dead
   slot (K = -10^4, V = 0) of the IntentKV page, and an order-preserving
-  compaction into freshly allocated pages.
+  compaction into freshly allocated pages;
+* Attention Matching (``oracle/am.py``, numpy fp64) -- the bias beta and the
+  compact values V_C fitted on the survivors, from the tutorial page's section
+  on the two compaction families.
 
 Parity status: the score, selection and compaction functions are pinned by the
 tests under ``tests/test_oracle_*.py`` (closed forms, invariants, brute force
