@@ -101,7 +101,8 @@ typedef struct kvc_cache {
     int32_t batch;        /* B */
     float *aux;           /* fp32 [L][num_pages][H][P]: per-slot state that
                            * travels with its entry through kvc_compact (the
-                           * LRFU values of kvc_lrfu_update), or NULL */
+                           * LRFU values of kvc_lrfu_update, the bias beta
+                           * of kvc_am_fit), or NULL */
 } kvc_cache;
 
 /* One segment per sequence, all host memory ([SE]: the application names the
@@ -359,6 +360,41 @@ kvc_status kvc_plan_fresh(const kvc_cache *cache, const kvc_segments *segs, cons
  * or from this step's own capacity check) it changes nothing. */
 kvc_status kvc_commit_fresh(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                             const kvc_allocator *alloc, const kvc_plan *plan, kvc_stream_t stream);
+
+/* ------------------------------------------------------ Attention Matching */
+
+/* Bytes of workspace kvc_am_fit needs: per (layer, head, sequence with m > 0)
+ * about 4 * ((R + m) * (m + 4) + R * (d + 1) + m * (d + 1)) bytes. */
+kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                                 int32_t R, size_t *bytes);
+
+/* Attention Matching on the survivors ([TE], section on the two compaction
+ * families): with K_C the kept keys (`keep`, as written by kvc_select_topm),
+ * fits an additive bias beta per kept key and compact values V_C so that the
+ * compacted attention reproduces the full one on the proxy rows q:
+ *   min_beta || exp(Q K_C^T + beta) 1_m - exp(Q K^T) 1_n ||^2
+ *   min_V_C  || softmax(Q K_C^T + beta) V_C - softmax(Q K^T) V ||_F^2
+ * (logits carry `scale`).  With w = exp(beta) >= 0 the first fit is
+ * non-negative least squares; both run `sweeps` sweeps of cyclic coordinate
+ * descent on their normal equations over the kept keys in ascending position
+ * order, from token eviction's answer (beta = 0, V_C = the kept V rows), the
+ * first projected onto w >= 0; the second uses the fitted beta.  sweeps in
+ * [0, 1000]; 0 leaves token eviction's answer.  fp32 throughout (CUDA cores).
+ * Effects: every kept entry's V row becomes its V_C row (bf16, round to
+ * nearest even) and, when cache->aux is not NULL, its per-slot state becomes
+ * beta (-inf where w = 0: the key is masked); kvc_compact then moves both with
+ * the entry.  K rows and tags are untouched.
+ *   m     host [batch] budgets (clamped to n_b); every m_b <= 2048
+ *   q     bf16 [B][L][H][R][d], R <= 4096, as for kvc_score
+ *   keep  int32 [L][H][Mtot] ascending segment positions (kvc_select_topm)
+ *   beta  out fp32 [L][H][Mtot] or NULL
+ *   vc    out fp32 [L][H][Mtot][d] (V_C before rounding) or NULL
+ *   ws    kvc_am_workspace_size bytes, 256-byte aligned
+ * A keep position outside its segment sets KVC_DEV_BAD_KEEP, a block-table
+ * entry outside the pool KVC_DEV_BAD_PAGE (that entry is skipped). */
+kvc_status kvc_am_fit(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
+                      const uint16_t *q, int32_t R, float scale, const int32_t *keep, int32_t sweeps,
+                      float *beta, float *vc, void *ws, size_t ws_bytes, kvc_stream_t stream);
 
 /* -------------------------------------------------------------- helpers */
 

@@ -46,7 +46,7 @@ EXPORTED = (
     "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
     "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc", "kvc_evict_sentinel",
     "kvc_plan_fresh_buffer_sizes", "kvc_plan_fresh", "kvc_commit_fresh", "kvc_score_action",
-    "kvc_lrfu_update",
+    "kvc_lrfu_update", "kvc_am_workspace_size", "kvc_am_fit",
 )
 
 
@@ -142,6 +142,8 @@ def lib():
             "kvc_commit_fresh": (I32, [C, SG, P, A, PL, P]),
             "kvc_score_action": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
             "kvc_lrfu_update": (I32, [C, SG, P, F, F, P, P, P]),
+            "kvc_am_workspace_size": (I32, [C, SG, P, I32, ctypes.POINTER(S)]),
+            "kvc_am_fit": (I32, [C, SG, P, P, I32, F, P, I32, P, P, P, S, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -401,6 +403,25 @@ def kvc_lrfu_update(cache: Cache, segs: Segments, attn: torch.Tensor, frac: floa
            "kvc_lrfu_update")
 
 
+def kvc_am_workspace_size(cache: Cache, segs: Segments, m, R: int) -> int:
+    mm = _host_i32(m)
+    out = ctypes.c_size_t(0)
+    _check(lib().kvc_am_workspace_size(cache.ref, segs.ref, mm.ctypes.data, int(R), ctypes.byref(out)),
+           "kvc_am_workspace_size")
+    return int(out.value)
+
+
+def kvc_am_fit(cache: Cache, segs: Segments, m, q: torch.Tensor, R: int, scale: float,
+               keep: torch.Tensor, sweeps: int, beta: Optional[torch.Tensor], vc: Optional[torch.Tensor],
+               ws: torch.Tensor, stream=None):
+    mm = _host_i32(m)
+    _check(lib().kvc_am_fit(cache.ref, segs.ref, mm.ctypes.data, _dev_ptr(q, "q", torch.bfloat16), int(R),
+                            float(scale), _dev_ptr(keep, "keep", torch.int32), int(sweeps),
+                            _dev_ptr(beta, "beta", torch.float32), _dev_ptr(vc, "vc", torch.float32),
+                            _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+           "kvc_am_fit")
+
+
 def kvc_status_string(status: int) -> str:
     return lib().kvc_status_string(int(status)).decode()
 
@@ -483,6 +504,18 @@ class Compactor:
              stream=None):
         """One LRFU step on the cache's aux values; the new values become self.scores."""
         kvc_lrfu_update(self.cache, self.segs, self.attn, frac, lam, self.scores, hits, stream)
+
+    def am_fit(self, q: torch.Tensor, scale: float, sweeps: int = 8, keep: Optional[torch.Tensor] = None,
+               beta: Optional[torch.Tensor] = None, vc: Optional[torch.Tensor] = None, stream=None):
+        """Attention Matching on the kept entries: beta into the cache's aux values (when it has
+        them) and `beta`, V_C over the kept V rows and into `vc`."""
+        if getattr(self, "am_ws", None) is None:
+            nbytes = max(256, kvc_am_workspace_size(self.cache, self.segs, self.m, self.R))
+            self.am_ws_raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.keep.device)
+            off = (-self.am_ws_raw.data_ptr()) % 256
+            self.am_ws = self.am_ws_raw[off:off + nbytes]
+        kvc_am_fit(self.cache, self.segs, self.m, q, self.R, scale, self.keep if keep is None else keep,
+                   sweeps, beta, vc, self.am_ws, stream)
 
     def select(self, stream=None):
         kvc_select_topm(self.cache, self.segs, self.scores, self.m, self.keep, None, stream)

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvc.so")
-SOURCES = ["api.cu", "score.cu", "select.cu", "compact.cu", "layout.cu", "actkv.cu"]
+SOURCES = ["api.cu", "score.cu", "select.cu", "compact.cu", "layout.cu", "actkv.cu", "am.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,678 @@
+// am.cu -- Attention Matching on the token-eviction survivors.
+//
+// Source: "Practical Online KV Cache Compaction for LLM Agents: An Empirical
+// Study" (agifrontier tutorial page), section on the two compaction families:
+// after the top-m keys K_C are chosen, AM fits an additive attention bias beta
+// (one value per kept key) and compact values V_C so that, on the proxy
+// queries Q, the compacted attention reproduces the full one:
+//   min_beta || exp(Q K_C^T + beta) 1_m - exp(Q K^T) 1_n ||^2      (mass fit)
+//   min_V_C  || A_hat(Q; K_C, beta, V_C) - A(Q; K, V) ||_F^2        (value fit)
+//
+// With w = exp(beta) >= 0 the mass fit is non-negative least squares in w.
+// Both fits run as cyclic coordinate descent on their normal equations,
+// starting from token eviction's own answer (w = 1, V_C = the kept values),
+// T sweeps over the kept keys in ascending position order; every logit of a
+// unit is shifted by c = max_i LSE_i, which changes neither minimiser.
+//
+// Work is fp32 on the CUDA cores: the fits are ill-conditioned (exp of
+// logits), so their Gram matrices cannot take the 8-bit-mantissa rounding of a
+// bf16 or tf32 tensor-core contraction.  Per unit the kernels run
+//   am_targets_kernel  Y = softmax(L) V and LSE over all n keys (online softmax)
+//   am_exp_kernel      E = exp(L_C - c) over the kept keys, s = exp(LSE - c)
+//   am_atb_kernel      G = E^T [E | s]              (mode 0)
+//   am_mass_kernel     w by projected coordinate descent; beta = ln w
+//   am_probs_kernel    Ph = rows of E diag(w), normalised (in place)
+//   am_atb_kernel      H = Ph^T Ph, Bm = Ph^T Y     (modes 1, 2)
+//   am_value_kernel    V_C by coordinate descent; written to the pool (bf16)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kAmThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// A coordinate moves only when its gradient exceeds 2^-14 of the scale of the
+// gradient's own terms: the normal equations square cond(E), which reaches
+// 1e14 on concentrated attention, and an fp32 gradient carries about 2e-6 of
+// that scale in rounding (row masses through an fp32 LSE, Gram sums over R
+// rows); below the guard the gradient is rounding, not signal.
+constexpr float kAmGuard = 6.103515625e-05f;  // 2^-14
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float* out) {
+  out[0] = bf16_bits_to_float(v.x & 0xffffu);
+  out[1] = bf16_bits_to_float(v.x >> 16);
+  out[2] = bf16_bits_to_float(v.y & 0xffffu);
+  out[3] = bf16_bits_to_float(v.y >> 16);
+  out[4] = bf16_bits_to_float(v.z & 0xffffu);
+  out[5] = bf16_bits_to_float(v.z >> 16);
+  out[6] = bf16_bits_to_float(v.w & 0xffffu);
+  out[7] = bf16_bits_to_float(v.w >> 16);
+}
+
+struct AmUnit {
+  int k;        // sequence index within the launch
+  int l, h;
+  int b, s0, n, m, ldE;
+  int64_t moff;
+  float* base;  // the unit's workspace
+};
+
+__device__ __forceinline__ AmUnit am_unit(const AmMeta& meta, int64_t unit, float* ws) {
+  int lo = 0, hi = meta.nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (meta.seq[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+  }
+  const AmSeq& q = meta.seq[lo];
+  const int r = (int)(unit - q.unit0);
+  AmUnit u;
+  u.k = lo;
+  u.l = r / meta.H;
+  u.h = r % meta.H;
+  u.b = q.b;
+  u.s0 = q.s0;
+  u.n = q.n;
+  u.m = q.m;
+  u.ldE = q.ldE;
+  u.moff = q.moff;
+  u.base = ws + q.ws + (int64_t)r * q.unit_floats;
+  return u;
+}
+
+// Pool row of segment position `pos` of the unit, or -1 (bad page, reported).
+__device__ __forceinline__ int64_t am_row(const AmMeta& meta, const AmUnit& u, const int32_t* bt, int pos,
+                                          unsigned* status) {
+  const int slot = u.s0 + pos;
+  const int32_t page = bt[(int64_t)u.b * meta.max_blocks + slot / meta.P];
+  if (page < 0 || page >= meta.num_pages) {
+    atomicOr(status, KVC_DEV_BAD_PAGE);
+    return -1;
+  }
+  return (((int64_t)u.l * meta.num_pages + page) * meta.H + u.h) * meta.P + slot % meta.P;
+}
+
+// Kept position j of the unit, or -1 (outside the segment, reported).
+__device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, const int32_t* keep, int j,
+                                       unsigned* status) {
+  const int pos = keep[((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff + j];
+  if (pos < 0 || pos >= u.n) {
+    atomicOr(status, KVC_DEV_BAD_KEEP);
+    return -1;
+  }
+  return pos;
+}
+
+// 64 rows x D of a bf16 matrix into shared memory (fp32, row stride D + 1),
+// zero rows where row_of(i) < 0.  16-byte loads, consecutive threads along a row.
+template <int D, typename RowOf>
+__device__ __forceinline__ void load_rows64(float* dst, const uint16_t* src, RowOf row_of) {
+  constexpr int kChunks = D / 8;
+  for (int ci = threadIdx.x; ci < 64 * kChunks; ci += kAmThreads) {
+    const int i = ci / kChunks, dc = ci % kChunks;
+    const int64_t row = row_of(i);
+    float v[8];
+    if (row >= 0) {
+      unpack8(*reinterpret_cast<const uint4*>(src + row * D + dc * 8), v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[i * (D + 1) + dc * 8 + e] = v[e];
+  }
+}
+
+// acc[a][b] = sum_k A[ty + 16a][k] * B[tx + 16b][k] over 64 x 64 tiles (stride D + 1).
+template <int D>
+__device__ __forceinline__ void dot64(const float* As, const float* Bs, int ty, int tx, float acc[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < D; ++k) {
+    float qa[4], kb[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) qa[a] = As[(ty + 16 * a) * (D + 1) + k];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) kb[b] = Bs[(tx + 16 * b) * (D + 1) + k];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qa[a], kb[b], acc[a][b]);
+  }
+}
+
+__device__ __forceinline__ float max16(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int D>
+constexpr int targets_smem_bytes() {
+  return (2 * 64 * (D + 1) + 64 * D + 64 * 65) * 4;
+}
+
+// ------------------------------------------------------------------ targets
+// Block = (unit, 64 proxy rows).  Online softmax over all n keys of the
+// segment: per row the running max, the running sum and Y = sum_j p_ij v_j.
+// Writes LSE (natural log) and Y = softmax(L) V to the unit's workspace.
+template <int D>
+__global__ void __launch_bounds__(kAmThreads) am_targets_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                                const uint16_t* __restrict__ kp,
+                                                                const uint16_t* __restrict__ vp,
+                                                                const uint16_t* __restrict__ q, float* ws,
+                                                                unsigned* status) {
+  extern __shared__ __align__(16) float am_smem[];
+  float* Qs = am_smem;                 // [64][D + 1]
+  float* Ks = Qs + 64 * (D + 1);       // [64][D + 1]
+  float* Vs = Ks + 64 * (D + 1);       // [64][D]
+  float* Ps = Vs + 64 * D;             // [64][65]
+  const int rb = (meta.R + 63) / 64;
+  const int64_t unit = blockIdx.x / rb;
+  const int r0 = (int)(blockIdx.x % rb) * 64;
+  const AmUnit u = am_unit(meta, unit, ws);
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int64_t qrow0 = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
+  load_rows64<D>(Qs, q, [&](int i) -> int64_t { return r0 + i < meta.R ? qrow0 + r0 + i : -1; });
+  const float c2 = meta.scale * kLog2e;
+  float mx[4], sm[4], y[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    mx[a] = -INFINITY;
+    sm[a] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) y[a][e] = 0.0f;
+  }
+  for (int j0 = 0; j0 < u.n; j0 += 64) {
+    __syncthreads();  // previous tile's Ks, Vs, Ps fully read
+    auto row_of = [&](int i) -> int64_t { return j0 + i < u.n ? am_row(meta, u, bt, j0 + i, status) : -1; };
+    load_rows64<D>(Ks, kp, row_of);
+    {  // values, row stride D
+      constexpr int kChunks = D / 8;
+      for (int ci = threadIdx.x; ci < 64 * kChunks; ci += kAmThreads) {
+        const int i = ci / kChunks, dc = ci % kChunks;
+        const int64_t row = row_of(i);
+        float v[8];
+        if (row >= 0) {
+          unpack8(*reinterpret_cast<const uint4*>(vp + row * D + dc * 8), v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Vs[i * D + dc * 8 + e] = v[e];
+      }
+    }
+    __syncthreads();
+    float acc[4][4];
+    dot64<D>(Qs, Ks, ty, tx, acc);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float t[4], tmax = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        t[b] = (j0 + tx + 16 * b < u.n) ? acc[a][b] * c2 : -INFINITY;
+        tmax = fmaxf(tmax, t[b]);
+      }
+      const float mnew = fmaxf(mx[a], max16(tmax));
+      const float alpha = exp2f(mx[a] - mnew);  // 0 on the first tile (mx = -inf)
+      float ps = 0.0f;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float p = exp2f(t[b] - mnew);
+        Ps[(ty + 16 * a) * 65 + tx + 16 * b] = p;
+        ps += p;
+      }
+      sm[a] = sm[a] * alpha + sum16(ps);
+      mx[a] = mnew;
+#pragma unroll
+      for (int e = 0; e < D / 16; ++e) y[a][e] *= alpha;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int j = 0; j < 64; ++j) {
+      float pv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) pv[a] = Ps[(ty + 16 * a) * 65 + j];
+#pragma unroll
+      for (int e = 0; e < D / 16; ++e) {
+        const float v = Vs[j * D + tx + 16 * e];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) y[a][e] = fmaf(pv[a], v, y[a][e]);
+      }
+    }
+  }
+  float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
+  float* lse = u.base + am_off_lse(meta.R, u.m, u.ldE, D);
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = r0 + ty + 16 * a;
+    if (i >= meta.R) continue;
+    const float inv = 1.0f / sm[a];
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) Y[(int64_t)i * D + tx + 16 * e] = y[a][e] * inv;
+    if (tx == 0) lse[i] = (mx[a] + log2f(sm[a])) * kLn2;
+  }
+}
+
+template <int D>
+constexpr int exp_smem_bytes() {
+  return (2 * 64 * (D + 1) + 8) * 4;
+}
+
+// ------------------------------------------------------------------ exp
+// Block = (unit, 64 proxy rows, 64 kept keys): E[i][j] = exp(L_ij - c) with
+// c = max_i LSE_i, and (key block 0) column m = s_i = exp(LSE_i - c).
+template <int D>
+__global__ void __launch_bounds__(kAmThreads) am_exp_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                            const uint16_t* __restrict__ kp,
+                                                            const uint16_t* __restrict__ q,
+                                                            const int32_t* __restrict__ keep, float* ws,
+                                                            unsigned* status) {
+  extern __shared__ __align__(16) float am_smem[];
+  float* Qs = am_smem;            // [64][D + 1]
+  float* Ks = Qs + 64 * (D + 1);  // [64][D + 1]
+  float* red = Ks + 64 * (D + 1); // [8]
+  const int rb = (meta.R + 63) / 64;
+  const int cb = (meta.max_m + 63) / 64;
+  const int cblk = (int)(blockIdx.x % cb);
+  const int64_t rest = blockIdx.x / cb;
+  const int r0 = (int)(rest % rb) * 64;
+  const AmUnit u = am_unit(meta, rest / rb, ws);
+  if (cblk * 64 >= u.m) return;
+  const float* lse = u.base + am_off_lse(meta.R, u.m, u.ldE, D);
+  // c = max_i LSE_i of the unit
+  float c = -INFINITY;
+  for (int i = threadIdx.x; i < meta.R; i += kAmThreads) c = fmaxf(c, lse[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int64_t qrow0 = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
+  load_rows64<D>(Qs, q, [&](int i) -> int64_t { return r0 + i < meta.R ? qrow0 + r0 + i : -1; });
+  const int j0 = cblk * 64;
+  load_rows64<D>(Ks, kp, [&](int i) -> int64_t {
+    if (j0 + i >= u.m) return -1;
+    const int pos = am_kept(meta, u, keep, j0 + i, status);
+    return pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
+  });
+  __syncthreads();
+  c = red[0];
+#pragma unroll
+  for (int w = 1; w < kAmThreads / 32; ++w) c = fmaxf(c, red[w]);
+  float acc[4][4];
+  dot64<D>(Qs, Ks, ty, tx, acc);
+  const float c2 = meta.scale * kLog2e, cc = c * kLog2e;
+  float* E = u.base;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = r0 + ty + 16 * a;
+    if (i >= meta.R) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int j = j0 + tx + 16 * b;
+      if (j < u.m) E[(int64_t)i * u.ldE + j] = exp2f(fmaf(acc[a][b], c2, -cc));
+    }
+    if (cblk == 0 && tx == 0) E[(int64_t)i * u.ldE + u.m] = exp2f((lse[i] - c) * kLog2e);
+  }
+}
+
+// ------------------------------------------------------------------ A^T B
+// Block = (unit, 64 x 64 tile of C): C[p][q] = sum_i A[i][p] B[i][q] over the
+// R proxy rows, 16 rows per step through shared memory.
+//   mode 0: A = E (m columns), B = [E | s] (m + 1), C = G        (stride ldE)
+//   mode 1: A = B = Ph (m columns),                 C = H in G's place
+//   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d)
+__global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, float* ws, int mode) {
+  __shared__ float As[16][64];
+  __shared__ float Bs[16][64];
+  const int mt = (meta.max_m + 63) / 64;
+  const int nt = mode == 2 ? (meta.d + 63) / 64 : (meta.max_m + 1 + 63) / 64;
+  const int ni = (int)(blockIdx.x % nt);
+  const int mi = (int)((blockIdx.x / nt) % mt);
+  const AmUnit u = am_unit(meta, blockIdx.x / ((int64_t)nt * mt), ws);
+  const int M = u.m;
+  const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
+  const int p0 = mi * 64, q0 = ni * 64;
+  if (p0 >= M || q0 >= N) return;
+  const float* A = u.base;
+  const int lda = u.ldE;
+  const float* B = mode == 2 ? u.base + am_off_Y(meta.R, u.m, u.ldE) : u.base;
+  const int ldb = mode == 2 ? meta.d : u.ldE;
+  float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
+  const int ldc = mode == 2 ? meta.d : u.ldE;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  float acc[4][4] = {};
+  for (int i0 = 0; i0 < meta.R; i0 += 16) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e = threadIdx.x + r * kAmThreads;
+      const int ii = e >> 6, pp = e & 63;
+      const bool in = i0 + ii < meta.R;
+      As[ii][pp] = (in && p0 + pp < M) ? A[(int64_t)(i0 + ii) * lda + p0 + pp] : 0.0f;
+      Bs[ii][pp] = (in && q0 + pp < N) ? B[(int64_t)(i0 + ii) * ldb + q0 + pp] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = As[i][ty + 16 * a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bv[b] = Bs[i][tx + 16 * b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int p = p0 + ty + 16 * a;
+    if (p >= M) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int qq = q0 + tx + 16 * b;
+      if (qq < N) C[(int64_t)p * ldc + qq] = acc[a][b];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ mass fit
+// Block = unit.  Projected cyclic coordinate descent on min_{w >= 0} ||E w - s||^2
+// from w = 1: with g = G w - b, coordinate j moves to max(0, w_j - g_j / G_jj)
+// and g follows by the change times column j of G (= row j, G symmetric).
+// Coordinate j moves only when |g_j| > 2^-14 b_j (every term of G w and of
+// b = E^T s is >= 0, so b_j is their scale).  Row j + 1 of G streams into
+// shared memory while step j runs.  Two barriers per step: every thread reads
+// g_j and w_j before any of them is updated.
+// Writes w (workspace), beta = ln w (-inf at 0) to `beta` and to the per-slot
+// state of each kept entry.
+__global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                             const int32_t* __restrict__ keep, float* ws,
+                                                             float* aux, float* beta, unsigned* status) {
+  extern __shared__ __align__(16) float am_smem[];
+  const AmUnit u = am_unit(meta, blockIdx.x, ws);
+  const int m = u.m;
+  float* g = am_smem;         // [m]
+  float* w = g + m;           // [m]
+  float* diag = w + m;        // [m]
+  float* bvec = diag + m;     // [m] b = E^T s
+  float* rows = bvec + m;     // [2][m]
+  const float* G = u.base + am_off_G(meta.R, u.ldE);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < m; i += kAmThreads / 32) {  // g = G 1 - b, one warp per row
+    const float* gr = G + (int64_t)i * u.ldE;
+    float acc = 0.0f;
+    for (int k = lane; k < m; k += 32) acc += gr[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      g[i] = acc - gr[m];
+      bvec[i] = gr[m];
+      diag[i] = gr[i];
+      w[i] = 1.0f;
+    }
+  }
+  const int64_t steps = (int64_t)meta.sweeps * m;
+  if (steps > 0) {
+    for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + i, G + i);
+    cp_async_commit();
+  }
+  for (int64_t st = 0; st < steps; ++st) {
+    const int j = (int)(st % m);
+    const int buf = (int)(st & 1);
+    if (st + 1 < steps) {  // prefetch the next step's row (its buffer was read in step st - 1)
+      const float* nr = G + (int64_t)((st + 1) % m) * u.ldE;
+      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + (buf ^ 1) * m + i, nr + i);
+    }
+    cp_async_commit();
+    cp_async_wait_group<1>();
+    __syncthreads();
+    const float gj = g[j], wj = w[j], Gjj = diag[j];
+    const float nw = (Gjj > 0.0f && fabsf(gj) > kAmGuard * bvec[j]) ? fmaxf(0.0f, wj - gj / Gjj) : wj;
+    const float dl = nw - wj;
+    __syncthreads();
+    if (dl != 0.0f) {
+      const float* rj = rows + buf * m;
+      for (int i = threadIdx.x; i < m; i += kAmThreads) g[i] = fmaf(dl, rj[i], g[i]);
+      if (threadIdx.x == 0) w[j] = nw;
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  float* wout = u.base + am_off_w(meta.R, m, u.ldE, meta.d);
+  const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
+  for (int j = threadIdx.x; j < m; j += kAmThreads) {
+    const float wj = w[j];
+    wout[j] = wj;
+    const float bj = wj > 0.0f ? logf(wj) : -INFINITY;
+    if (beta != nullptr) beta[orow + j] = bj;
+    if (aux != nullptr) {
+      const int pos = am_kept(meta, u, keep, j, status);
+      const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
+      if (row >= 0) aux[row] = bj;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ compact probabilities
+// Block = (unit, 8 proxy rows), one warp per row: z_i = sum_j E_ij w_j, then
+// Ph_ij = E_ij w_j / z_i in place (a row without mass stays zero).
+__global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta, float* ws) {
+  const int rb = (meta.R + 7) / 8;
+  const AmUnit u = am_unit(meta, blockIdx.x / rb, ws);
+  const int i = (int)(blockIdx.x % rb) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= meta.R) return;
+  float* E = u.base + (int64_t)i * u.ldE;
+  const float* w = u.base + am_off_w(meta.R, u.m, u.ldE, meta.d);
+  float z = 0.0f;
+  for (int j = lane; j < u.m; j += 32) z = fmaf(E[j], w[j], z);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float inv = z > 0.0f ? 1.0f / z : 0.0f;
+  for (int j = lane; j < u.m; j += 32) E[j] = E[j] * w[j] * inv;
+}
+
+constexpr int kValueCols = 8;  // value-fit columns per block (32 row slices x 8 columns)
+
+__host__ __device__ constexpr int value_smem_bytes(int m) {
+  return (2 * m * kValueCols + 4 * m + (kAmThreads / kValueCols + 1) * kValueCols) * 4;
+}
+__host__ __device__ constexpr int mass_smem_bytes(int m) { return 6 * m * 4; }
+
+// ------------------------------------------------------------------ value fit
+// Block = (unit, 8 of the d value columns).  The columns are independent
+// least-squares problems sharing H = Ph^T Ph: cyclic coordinate descent from
+// X = the kept values, gradient Gv = H X - Bm kept in shared memory; row j of
+// X moves by -Gv_j / H_jj and Gv follows by column j of H (= row j) times the
+// change, when |Gv_jc| > 2^-14 pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic|
+// + max_k |X0_kc|: the scale of the gradient's terms in column c).  Row j + 1
+// of H streams in while step j runs.  At the end V_C is
+// written to `vc` (fp32) and over the kept entries' V rows (bf16, round to
+// nearest even).
+template <int D>
+__global__ void __launch_bounds__(kAmThreads) am_value_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                              const int32_t* __restrict__ keep, uint16_t* vp,
+                                                              float* ws, float* vc, unsigned* status) {
+  extern __shared__ __align__(16) float am_smem[];
+  constexpr int kCb = D / kValueCols;
+  const AmUnit u = am_unit(meta, blockIdx.x / kCb, ws);
+  const int col0 = (int)(blockIdx.x % kCb) * kValueCols;
+  const int m = u.m;
+  float* Gv = am_smem;                 // [m][8]
+  float* X = Gv + m * kValueCols;      // [m][8]
+  float* hdiag = X + m * kValueCols;   // [m]
+  float* pi = hdiag + m;               // [m]
+  float* rows = pi + m;                // [2][m]
+  float* red = rows + 2 * m;           // [32][8] partial column scales, then S[8]
+  const float* Hm = u.base + am_off_G(meta.R, u.ldE);
+  const float* Bm = u.base + am_off_Bm(meta.R, m, u.ldE, D);
+  const int c = threadIdx.x & (kValueCols - 1), r = threadIdx.x / kValueCols;
+  constexpr int kSlices = kAmThreads / kValueCols;
+  for (int j = threadIdx.x; j < m; j += kAmThreads) {  // start: the kept entries' values
+    const int pos = am_kept(meta, u, keep, j, status);
+    const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
+    float v[8];
+    if (row >= 0) {
+      unpack8(*reinterpret_cast<const uint4*>(vp + row * D + col0), v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) X[j * kValueCols + e] = v[e];
+    hdiag[j] = Hm[(int64_t)j * u.ldE + j];
+  }
+  __syncthreads();
+  {  // S_c = max_i |Y_ic| + max_k |X0_kc|
+    const float* Y = u.base + am_off_Y(meta.R, m, u.ldE);
+    float ym = 0.0f, xm = 0.0f;
+    for (int i = r; i < meta.R; i += kSlices) ym = fmaxf(ym, fabsf(Y[(int64_t)i * D + col0 + c]));
+    for (int k = r; k < m; k += kSlices) xm = fmaxf(xm, fabsf(X[k * kValueCols + c]));
+    red[r * kValueCols + c] = ym;
+    __syncthreads();
+    if (r == 0) {
+      for (int t = 1; t < kSlices; ++t) ym = fmaxf(ym, red[t * kValueCols + c]);
+    }
+    __syncthreads();
+    red[r * kValueCols + c] = xm;
+    __syncthreads();
+    if (r == 0) {
+      for (int t = 1; t < kSlices; ++t) xm = fmaxf(xm, red[t * kValueCols + c]);
+      red[kSlices * kValueCols + c] = ym + xm;
+    }
+  }
+  for (int i = r; i < m; i += kSlices) {  // Gv = H X - Bm and pi = H 1
+    const float* hr = Hm + (int64_t)i * u.ldE;
+    float acc = 0.0f, ps = 0.0f;
+    for (int k = 0; k < m; ++k) {
+      acc = fmaf(hr[k], X[k * kValueCols + c], acc);
+      ps += hr[k];
+    }
+    Gv[i * kValueCols + c] = acc - Bm[(int64_t)i * D + col0 + c];
+    if (c == 0) pi[i] = ps;
+  }
+  __syncthreads();
+  const float Sc = red[kSlices * kValueCols + c];
+  const int64_t steps = (int64_t)meta.sweeps * m;
+  if (steps > 0) {
+    for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + i, Hm + i);
+    cp_async_commit();
+  }
+  for (int64_t st = 0; st < steps; ++st) {
+    const int j = (int)(st % m);
+    const int buf = (int)(st & 1);
+    if (st + 1 < steps) {
+      const float* nr = Hm + (int64_t)((st + 1) % m) * u.ldE;
+      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + (buf ^ 1) * m + i, nr + i);
+    }
+    cp_async_commit();
+    cp_async_wait_group<1>();
+    __syncthreads();
+    const float Hjj = hdiag[j];
+    const float gv = Gv[j * kValueCols + c];
+    const float dl = (Hjj > 0.0f && fabsf(gv) > kAmGuard * pi[j] * Sc) ? -gv / Hjj : 0.0f;
+    __syncthreads();
+    if (dl != 0.0f) {
+      const float* rj = rows + buf * m;
+      for (int i = r; i < m; i += kSlices) Gv[i * kValueCols + c] = fmaf(rj[i], dl, Gv[i * kValueCols + c]);
+      if (r == 0) X[j * kValueCols + c] += dl;
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
+  for (int j = r; j < m; j += kSlices) {
+    const float x = X[j * kValueCols + c];
+    if (vc != nullptr) vc[(orow + j) * D + col0 + c] = x;
+    const int pos = am_kept(meta, u, keep, j, status);
+    const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
+    if (row >= 0) {
+      const __nv_bfloat16 hb = __float2bfloat16_rn(x);
+      vp[row * D + col0 + c] = *reinterpret_cast<const uint16_t*>(&hb);
+    }
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D>
+cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    if ((e = set_smem(am_targets_kernel<D>, targets_smem_bytes<D>())) != cudaSuccess) return e;
+    if ((e = set_smem(am_exp_kernel<D>, exp_smem_bytes<D>())) != cudaSuccess) return e;
+    if ((e = set_smem(am_mass_kernel, mass_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
+    if ((e = set_smem(am_value_kernel<D>, value_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  const uint16_t* kp = static_cast<const uint16_t*>(al.k_pool);
+  uint16_t* vp = static_cast<uint16_t*>(al.v_pool);
+  auto check = [&]() {
+    count_launch();
+    return cudaGetLastError();
+  };
+  for (size_t ci = 0; ci < al.chunks; ++ci) {
+    const AmMeta& m = al.meta[ci];
+    if (m.units <= 0) continue;
+    const int rb64 = (m.R + 63) / 64;
+    const int mt = (m.max_m + 63) / 64;
+    am_targets_kernel<D><<<(unsigned)(m.units * rb64), kAmThreads, targets_smem_bytes<D>(), stream>>>(
+        m, al.block_table, kp, vp, al.q, al.ws, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+    am_exp_kernel<D><<<(unsigned)(m.units * rb64 * mt), kAmThreads, exp_smem_bytes<D>(), stream>>>(
+        m, al.block_table, kp, al.q, al.keep, al.ws, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+    const int nt0 = (m.max_m + 1 + 63) / 64;
+    am_atb_kernel<<<(unsigned)(m.units * mt * nt0), kAmThreads, 0, stream>>>(m, al.ws, 0);
+    if ((e = check()) != cudaSuccess) return e;
+    am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
+        m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+    am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
+    if ((e = check()) != cudaSuccess) return e;
+    am_atb_kernel<<<(unsigned)(m.units * mt * nt0), kAmThreads, 0, stream>>>(m, al.ws, 1);
+    if ((e = check()) != cudaSuccess) return e;
+    am_atb_kernel<<<(unsigned)(m.units * mt * ((D + 63) / 64)), kAmThreads, 0, stream>>>(m, al.ws, 2);
+    if ((e = check()) != cudaSuccess) return e;
+    am_value_kernel<D><<<(unsigned)(m.units * (D / kValueCols)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
+        m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_am(const AmLaunch& al, cudaStream_t stream) {
+  if (al.chunks == 0) return cudaSuccess;
+  return al.meta[0].d == 64 ? launch_am_d<64>(al, stream) : launch_am_d<128>(al, stream);
+}
+
+}  // namespace kvc

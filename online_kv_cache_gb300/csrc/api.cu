@@ -1090,6 +1090,131 @@ kvc_status kvc_lrfu_update(const kvc_cache* cache, const kvc_segments* segs, con
   return ok();
 }
 
+}  // extern "C"
+
+namespace kvc {
+namespace {
+
+// Launch chunks and workspace offsets of Attention Matching: units are the
+// (sequence, layer, head) triples of the sequences with m > 0.
+struct AmPlan {
+  std::vector<AmMeta> metas;
+  int64_t floats = 0;
+};
+
+void build_am_plan(const kvc_cache* c, const Plan& p, int R, float scale, int sweeps, AmPlan* out) {
+  const int64_t LH = (int64_t)c->num_layers * c->num_kv_heads;
+  std::vector<size_t> act;
+  for (size_t i = 0; i < p.seqs.size(); ++i)
+    if (p.seqs[i].m > 0) act.push_back(i);
+  int64_t wsf = 0;
+  for (size_t a0 = 0; a0 < act.size(); a0 += kMaxSeqPerLaunch) {
+    AmMeta am;
+    std::memset(&am, 0, sizeof am);
+    am.L = c->num_layers;
+    am.H = c->num_kv_heads;
+    am.P = c->page_size;
+    am.d = c->head_dim;
+    am.num_pages = c->num_pages;
+    am.max_blocks = c->max_blocks;
+    am.R = R;
+    am.sweeps = sweeps;
+    am.scale = scale;
+    am.Mtot = p.Mtot;
+    const size_t a1 = std::min(act.size(), a0 + (size_t)kMaxSeqPerLaunch);
+    am.nseq = (int)(a1 - a0);
+    int64_t units = 0;
+    for (size_t k = a0; k < a1; ++k) {
+      const size_t i = act[k];
+      const Seq& q = p.seqs[i];
+      AmSeq& s = am.seq[k - a0];
+      s.b = q.b;
+      s.s0 = q.s0;
+      s.n = q.n;
+      s.m = q.m;
+      s.ldE = (q.m + 1 + 3) & ~3;
+      s.moff = p.moff[i];
+      s.unit0 = units;
+      s.ws = wsf;
+      s.unit_floats = am_unit_floats(R, q.m, s.ldE, c->head_dim);
+      units += LH;
+      wsf += LH * s.unit_floats;
+      am.max_m = std::max(am.max_m, q.m);
+    }
+    am.units = units;
+    out->metas.push_back(am);
+  }
+  out->floats = wsf;
+}
+
+kvc_status check_am_args(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, int32_t R, Plan* p) {
+  kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedBT);
+  if (st != KVC_OK) return st;
+  if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
+  if (R < 1 || R > kAmMaxR) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..%d)", R, kAmMaxR);
+  if ((st = build_plan(cache, segs, m, p)) != KVC_OK) return st;
+  for (const Seq& q : p->seqs)
+    if (q.m > kAmMaxM)
+      return fail(KVC_ERR_UNSUPPORTED, "budget m = %d exceeds %d (Attention Matching's m x m Gram matrices)", q.m,
+                  kAmMaxM);
+  return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_am_workspace_size(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, int32_t R,
+                                 size_t* bytes) {
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  Plan p;
+  kvc_status st = check_am_args(cache, segs, m, R, &p);
+  if (st != KVC_OK) return st;
+  AmPlan ap;
+  build_am_plan(cache, p, R, 1.0f, 0, &ap);
+  *bytes = (size_t)ap.floats * sizeof(float);
+  return ok();
+}
+
+kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, const uint16_t* q,
+                      int32_t R, float scale, const int32_t* keep, int32_t sweeps, float* beta, float* vc, void* ws,
+                      size_t ws_bytes, kvc_stream_t stream) {
+  Plan p;
+  kvc_status st = check_am_args(cache, segs, m, R, &p);
+  if (st != KVC_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(KVC_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (sweeps < 0 || sweeps > 1000) return fail(KVC_ERR_INVALID_ARG, "sweeps = %d (allowed: 0..1000)", sweeps);
+  if (p.Mtot == 0) return ok();
+  if (q == nullptr || !aligned16(q)) return fail(KVC_ERR_INVALID_ARG, "q is NULL or not 16-byte aligned");
+  if (keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");
+  const int64_t qrows = (int64_t)cache->batch * cache->num_layers * cache->num_kv_heads * R;
+  if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
+  AmPlan ap;
+  build_am_plan(cache, p, R, scale, sweeps, &ap);
+  const size_t need = (size_t)ap.floats * sizeof(float);
+  if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVC_OK) return st;
+  AmLaunch al;
+  al.chunks = ap.metas.size();
+  al.meta = ap.metas.data();
+  al.block_table = cache->block_table;
+  al.k_pool = cache->k_pool;
+  al.v_pool = cache->v_pool;
+  al.q = q;
+  al.keep = keep;
+  al.ws = static_cast<float*>(ws);
+  al.aux = cache->aux;
+  al.beta = beta;
+  al.vc = vc;
+  al.status = di.status;
+  const cudaError_t e = launch_am(al, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_am_fit launch");
+  return ok();
+}
+
 kvc_status kvc_read_device_status(uint32_t* out, int32_t clear, kvc_stream_t stream) {
   if (out == nullptr) return fail(KVC_ERR_INVALID_ARG, "out is NULL");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

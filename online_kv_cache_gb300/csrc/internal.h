@@ -140,6 +140,73 @@ constexpr int kSelectMaxSegment = 1 << 20;
 // below 2^32 for up to 2^16 elements per warp (16 warps).
 constexpr int kLrfuMaxSegment = 1 << 20;
 
+// Attention Matching on the survivors (am.cu).  Units are (sequence, layer,
+// head) with m > 0; every unit owns `unit_floats` floats of the workspace:
+//   E   [R][ldE]   exp(L_C - c) in columns [0, m), s = exp(LSE - c) in column m;
+//                  overwritten by the compact probabilities Ph after the mass fit
+//   G   [m][ldE]   E^T [E | s] (the mass fit's Gram matrix and E^T s in column m);
+//                  overwritten by H = Ph^T Ph for the value fit
+//   Y   [R][d]     full attention output softmax(L) V
+//   lse [R]        natural-log row mass of the full attention
+//   Bm  [m][d]     Ph^T Y
+//   w   [m4]       fitted exp(beta)
+struct AmSeq {
+  int32_t b, s0, n, m;
+  int32_t ldE;          // row stride of E and G: m + 1 rounded up to a multiple of 4
+  int32_t pad;
+  int64_t moff;         // offset of the sequence in [L][H][Mtot]
+  int64_t unit0;        // first unit of the sequence in this launch
+  int64_t ws;           // float offset of the sequence's first unit in the workspace
+  int64_t unit_floats;  // workspace floats per unit
+};
+
+struct AmMeta {
+  int32_t nseq, L, H, P, d, num_pages, max_blocks, R;
+  int32_t max_m;   // largest m of the launch (grid sizing)
+  int32_t sweeps;  // coordinate-descent sweeps of each fit
+  float scale;
+  int32_t pad;
+  int64_t Mtot;
+  int64_t units;   // units of this launch
+  AmSeq seq[kMaxSeqPerLaunch];
+};
+
+// Unit workspace offsets (floats, from the unit's base).
+__host__ __device__ inline int64_t am_off_G(int R, int ldE) { return (int64_t)R * ldE; }
+__host__ __device__ inline int64_t am_off_Y(int R, int m, int ldE) { return (int64_t)(R + m) * ldE; }
+__host__ __device__ inline int64_t am_off_lse(int R, int m, int ldE, int d) {
+  return am_off_Y(R, m, ldE) + (int64_t)R * d;
+}
+__host__ __device__ inline int64_t am_off_Bm(int R, int m, int ldE, int d) { return am_off_lse(R, m, ldE, d) + R; }
+__host__ __device__ inline int64_t am_off_w(int R, int m, int ldE, int d) {
+  return am_off_Bm(R, m, ldE, d) + (int64_t)m * d;
+}
+__host__ __device__ inline int64_t am_unit_floats(int R, int m, int ldE, int d) {
+  const int64_t x = am_off_w(R, m, ldE, d) + ((m + 3) & ~3);
+  return (x + 63) & ~int64_t(63);  // 256-byte aligned units
+}
+
+// Largest budget and proxy-row count the fits take (the Gram matrices are m x m).
+constexpr int kAmMaxM = 2048;
+constexpr int kAmMaxR = 4096;
+
+struct AmLaunch {
+  size_t chunks = 0;
+  const AmMeta* meta = nullptr;  // [chunks]
+  const int32_t* block_table = nullptr;
+  const void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  const uint16_t* q = nullptr;   // [B][L][H][R][d]
+  const int32_t* keep = nullptr; // [L][H][Mtot]
+  float* ws = nullptr;
+  float* aux = nullptr;          // per-slot beta, or null
+  float* beta = nullptr;         // [L][H][Mtot] or null
+  float* vc = nullptr;           // [L][H][Mtot][d] or null
+  unsigned* status = nullptr;
+};
+
+cudaError_t launch_am(const AmLaunch& al, cudaStream_t stream);
+
 cudaError_t launch_lrfu(const LrfuLaunch& ll, cudaStream_t stream);
 cudaError_t launch_sentinel(const LayoutLaunch& ll, cudaStream_t stream);
 cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream);

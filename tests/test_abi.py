@@ -228,3 +228,43 @@ def test_layout_variant_validation(lib):
     bad = np.array([20, -1], np.int32)
     assert lib.kvc_evict_sentinel(ctypes.byref(c), ctypes.byref(s), bad.ctypes.data, 0x700,
                                   None) == kvc.KVC_ERR_BUDGET
+
+
+def test_am_validation(lib):
+    """kvc_am_fit checks its arguments before any launch: budget and row limits of the m x m
+    fits, sweeps, pointers and the workspace; the workspace grows with R and is 0 when nothing is
+    kept."""
+    c = fake_cache()
+    s, _ = segs([0, 16], [100, 64], [100, 80])
+    m = np.array([20, 48], np.int32)
+
+    def size(mm, R):
+        out = ctypes.c_size_t(0)
+        st = lib.kvc_am_workspace_size(ctypes.byref(c), ctypes.byref(s), mm.ctypes.data, R, ctypes.byref(out))
+        return st, out.value
+
+    st, b16 = size(m, 16)
+    assert st == kvc.KVC_OK and b16 > 0 and b16 % 256 == 0
+    assert size(m, 64)[1] > b16
+    assert size(np.zeros(2, np.int32), 16) == (kvc.KVC_OK, 0)
+    assert size(m, 4097)[0] == kvc.KVC_ERR_UNSUPPORTED
+    assert size(m, 0)[0] == kvc.KVC_ERR_UNSUPPORTED
+
+    def fit(mm=m, R=16, scale=0.1, q=0x60000, keep=0x70000, sweeps=4, ws=0x80000, ws_bytes=1 << 30):
+        return lib.kvc_am_fit(ctypes.byref(c), ctypes.byref(s), mm.ctypes.data, q, R, scale, keep, sweeps, None,
+                              None, ws, ws_bytes, None)
+
+    assert fit(sweeps=-1) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(sweeps=1001) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(scale=float("inf")) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(q=0x60004) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(keep=None) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(ws_bytes=b16 - 256) == kvc.KVC_ERR_WORKSPACE
+    assert fit(ws=0x80010) == kvc.KVC_ERR_WORKSPACE
+    assert fit(np.array([20, -1], np.int32)) == kvc.KVC_ERR_BUDGET
+    big = fake_cache(max_blocks=256)
+    sb, _ = segs([0, 0], [3000, 16], [3000, 16])
+    out = ctypes.c_size_t(0)
+    assert lib.kvc_am_workspace_size(ctypes.byref(big), ctypes.byref(sb), np.array([2049, 1], np.int32).ctypes.data,
+                                     16, ctypes.byref(out)) == kvc.KVC_ERR_UNSUPPORTED
+    assert "2048" in kvc.kvc_last_error()

@@ -1,0 +1,192 @@
+"""GPU parity of Attention Matching (the bias beta and compact values V_C fitted on the survivors)
+with the oracle.
+
+Source: "Practical Online KV Cache Compaction for LLM Agents: An Empirical Study" (agifrontier
+tutorial page), section on the two compaction families: min ||exp(Q K_C^T + beta) 1_m -
+exp(Q K^T) 1_n||^2 and min ||A_hat(Q; K_C, beta, V_C) - A(Q; K, V)||_F^2.
+
+The fits are ill-conditioned (exp of logits: cond(E) reaches 1e14 on these inputs), so their
+minimisers are not unique to fp32 and the individual beta_j and V_C rows are not compared.  What
+is compared is unique: the residual norms the fits reach after the same sweeps, each evaluated in
+fp64 by the oracle on its own problem (E, s, Y) at the GPU's outputs, against the oracle's own
+fit.  Tolerance: the GPU forms E, the Gram matrices and the descent in fp32 (unit roundoff
+2^-24 ~ 6e-8); the logit error of an fp32 dot product over d = 128 bf16 products and the Gram
+sums over R rows put the residual's floor near 1e-6 of the target norm (an fp32 re-run of the
+same steps on the CPU lands within 6e-7 of the fp64 residuals); the bound is 3e-5 of it.
+The keep sets come from the oracle's own token-eviction scores, and every value the tests
+expect comes from the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import online_kv_cache_gb300 as kvc
+import oracle
+import workloads
+from oracle import am
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+RES_TOL = 3e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from online_kv_cache_gb300 import build
+    build.build()
+    kvc.kvc_read_device_status(clear=True)
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_keep(case, m):
+    s, _ = oracle.score_cache(case.k_pool, case.block_table, case.nblocks, case.seg_start, case.seg_end,
+                              case.seq_len, case.q, case.spec.scale)
+    return oracle.select_cache(s, case.seg_start, case.seg_end, m)
+
+
+def run_gpu(case, m, keep_np, sweeps, aux):
+    sp = case.spec
+    cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks, case.free_ids,
+                       case.free_top, case.seg_start, case.seg_end, case.seq_len, m, sp.R, aux=aux)
+    keep = torch.from_numpy(np.ascontiguousarray(keep_np)).to(DEV)
+    beta = torch.full((sp.L, sp.H, max(1, cp.Mtot)), float("nan"), device=DEV)
+    vc = torch.full((sp.L, sp.H, max(1, cp.Mtot), sp.d), float("nan"), device=DEV)
+    cp.am_fit(case.q, sp.scale, sweeps, keep=keep, beta=beta, vc=vc)
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    return beta.cpu().numpy().astype(np.float64), vc.cpu().numpy().astype(np.float64)
+
+
+def check_units(units, m, beta, vc, sweeps, sample=None):
+    """Residuals of both fits at the GPU's outputs against the oracle's, per unit."""
+    moff = np.concatenate([[0], np.cumsum(m)])
+    worst = [0.0, 0.0]
+    keys = sorted(units) if sample is None else sample
+    for (b, l, h) in keys:
+        u = units[(b, l, h)]
+        sl = slice(moff[b], moff[b + 1])
+        bg = beta[l, h, sl]
+        assert not np.any(np.isnan(bg)) and not np.any(bg == np.inf)
+        wg = np.exp(bg)  # exp(-inf) = 0: a masked key
+        s_norm = np.linalg.norm(u["s"])
+        r_gpu = np.sqrt(am.mass_objective(u["E"], u["s"], wg))
+        r_orc = np.sqrt(am.mass_objective(u["E"], u["s"], u["w"]))
+        r_te = np.sqrt(am.mass_objective(u["E"], u["s"], np.ones_like(wg)))
+        dm = abs(r_gpu - r_orc) / s_norm
+        assert dm <= RES_TOL, f"unit {(b, l, h)}: mass residual {r_gpu:.4e} vs oracle {r_orc:.4e} (|s| {s_norm:.3e})"
+        assert r_gpu <= r_te + RES_TOL * s_norm  # never worse than token eviction's beta = 0
+        y_norm = np.linalg.norm(u["Y"])
+        v_gpu = np.sqrt(am.value_objective(u["E"], u["Y"], wg, vc[l, h, sl]))
+        v_orc = np.sqrt(am.value_objective(u["E"], u["Y"], u["w"], u["vc"]))
+        dv = abs(v_gpu - v_orc) / y_norm
+        assert dv <= RES_TOL, f"unit {(b, l, h)}: value residual {v_gpu:.4e} vs oracle {v_orc:.4e} (|Y| {y_norm:.3e})"
+        worst = [max(worst[0], dm), max(worst[1], dv)]
+    print(f"sweeps={sweeps}: worst mass / value residual gap {worst[0]:.2e} / {worst[1]:.2e} of the target norm")
+
+
+def check_writes(case, m, keep_np, beta, vc, before_v, before_k, before_aux, aux):
+    """Kept V rows hold bf16(V_C) (round to nearest even), their aux slots hold beta; every other
+    V row, every K row and every other aux slot is untouched."""
+    sp = case.spec
+    v_after = case.v_pool.cpu()
+    k_after = case.k_pool.cpu()
+    assert torch.equal(k_after, before_k)
+    bt = case.block_table.cpu().numpy()
+    moff = np.concatenate([[0], np.cumsum(m)])
+    want_v = before_v.clone()
+    want_aux = before_aux.copy()
+    for b in range(sp.B):
+        for l in range(sp.L):
+            for h in range(sp.H):
+                for j in range(m[b]):
+                    pos = int(keep_np[l, h, moff[b] + j])
+                    slot = case.seg_start[b] + pos
+                    pg, o = bt[b, slot // sp.P], slot % sp.P
+                    want_v[l, pg, h, o] = torch.from_numpy(vc[l, h, moff[b] + j].astype(np.float32)).to(torch.bfloat16)
+                    want_aux[l, pg, h, o] = beta[l, h, moff[b] + j]
+    assert torch.equal(v_after.view(torch.int16), want_v.view(torch.int16))
+    got_aux = aux.cpu().numpy()
+    assert np.array_equal(np.isneginf(got_aux), np.isneginf(want_aux))
+    fin = np.isfinite(want_aux)
+    assert np.array_equal(got_aux[fin], want_aux[fin].astype(np.float32))
+
+
+@pytest.mark.parametrize("d,P,G,q,lengths,ratio,sweeps,qdist", [
+    (128, 16, 4, 8, (300, 129), 0.2, 8, "planted4"),   # R = 32 < m, concentrated attention
+    (128, 16, 4, 8, (300, 129), 0.2, 8, "normal"),     # diffuse attention: the fits do real work
+    (64, 32, 2, 40, (200, 65, 1), 0.2, 8, "normal"),   # R = 80 > m, a one-key unit
+    (128, 16, 8, 16, (700,), 0.1, 3, "planted4"),      # R = 128 > m = 70, two key tiles of rows
+])
+def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist):
+    sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, shuffle_pages=True,
+                          qdist=qdist)
+    case = workloads.build(sp, 5, DEV)
+    m = [oracle.budget_ratio(n, ratio) for n in PT.seg_lengths(case)]
+    keep_np = oracle_keep(case, m)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    aux = torch.rand(case.tags.shape, generator=g, device=DEV)
+    before = (case.v_pool.cpu().clone(), case.k_pool.cpu().clone(), aux.cpu().numpy().copy())
+    kb, vb, qb = bits(case.k_pool), bits(case.v_pool), bits(case.q)
+    beta, vc = run_gpu(case, m, keep_np, sweeps, aux)
+    _, _, units = am.cache(kb, vb, qb, case.block_table.cpu().numpy(), case.seg_start, case.seg_end, keep_np, m,
+                           sp.scale, sweeps)
+    check_units(units, m, beta, vc, sweeps)
+    check_writes(case, m, keep_np, beta, vc, *before, aux)
+
+
+def test_zero_sweeps_is_token_eviction():
+    """sweeps = 0 returns token eviction's answer: beta = 0, V_C = V, the pool unchanged."""
+    sp = workloads.custom(L=1, H=2, G=2, d=128, P=16, q=8, lengths=(257,), shuffle_pages=True)
+    case = workloads.build(sp, 6, DEV)
+    m = [oracle.budget_ratio(257, 0.2)]
+    keep_np = oracle_keep(case, m)
+    v0 = case.v_pool.cpu().clone()
+    beta, vc = run_gpu(case, m, keep_np, 0, None)
+    assert np.all(beta == 0.0)
+    assert torch.equal(case.v_pool.cpu().view(torch.int16), v0.view(torch.int16))
+    _, _, units = am.cache(bits(case.k_pool), bits(case.v_pool), bits(case.q), case.block_table.cpu().numpy(),
+                           case.seg_start, case.seg_end, keep_np, m, sp.scale, 0)
+    for (b, l, h), u in units.items():
+        np.testing.assert_array_equal(vc[l, h, :m[0]], u["vc"])  # the bf16 values, exactly
+
+
+def test_keep_all_reproduces_the_full_attention():
+    """m = n: the kept keys carry all the mass and V reproduces the output; the fits stay at
+    (numerically) zero residual."""
+    sp = workloads.custom(L=1, H=2, G=4, d=64, P=16, q=8, lengths=(96,))
+    case = workloads.build(sp, 7, DEV)
+    m = [96]
+    keep_np = np.tile(np.arange(96, dtype=np.int32), (1, 2, 1))
+    beta, vc = run_gpu(case, m, keep_np, 4, None)
+    _, _, units = am.cache(bits(case.k_pool), bits(case.v_pool), bits(case.q), case.block_table.cpu().numpy(),
+                           case.seg_start, case.seg_end, keep_np, m, sp.scale, 4)
+    check_units(units, m, beta, vc, 4)
+    for (b, l, h), u in units.items():
+        assert np.sqrt(am.mass_objective(u["E"], u["s"], np.exp(beta[l, h]))) <= RES_TOL * np.linalg.norm(u["s"])
+
+
+def test_am_multi_turn_shape_sampled():
+    """The delay-1 multi-turn compaction shape (28 layers, 2 KV heads, 16 query heads x 128 rows:
+    R = 2048 > m = 307), 8 sweeps, in the launch configuration the benchmark times; six units
+    sampled for the oracle."""
+    sp = workloads.spec("multi-turn")
+    case = workloads.build(sp, 0, DEV)
+    m = [oracle.budget_ratio(n, 0.2) for n in PT.seg_lengths(case)]
+    s_orc, _ = oracle.score_cache(case.k_pool, case.block_table, case.nblocks, case.seg_start, case.seg_end,
+                                  case.seq_len, case.q, sp.scale)
+    keep_np = oracle.select_cache(s_orc, case.seg_start, case.seg_end, m)
+    kb, vb, qb = bits(case.k_pool), bits(case.v_pool), bits(case.q)
+    beta, vc = run_gpu(case, m, keep_np, 8, None)
+    rng = np.random.default_rng(0)
+    sample = [(0, int(l), int(h)) for l, h in zip(rng.choice(sp.L, 6, replace=False), rng.integers(0, sp.H, 6))]
+    bt = case.block_table.cpu().numpy()
+    units = {}
+    for (b, l, h) in sample:
+        K = am.gather(kb, bt, l, h, b, 0, sp.lengths[0])
+        V = am.gather(vb, bt, l, h, b, 0, sp.lengths[0])
+        units[(b, l, h)] = am.unit(am.bf16_to_f64(qb[b, l, h]), K, V, keep_np[l, h, :m[0]], sp.scale, 8)
+    check_units(units, m, beta, vc, 8, sample=sample)
