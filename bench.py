@@ -58,6 +58,10 @@ def parse_args():
                     help="override the workload's layer count (small profiling cases)")
     ap.add_argument("--seqs", type=int, default=None,
                     help="keep the workload's first N sequences (small profiling cases)")
+    ap.add_argument("--am-sweeps", type=int, default=0,
+                    help="Attention Matching after the selection: fit the bias and the compact "
+                         "values of the kept entries with this many coordinate-descent sweeps "
+                         "(0: token eviction alone)")
     return ap.parse_args()
 
 
@@ -280,6 +284,30 @@ def profile_traffic(kernel: str, workload: str):
 # The job ends when the slowest rank does: the step time is the maximum over ranks,
 # and the whole-job throughput counts every rank's entries.
 
+def am_flops(sp, n, m, sweeps: int) -> float:
+    """Algorithmic fp32 flops of one Attention Matching fit (2 per multiply-add), summed over the
+    units: full-attention targets (Q K^T and P V over all n keys), the kept keys' exponentials,
+    the Gram products E^T [E | s], Ph^T Ph and Ph^T Y, and the two descents (m-long updates of the
+    mass gradient, m x d-long updates of the value gradient, per step; their initial gradients)."""
+    R, d = sp.R, sp.d
+    f = 0.0
+    for nb, mb in zip(n, m):
+        mb = min(mb, nb)
+        if mb <= 0:
+            continue
+        per = (4.0 * R * nb * d + 2.0 * R * mb * d + 2.0 * R * mb * (mb + 1) + 2.0 * R * mb * mb
+               + 2.0 * R * mb * d + 2.0 * R * mb + 2.0 * mb * mb * (d + 1)
+               + sweeps * (2.0 * mb * mb + 2.0 * mb * mb * d))
+        f += sp.L * sp.H * per
+    return f
+
+
+def fp32_peak_tflops() -> float:
+    """fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flops at the 2070 MHz maximum SM
+    clock."""
+    return 152 * 128 * 2 * 2070e6 / 1e12
+
+
 def replica_seed(seed: int, rank: int) -> int:
     return seed + rank
 
@@ -332,7 +360,7 @@ def our_arm(args):
     case = workloads.build(sp, replica_seed(args.seed, rank), dev)
     m = budgets_lib(case)
     aux = None
-    if args.scorer == "actkv":  # per-slot LRFU values, moved with their entries
+    if args.scorer == "actkv" or args.am_sweeps > 0:  # per-slot LRFU values / AM biases, moved with their entries
         aux = torch.zeros(case.tags.shape, dtype=torch.float32, device=dev)
     cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks,
                        case.free_ids, case.free_top, case.seg_start, case.seg_end, case.seq_len, m,
@@ -349,7 +377,8 @@ def our_arm(args):
     n = [e - s for s, e in zip(case.seg_start, case.seg_end)]
     entries = sp.L * sp.H * sum(n)
     stream = torch.cuda.current_stream()
-    stages = ("score_lse", "score_alpha", "select", "plan", "compact", "free")
+    stages = ("score_lse", "score_alpha", "select", "am_fit", "plan", "compact", "free")
+    nev = len(stages) + 1
 
     class _NoEvent:
         def record(self, _stream):
@@ -357,7 +386,7 @@ def our_arm(args):
 
     def step(ev):
         if ev is None:  # under graph capture: no timing events inside the graph
-            ev = [_NoEvent()] * 7
+            ev = [_NoEvent()] * nev
         ev[0].record(stream)
         if args.scorer == "actkv":  # both scoring passes, then the LRFU step, in "score_alpha"
             cp.score_action(case.q, sp.scale)
@@ -370,31 +399,34 @@ def our_arm(args):
         ev[2].record(stream)
         cp.select()
         ev[3].record(stream)
+        if args.am_sweeps > 0:
+            cp.am_fit(case.q, sp.scale, args.am_sweeps)
+        ev[4].record(stream)
         if args.variant == "inplace":
             cp.plan_compact()
-            ev[4].record(stream)
-            cp.compact()
             ev[5].record(stream)
+            cp.compact()
+            ev[6].record(stream)
             cp.free_pages()
         elif args.variant == "fresh":
             fplan = cp.plan_fresh()
-            ev[4].record(stream)
-            cp.compact(plan=fplan)
             ev[5].record(stream)
+            cp.compact(plan=fplan)
+            ev[6].record(stream)
             cp.commit_fresh()
         else:  # sentinel: the whole layout step is the "compact" stage
-            ev[4].record(stream)
-            cp.evict_sentinel()
             ev[5].record(stream)
-        ev[6].record(stream)
+            cp.evict_sentinel()
+            ev[6].record(stream)
+        ev[7].record(stream)
 
     for _ in range(args.warmup):
         case.restore(snap)
-        step([torch.cuda.Event(enable_timing=True) for _ in range(7)])
+        step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
     torch.cuda.synchronize()
     assert kvc.kvc_read_device_status(clear=True) == 0
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     if world > 1:
@@ -412,7 +444,7 @@ def our_arm(args):
     launches = kvc.kvc_launch_count()
     status = kvc.kvc_read_device_status(clear=True)
     assert status == 0, f"device status {status:#x}"
-    per_step = [events[k][0].elapsed_time(events[k][6]) for k in range(args.steps)]
+    per_step = [events[k][0].elapsed_time(events[k][nev - 1]) for k in range(args.steps)]
     per_stage = {s: statistics.mean(events[k][i].elapsed_time(events[k][i + 1])
                                     for k in range(args.steps)) for i, s in enumerate(stages)}
     ms = slowest_rank_ms(statistics.mean(per_step), world, dev)
@@ -494,6 +526,17 @@ def our_arm(args):
                     "tensor_frac": F_alg / t_dom / 1e12 / pk["bf16_tflops"]}
     roofline.update({"traffic": profile_traffic(dom_kernel, sp.name), "peak_source": pk["source"],
                      "algorithmic_flops_per_launch": F_alg, "algorithmic_bytes_per_launch": B_pass})
+    if args.am_sweeps > 0:
+        # Attention Matching dominates the step: its kernels are fp32 contractions and
+        # descents on the CUDA cores, timed as one stage against the fp32 FMA peak
+        F_am = am_flops(sp, n, m, args.am_sweeps)
+        t_am = per_stage["am_fit"] * 1e-3
+        peak = fp32_peak_tflops()
+        roofline = {"bound": "alu", "kernel": "kvc_am_fit (8 fp32 kernels, one stage)",
+                    "achieved": F_am / t_am / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "frac": F_am / t_am / 1e12 / peak, "traffic": None,
+                    "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x 2070 MHz",
+                    "algorithmic_flops_per_launch": F_am}
     if args.variant == "sentinel":  # evicted rows written: K and V rows (2d bytes each) and a tag
         compact_bytes = (entries - sp.L * sp.H * Mtot) * (4.0 * d + 4.0)
     else:
@@ -511,6 +554,7 @@ def our_arm(args):
                          % (2 * case.k_pool.numel() * 2 / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "eviction_layout": args.variant, "eviction_score": args.scorer,
+                   "attention_matching_sweeps": args.am_sweeps,
                    "launch": (f"CUDA graph of the step ({graph_nodes} kernel nodes), replayed"
                               if graph_ms is not None else "eager C-ABI calls")},
         "roofline": roofline,
@@ -525,10 +569,10 @@ def our_arm(args):
         line["clocks"] = clocks.summary(w0, w1)
 
     # the end-to-end and CPU-baseline legs measure the default in-place chain only
-    if not args.no_e2e and args.variant == "inplace" and args.scorer == "te":
+    if not args.no_e2e and args.variant == "inplace" and args.scorer == "te" and args.am_sweeps == 0:
         line["e2e"] = e2e_run(args, case, cp, snap, entries, world, dev)
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "inplace"
-            and args.scorer == "te"):
+            and args.scorer == "te" and args.am_sweeps == 0):
         case.restore(snap)  # the oracle reads the pristine cache
         torch.cuda.synchronize()
         line["cpu_baseline"] = cpu_baseline(case, budgets_oracle(case))
