@@ -251,7 +251,11 @@ ScoreGeom score_geom(int R, int d) {
   const int fixed = score_smem_bytes(0, 0, d);
   g.gsub1 = std::min(4, g.rowtiles);
   g.ngroups1 = (int)ceil_div(g.rowtiles, g.gsub1);
-  g.qbytes1 = 2 * 128 * d * 2;  // two staging buffers: pass 1 keeps Q in TMEM
+  // pass 1 keeps Q in TMEM; its sub-tiles pass through staging buffers: a whole row
+  // group (4) when it has more than two, so the next item's Q is in shared memory
+  // before this item's MMAs drain (measured: -3.6% on short items, -0.8% on long
+  // ones, although fewer K stages remain), else two
+  g.qbytes1 = (g.gsub1 > 2 ? 4 : 2) * 128 * d * 2;
   g.kst1 = std::min(8, (kScoreSmemLimit - fixed - g.qbytes1) / tile_bytes);
   g.gsub2 = std::min(g.nchunks, std::max(1, 512 / g.W));
   g.ngroups2 = (int)ceil_div(g.nchunks, g.gsub2);
@@ -312,6 +316,7 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
     a.gsub = g.gsub1;
     a.qbytes = g.qbytes1;
     a.kst = g.kst1;
+
     z.ngroups = g.ngroups2;
     z.gsub = g.gsub2;
     z.qbytes = g.qbytes2;

@@ -96,20 +96,28 @@ __device__ __forceinline__ Item decode_item(const LaunchMeta& meta, int64_t item
   Item it;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
-  int64_t local = item - s.item0;
-  const int sp = (int)(local % s.split);
-  local /= s.split;
-  it.u.g = (int)(local % meta.ngroups);
-  local /= meta.ngroups;
-  it.u.h = (int)(local % meta.H);
-  it.u.l = (int)(local / meta.H);
+  // 32-bit arithmetic: a sequence owns fewer than 2^32 items of a launch, and the
+  // 64-bit divisions cost the MMA issuer ~0.5 us at every item boundary
+  uint32_t local = (uint32_t)(item - s.item0);
+  const uint32_t split = (uint32_t)s.split;
+  const uint32_t sp = local % split;
+  local /= split;
+  it.u.g = (int)(local % (uint32_t)meta.ngroups);
+  local /= (uint32_t)meta.ngroups;
+  it.u.h = (int)(local % (uint32_t)meta.H);
+  it.u.l = (int)(local / (uint32_t)meta.H);
   it.u.b = s.b;
   it.u.s0 = s.s0;
   it.u.n = s.n;
   it.u.off = s.off;
-  const int T = (s.n + kTile - 1) / kTile;
-  it.t0 = (int)((int64_t)sp * T / s.split);
-  it.t1 = (int)((int64_t)(sp + 1) * T / s.split);
+  const uint32_t T = ((uint32_t)s.n + kTile - 1) / kTile;
+  if (T < 46341u) {  // (sp + 1) * T < 2^31
+    it.t0 = (int)(sp * T / split);
+    it.t1 = (int)((sp + 1) * T / split);
+  } else {
+    it.t0 = (int)((uint64_t)sp * T / split);
+    it.t1 = (int)((uint64_t)(sp + 1) * T / split);
+  }
   it.J = min(meta.gsub, total_sub - it.u.g * meta.gsub);
   return it;
 }
@@ -210,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_sub = (PASS == 1) ? meta.rowtiles : meta.nchunks;
   const int sub_rows = (PASS == 1) ? kTile : meta.W;  // Q rows per job
   const uint32_t sub_bytes = (uint32_t)(C::KB * sub_rows * 128);
+  // pass 1: staging buffers for Q sub-tiles on their way to TMEM (2, or 4 when
+  // items are short and a whole row group is prefetched during the previous item)
+  const uint32_t qst = (PASS == 1) ? (uint32_t)meta.qbytes / sub_bytes : 4u;
+  const uint32_t qsh = qst == 4u ? 2u : 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
@@ -275,17 +287,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pre = min(kst - 1, kit_.t1 - kit_.t0);
       // Q of item q_item goes after that item's first `pre` K tiles (or at once
       // when the K cursor has already passed them)
-      const bool do_q = q_item < meta.items &&
-                        (q_item < k_item || k_item >= meta.items ||
-                         (q_item == k_item && kt >= kit_.t0 + pre));
+      bool do_q = q_item < meta.items &&
+                  (q_item < k_item || k_item >= meta.items ||
+                   (q_item == k_item && kt >= kit_.t0 + pre));
+      if (PASS == 1 && qst == 4u && !do_q && q_item == k_item + gridDim.x) {
+        // a whole row group is staged: the next item's Q goes as soon as its
+        // buffers are free (tested, not waited for, so K keeps flowing)
+        unsigned fr = 0;
+        if (lane == 0) fr = mbar_try_wait(&q_empty[qc & 3u], ((qc >> 2) & 1u) ^ 1u) ? 1u : 0u;
+        do_q = __shfl_sync(0xffffffffu, fr, 0) != 0u;
+      }
       if (do_q) {
         const Item qi = decode_item(meta, q_item, total_sub);
         const int qrow = ((qi.u.b * meta.L + qi.u.l) * meta.H + qi.u.h) * meta.R +
                          qi.u.g * meta.gsub * sub_rows;
         for (int j = 0; j < qi.J && ok; ++j) {
           // pass 1: staging buffer qc % 2; pass 2: the group's own sub-tile slot j
-          const int qs = (PASS == 1) ? (int)(qc & 1) : j;
-          const uint32_t qpar = (PASS == 1) ? ((qc >> 1) & 1) : (q_use[j] & 1);
+          const int qs = (PASS == 1) ? (int)(qc & (qst - 1)) : j;
+          const uint32_t qpar = (PASS == 1) ? ((qc >> qsh) & 1) : (q_use[j] & 1);
           if (lane == 0) {
             ok = mbar_wait(&q_empty[qs], qpar ^ 1, abort_flag, status);
             if (ok) mbar_arrive_expect_tx(&q_full[qs], sub_bytes);
@@ -343,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t j = (kcount > (uint32_t)kst ? kcount - kst : 0); j < kcount; ++j)
         mbar_wait(&k_full[j % kst], (j / kst) & 1, nullptr, status);
       if (PASS == 1) {
-        for (uint32_t j = (qc > 2 ? qc - 2 : 0); j < qc; ++j)
-          mbar_wait(&q_full[j & 1], (j >> 1) & 1, nullptr, status);
+        for (uint32_t j = (qc > qst ? qc - qst : 0); j < qc; ++j)
+          mbar_wait(&q_full[j & (qst - 1)], (j >> qsh) & 1, nullptr, status);
       } else {
         for (int j = 0; j < 4; ++j)
           if (q_use[j] > 0) mbar_wait(&q_full[j], (q_use[j] - 1) & 1, nullptr, status);
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the 16-byte-unit offset of each k-step to the start-address field.
     if (lane == 0) {
       const uint32_t idesc = (PASS == 1) ? idesc_bf16_f32(kTile, kTile) : idesc_bf16_f32(kTile, meta.W);
-      uint32_t q_use[4] = {0, 0, 0, 0}, last_slot = 0, last_use = 0;
+      uint32_t q_use[4] = {0, 0, 0, 0};
       uint32_t slot = 0, use = 0;  // accumulator slot of the next job and its use count
       int ks = 0;                  // K ring stage of the next tile and its phase parity
       uint32_t kph = 0;
@@ -376,9 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++dc;
             tc_fence_after_sync();
           }
+          // the group's Q sub-tiles into TMEM; the tensor pipe runs the copies and the
+          // MMAs in issue order.  (Copying each sub-tile just before its first job was
+          // measured slower: a copy then waits behind the epilogue's slot release.)
           for (int j = 0; j < it.J && ok; ++j) {
-            const uint32_t qs = qc & 1;
-            if (!(ok = mbar_wait(&q_full[qs], (qc >> 1) & 1, abort_flag, status))) break;
+            const uint32_t qs = qc & (qst - 1);
+            if (!(ok = mbar_wait(&q_full[qs], (qc >> qsh) & 1, abort_flag, status))) break;
             const uint64_t stage = q_desc + ((qs * sub_bytes) >> 4);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
@@ -415,8 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&t_full[slot]);
             if (PASS == 2 && t == it.t1 - 1) mma_commit(&q_empty[j]);  // last use of this Q sub-tile
             issued = true;
-            last_slot = slot;
-            last_use = use;
             if (++slot == nslots) {
               slot = 0;
               ++use;
@@ -431,8 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < it.J; ++j) ++q_use[j];
       }
-      if (!ok && issued)  // the last commit covers every MMA issued
-        mbar_wait(&t_full[last_slot], last_use & 1, nullptr, status);
+      if (!ok && issued) {  // one more commit covers every copy and MMA issued
+        mma_commit(drain);
+        mbar_wait(drain, dc & 1, nullptr, status);
+      }
     }
   }  // warps 2 and 3: nothing to do
   } else {
