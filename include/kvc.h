@@ -43,7 +43,11 @@
  *     of the last error of the calling thread is kvc_last_error().  Errors a
  *     kernel detects (bounded wait expired, free stack overflow, a block-table
  *     entry out of range) set bits of the device status word instead of
- *     trapping.
+ *     trapping.  Checked mode (environment variable KVC_CHECKED set and not
+ *     "0"): every call that launched work synchronises its stream and returns
+ *     KVC_ERR_DEVICE_CHECK if the status word has a bit set (not while the
+ *     stream is being captured into a graph).
+ *   Tracing: each call is an NVTX range named after it.
  *   Cache layout (all layers share one block table and one page id space):
  *     k_pool, v_pool  bf16  [L][num_pages][H][P][d]  (H = KV heads)
  *     tags            int32 [L][num_pages][H][P]     logical position of the
@@ -74,7 +78,7 @@ typedef int32_t kvc_status;
 #define KVC_ERR_WORKSPACE (-4)         /* workspace or plan buffer too small    */
 #define KVC_ERR_UNSUPPORTED (-5)       /* d, P or R outside the supported set   */
 #define KVC_ERR_CUDA (-6)              /* CUDA runtime/driver error             */
-#define KVC_ERR_DEVICE_CHECK (-7)      /* device status word has a bit set      */
+#define KVC_ERR_DEVICE_CHECK (-7)      /* checked mode: status word has a bit set */
 
 /* Device status word bits (kvc_read_device_status). */
 #define KVC_DEV_WAIT_TIMEOUT 1u /* a bounded pipeline wait gave up           */

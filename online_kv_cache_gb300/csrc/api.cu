@@ -6,6 +6,7 @@
 // the paged K pool and the proxy queries, and the device status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -113,6 +114,31 @@ int grid_limit(int num_sms) {
 enum Need : unsigned {
   kNeedK = 1, kNeedV = 2, kNeedTags = 4, kNeedBT = 8, kNeedNB = 16,
 };
+
+// NVTX range around each C-ABI call (seen by nsys / ncu; a no-op without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+// Checked mode (environment KVC_CHECKED set and not "0"): a call that launched work
+// waits for its stream and turns a set bit of the device status word (a bad page, a
+// bad keep position, an expired wait, a stack overflow) into KVC_ERR_DEVICE_CHECK.
+// Skipped while the stream is being captured into a graph.
+kvc_status launched(kvc_stream_t stream, const char* where) {
+  const char* env = std::getenv("KVC_CHECKED");
+  if (env == nullptr || env[0] == '\0' || (env[0] == '0' && env[1] == '\0')) return ok();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return ok();
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  if (v != 0) return fail(KVC_ERR_DEVICE_CHECK, "%s: device status word 0x%x (checked mode)", where, v);
+  return ok();
+}
 
 kvc_status check_cache(const kvc_cache* c, unsigned need) {
   if (c == nullptr) return fail(KVC_ERR_INVALID_ARG, "cache is NULL");
@@ -473,6 +499,7 @@ kvc_status score_common(const char* where, unsigned phases, float pw, const kvc_
                         const kvc_segments* segs, const uint16_t* q, int32_t R, float scale,
                         const float* lse_in, float* lse_out, float* scores, void* ws, size_t ws_bytes,
                         kvc_stream_t stream) {
+  const NvtxRange nvtx_range(where);
   kvc_status st = check_cache(cache, kNeedK | kNeedBT);
   if (st != KVC_OK) return st;
   if (R < 1 || R > 4096) return fail(KVC_ERR_UNSUPPORTED, "R = %d (supported: 1..4096)", R);
@@ -524,7 +551,7 @@ kvc_status score_common(const char* where, unsigned phases, float pw, const kvc_
   sl.status = di.status;
   const cudaError_t e = launch_score(sl, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, where);
-  return ok();
+  return launched(stream, where);
 }
 
 std::atomic<uint64_t> g_launches{0};
@@ -636,6 +663,7 @@ kvc_status kvc_select_workspace_size(const kvc_cache* cache, const kvc_segments*
 
 kvc_status kvc_select_topm(const kvc_cache* cache, const kvc_segments* segs, const float* scores,
                            const int32_t* m, int32_t* keep, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_select_topm");
   (void)ws;
   (void)ws_bytes;
   kvc_status st = check_cache(cache, 0);
@@ -674,7 +702,7 @@ kvc_status kvc_select_topm(const kvc_cache* cache, const kvc_segments* segs, con
   sl.status = di.status;
   const cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_select_topm launch");
-  return ok();
+  return launched(stream, "kvc_select_topm");
 }
 
 kvc_status kvc_plan_buffer_sizes(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
@@ -752,6 +780,7 @@ void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta
 
 kvc_status kvc_plan_compact(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                             const int32_t* keep, const kvc_plan* plan, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_plan_compact");
   kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -785,11 +814,12 @@ kvc_status kvc_plan_compact(const kvc_cache* cache, const kvc_segments* segs, co
   cl.status = di.status;
   const cudaError_t e = launch_plan(cl, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_plan_compact launch");
-  return ok();
+  return launched(stream, "kvc_plan_compact");
 }
 
 kvc_status kvc_compact(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                        const kvc_plan* plan, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_compact");
   kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedTags);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -816,11 +846,12 @@ kvc_status kvc_compact(const kvc_cache* cache, const kvc_segments* segs, const i
   cl.status = di.status;
   const cudaError_t e = launch_compact(cl, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_compact launch");
-  return ok();
+  return launched(stream, "kvc_compact");
 }
 
 kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                           const kvc_allocator* alloc, const kvc_plan* plan, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_free_pages");
   kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -848,7 +879,7 @@ kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, cons
   cl.status = di.status;
   const cudaError_t e = launch_free(cl, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_free_pages launch");
-  return ok();
+  return launched(stream, "kvc_free_pages");
 }
 
 // ------------------------------------------------------------- layout variants
@@ -931,6 +962,7 @@ kvc_status check_allocator(const kvc_allocator* alloc) {
 
 kvc_status kvc_evict_sentinel(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                               const int32_t* keep, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_evict_sentinel");
   kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedTags | kNeedBT);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -965,7 +997,7 @@ kvc_status kvc_evict_sentinel(const kvc_cache* cache, const kvc_segments* segs, 
   ll.status = di.status;
   const cudaError_t e = launch_sentinel(ll, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_evict_sentinel launch");
-  return ok();
+  return launched(stream, "kvc_evict_sentinel");
 }
 
 kvc_status kvc_plan_fresh_buffer_sizes(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
@@ -981,6 +1013,7 @@ kvc_status kvc_plan_fresh_buffer_sizes(const kvc_cache* cache, const kvc_segment
 kvc_status kvc_plan_fresh(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                           const int32_t* keep, const kvc_allocator* alloc, const kvc_plan* plan,
                           kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_plan_fresh");
   kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -1012,11 +1045,12 @@ kvc_status kvc_plan_fresh(const kvc_cache* cache, const kvc_segments* segs, cons
   ll.status = di.status;
   const cudaError_t e = launch_fresh_plan(ll, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_plan_fresh launch");
-  return ok();
+  return launched(stream, "kvc_plan_fresh");
 }
 
 kvc_status kvc_commit_fresh(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,
                             const kvc_allocator* alloc, const kvc_plan* plan, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_commit_fresh");
   kvc_status st = check_cache(cache, kNeedBT | kNeedNB);
   if (st != KVC_OK) return st;
   if (m == nullptr) return fail(KVC_ERR_INVALID_ARG, "m is NULL");
@@ -1043,13 +1077,14 @@ kvc_status kvc_commit_fresh(const kvc_cache* cache, const kvc_segments* segs, co
   ll.status = di.status;
   const cudaError_t e = launch_fresh_commit(ll, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_commit_fresh launch");
-  return ok();
+  return launched(stream, "kvc_commit_fresh");
 }
 
 // ------------------------------------------------------------- ActKV LRFU
 
 kvc_status kvc_lrfu_update(const kvc_cache* cache, const kvc_segments* segs, const float* attn, float frac,
                            float lambda, float* crf_out, uint8_t* hits, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_lrfu_update");
   kvc_status st = check_cache(cache, kNeedBT);
   if (st != KVC_OK) return st;
   if (cache->aux == nullptr) return fail(KVC_ERR_INVALID_ARG, "cache->aux (the per-slot LRFU values) is NULL");
@@ -1092,7 +1127,7 @@ kvc_status kvc_lrfu_update(const kvc_cache* cache, const kvc_segments* segs, con
   ll.status = di.status;
   const cudaError_t e = launch_lrfu(ll, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_lrfu_update launch");
-  return ok();
+  return launched(stream, "kvc_lrfu_update");
 }
 
 }  // extern "C"
@@ -1185,6 +1220,7 @@ kvc_status kvc_am_workspace_size(const kvc_cache* cache, const kvc_segments* seg
 kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, const uint16_t* q,
                       int32_t R, float scale, const int32_t* keep, int32_t sweeps, float* beta, float* vc, void* ws,
                       size_t ws_bytes, kvc_stream_t stream) {
+  const NvtxRange nvtx_range("kvc_am_fit");
   Plan p;
   kvc_status st = check_am_args(cache, segs, m, R, &p);
   if (st != KVC_OK) return st;
@@ -1217,7 +1253,7 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   al.status = di.status;
   const cudaError_t e = launch_am(al, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvc_am_fit launch");
-  return ok();
+  return launched(stream, "kvc_am_fit");
 }
 
 kvc_status kvc_read_device_status(uint32_t* out, int32_t clear, kvc_stream_t stream) {
