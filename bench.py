@@ -637,10 +637,19 @@ def cpu_baseline(case, m):
         dt_s, entries, used = oracle_sample(case, m, layers, cores)
     else:
         dt_s, entries, used = dt1, e1, max(1, min(cores, sp.H))
-    return {"value": entries / dt_s, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"{layers} of {sp.L} layers x {sp.H} KV heads ({entries} entries): fp64 "
-                      f"score + select + compact + free, {dt_s:.1f} s",
-            "host_cores": cores}
+    out = {"value": entries / dt_s, "unit": UNIT, "cores": used, "kind": "oracle",
+           "sample": f"{layers} of {sp.L} layers x {sp.H} KV heads ({entries} entries): fp64 "
+                     f"score + select + compact + free, {dt_s:.1f} s",
+           "host_cores": cores}
+    # the same oracle on one thread, on one layer when that takes at most ~30 s
+    used1 = max(1, min(cores, sp.H * sum(1 for a, b in zip(case.seg_start, case.seg_end) if b > a)))
+    if dt1 * used1 <= 30.0:
+        dts, es, _ = oracle_sample(case, m, 1, 1)
+        out["single_thread"] = {"value": es / dts, "unit": UNIT, "cores": 1,
+                                "sample": f"1 of {sp.L} layers x {sp.H} KV heads ({es} entries), {dts:.1f} s"}
+    else:
+        out["single_thread"] = {"value": None, "skipped": f"one layer would take ~{dt1 * used1:.0f} s on one thread"}
+    return out
 
 
 def main():
