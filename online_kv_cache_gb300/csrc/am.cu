@@ -335,22 +335,26 @@ __global__ void __launch_bounds__(kAmThreads) am_exp_kernel(const AmMeta meta, c
 }
 
 // ------------------------------------------------------------------ A^T B
-// Block = (unit, 64 x 64 tile of C): C[p][q] = sum_i A[i][p] B[i][q] over the
-// R proxy rows, 16 rows per step through shared memory.
+// Block = (unit, 128 x 128 tile of C): C[p][q] = sum_i A[i][p] B[i][q] over the
+// R proxy rows, 16 rows per step through shared memory; each thread holds an
+// 8 x 8 sub-tile (rows ty*4 + {0..3, 64..67}, columns tx*4 + {0..3, 64..67}) and
+// reads its operands with 128-bit shared loads (4 loads per 64 multiply-adds).
 //   mode 0: A = E (m columns), B = [E | s] (m + 1), C = G        (stride ldE)
 //   mode 1: A = B = Ph (m columns),                 C = H in G's place
 //   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d)
+constexpr int kAtbTile = 128;
+
 __global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, float* ws, int mode) {
-  __shared__ float As[16][64];
-  __shared__ float Bs[16][64];
-  const int mt = (meta.max_m + 63) / 64;
-  const int nt = mode == 2 ? (meta.d + 63) / 64 : (meta.max_m + 1 + 63) / 64;
+  __shared__ __align__(16) float As[16][kAtbTile];
+  __shared__ __align__(16) float Bs[16][kAtbTile];
+  const int mt = (meta.max_m + kAtbTile - 1) / kAtbTile;
+  const int nt = mode == 2 ? (meta.d + kAtbTile - 1) / kAtbTile : (meta.max_m + 1 + kAtbTile - 1) / kAtbTile;
   const int ni = (int)(blockIdx.x % nt);
   const int mi = (int)((blockIdx.x / nt) % mt);
   const AmUnit u = am_unit(meta, blockIdx.x / ((int64_t)nt * mt), ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
-  const int p0 = mi * 64, q0 = ni * 64;
+  const int p0 = mi * kAtbTile, q0 = ni * kAtbTile;
   if (p0 >= M || q0 >= N) return;
   const float* A = u.base;
   const int lda = u.ldE;
@@ -359,12 +363,16 @@ __global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, f
   float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
   const int ldc = mode == 2 ? meta.d : u.ldE;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  float acc[4][4] = {};
+  float acc[8][8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
   for (int i0 = 0; i0 < meta.R; i0 += 16) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 8; ++r) {  // 16 x 128 of A and of B, consecutive threads along a row
       const int e = threadIdx.x + r * kAmThreads;
-      const int ii = e >> 6, pp = e & 63;
+      const int ii = e >> 7, pp = e & 127;
       const bool in = i0 + ii < meta.R;
       As[ii][pp] = (in && p0 + pp < M) ? A[(int64_t)(i0 + ii) * lda + p0 + pp] : 0.0f;
       Bs[ii][pp] = (in && q0 + pp < N) ? B[(int64_t)(i0 + ii) * ldb + q0 + pp] : 0.0f;
@@ -372,25 +380,26 @@ __global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, f
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float av[4], bv[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[i][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[i][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[i][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[i][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a) av[a] = As[i][ty + 16 * a];
+      for (int a = 0; a < 8; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) bv[b] = Bs[i][tx + 16 * b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int p = p0 + ty + 16 * a;
+  for (int a = 0; a < 8; ++a) {
+    const int p = p0 + (a < 4 ? ty * 4 + a : 64 + ty * 4 + a - 4);
     if (p >= M) continue;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int qq = q0 + tx + 16 * b;
+    for (int b = 0; b < 8; ++b) {
+      const int qq = q0 + (b < 4 ? tx * 4 + b : 64 + tx * 4 + b - 4);
       if (qq < N) C[(int64_t)p * ldc + qq] = acc[a][b];
     }
   }
@@ -649,17 +658,18 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     am_exp_kernel<D><<<(unsigned)(m.units * rb64 * mt), kAmThreads, exp_smem_bytes<D>(), stream>>>(
         m, al.block_table, kp, al.q, al.keep, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    const int nt0 = (m.max_m + 1 + 63) / 64;
-    am_atb_kernel<<<(unsigned)(m.units * mt * nt0), kAmThreads, 0, stream>>>(m, al.ws, 0);
+    const int mt128 = (m.max_m + kAtbTile - 1) / kAtbTile;
+    const int nt0 = (m.max_m + 1 + kAtbTile - 1) / kAtbTile;
+    am_atb_kernel<<<(unsigned)(m.units * mt128 * nt0), kAmThreads, 0, stream>>>(m, al.ws, 0);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_kernel<<<(unsigned)(m.units * mt * nt0), kAmThreads, 0, stream>>>(m, al.ws, 1);
+    am_atb_kernel<<<(unsigned)(m.units * mt128 * nt0), kAmThreads, 0, stream>>>(m, al.ws, 1);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_kernel<<<(unsigned)(m.units * mt * ((D + 63) / 64)), kAmThreads, 0, stream>>>(m, al.ws, 2);
+    am_atb_kernel<<<(unsigned)(m.units * mt128 * ((D + kAtbTile - 1) / kAtbTile)), kAmThreads, 0, stream>>>(m, al.ws, 2);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kValueCols)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);
