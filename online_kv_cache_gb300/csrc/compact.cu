@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(256)
     const int f = s.nb - s.X;
     if (f <= 0) return;
     const int64_t ro = (int64_t)s.b * meta.max_blocks;
-    for (int j = threadIdx.x; j < meta.max_blocks; j += blockDim.x) block_table[ro + j] = new_rows[ro + j];
+    copy_ints8(block_table + ro, new_rows + ro, meta.max_blocks);
     if (threadIdx.x == 0) nblocks[s.b] -= f;
     return;
   }
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   if (!sh_ok) return;
-  for (int64_t i = threadIdx.x; i < count; i += blockDim.x) free_ids[sh_top + i] = freed[f0 + i];
+  copy_ints8(free_ids + sh_top, freed + f0, count);
   __syncthreads();
   if (threadIdx.x == 0) *free_top = sh_top + (int)count;
 }

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   if (!sh_ok) return;
-  for (int64_t i = threadIdx.x; i < Ftot; i += blockDim.x) free_ids[sh_base + i] = freed[i];
+  copy_ints8(free_ids + sh_base, freed, Ftot);
   __syncthreads();
   if (threadIdx.x == 0) *free_top = sh_base + (int)Ftot;
 }

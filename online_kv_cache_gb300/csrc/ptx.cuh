@@ -320,4 +320,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// dst[i] = src[i] for i < n by the whole block, eight loads in flight per thread
+// before their stores (a one-block copy of tens of thousands of ids is latency
+// bound with one load at a time).
+__device__ __forceinline__ void copy_ints8(int32_t* __restrict__ dst, const int32_t* __restrict__ src, int64_t n) {
+  const int64_t step = (int64_t)blockDim.x * 8;
+  for (int64_t base = threadIdx.x; base < n; base += step) {
+    int32_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = base + (int64_t)u * blockDim.x;
+      if (i < n) v[u] = src[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = base + (int64_t)u * blockDim.x;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
 }  // namespace kvc
