@@ -55,3 +55,37 @@ def test_graph_replay_equals_eager(name):
         assert torch.equal(cp.scores.cpu(), eager_scores), f"scores differ on replay {rep}"
         assert torch.equal(cp.keep.cpu(), eager_keep), f"keep differs on replay {rep}"
         PT.assert_state_equal(PT.host_state(case), eager, f"{name} replay {rep}")
+
+
+@pytest.mark.parametrize("name", ["qwen3-30b-a3b", "batched-ragged"])
+def test_graph_replay_equals_eager_full_size(name):
+    """At full size, in the launch configuration the benchmark times (the five calls captured
+    into one CUDA graph and replayed), the replay leaves scores, keep sets and the whole cache
+    state bit-identical to the eager calls, whose parity with the oracle test_gpu_workloads
+    checks at the same sizes.  Compared on the device."""
+    sp = workloads.spec(name)
+    case = workloads.build(sp, 0, DEV)
+    m = PT.lib_budgets(case)
+    snap = case.snapshot()
+    cp = PT.compactor(case, m)
+    chain(cp, case)
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    eager_state = [t.clone() for t in case.state()]
+    eager_scores, eager_keep = cp.scores.clone(), cp.keep.clone()
+    g = torch.cuda.CUDAGraph()
+    case.restore(snap)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        chain(cp, case)
+    for rep in range(2):
+        case.restore(snap)
+        cp.scores.zero_()
+        cp.keep.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        PT.device_status_clean()
+        assert torch.equal(cp.scores, eager_scores), f"{name}: scores differ on replay {rep}"
+        assert torch.equal(cp.keep, eager_keep), f"{name}: keep differs on replay {rep}"
+        for i, (a, b) in enumerate(zip(case.state(), eager_state)):
+            assert torch.equal(a, b), f"{name}: cache state tensor {i} differs on replay {rep}"
