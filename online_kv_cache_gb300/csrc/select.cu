@@ -5,16 +5,25 @@
 // section).  Equal scores go to the lower position; the kept positions are
 // written in ascending order (the order the slot plan consumes them).
 //
-// One 512-thread CTA per unit.  Scores are >= 0, so their fp32 bit patterns
-// order like the values.  Three radix passes over the bits (11, 11, 10 from
-// the top) find the exact bit pattern T of the m-th largest score and how many
-// elements equal to T are kept (k_eq); each pass counts into warp-private
-// histograms with plain shared atomics (scores bunch into few bins, and
-// per-warp bins keep those updates from queueing across the block).  A final pass keeps every element > T
-// and the first k_eq elements == T, and writes each kept position at its rank
-// (warp ballots + a block scan of the warp counts).
+// A thread-block cluster of CS 512-thread CTAs per unit (CS > 1 only when the
+// units are too few to fill the GPU and long enough to split, up to 8); CTA r
+// of the cluster owns the r-th contiguous slice of the unit's positions.  Scores are >= 0, so their fp32
+// bit patterns order like the values.  Three radix passes over the bits (11,
+// 11, 10 from the top) find the exact bit pattern T of the m-th largest score
+// and how many elements equal to T are kept (k_eq); each pass counts into
+// warp-private histograms with plain shared atomics (scores bunch into few
+// bins, and per-warp bins keep those updates from queueing across the block),
+// then every CTA adds up the cluster's histograms through distributed shared
+// memory and picks the same digit.  The same histograms give each CTA how many
+// of its elements are > T and == T, so a CTA's ranks start after its
+// lower-ranked peers' counts.  A final pass keeps every element > T and the
+// first k_eq elements == T (in position order across the cluster), and writes
+// each kept position at its rank (warp ballots + a block scan of the warp
+// counts).
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -33,37 +42,45 @@ constexpr int kBins = 2048;
 // sees at most 2^16 - 1 elements of a unit per pass for n < 2^20)
 constexpr int kWarpWords = kBins / 2;
 constexpr size_t kSelSmem = (size_t)kWarps * kWarpWords * sizeof(uint32_t);
+constexpr int kSelSlice = 16384;  // fewest positions per CTA of a cluster
 
-// One CTA per unit.  Element i of a tile sits at tile + q * kSelThreads + tid, so
-// every load instruction is coalesced and the (q, warp, lane) order is the index
-// order used for ranks.
-__global__ void __launch_bounds__(kSelThreads)
+// Element i of a tile sits at tile + q * kSelThreads + tid, so every load
+// instruction is coalesced and the (q, warp, lane) order is the index order
+// used for ranks.
+template <int CS>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
     select_topm_kernel(const __grid_constant__ LaunchMeta meta, const float* __restrict__ scores,
                        int32_t* __restrict__ keep) {
-  __shared__ uint32_t hist[kBins];
+  namespace cg = cooperative_groups;
+  __shared__ uint32_t hist[kBins];   // this CTA's counts (read by the peers)
+  __shared__ uint32_t ghist[kBins];  // the cluster's counts
   extern __shared__ uint32_t whist[];  // [kWarps][kWarpWords]
   __shared__ uint32_t pre_gt[kU * kWarps], pre_eq[kU * kWarps];
-  __shared__ uint32_t sh_digit, sh_k, sh_tot_gt, sh_tot_eq;
+  __shared__ uint32_t sh_digit, sh_k, sh_tot_gt, sh_tot_eq, sh_above;
+  __shared__ uint32_t sh_cnt[2];     // this CTA's elements > T and == T (read by the peers)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t item = blockIdx.x;
+  const int rank = CS > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int64_t item = blockIdx.x / CS;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
   const int64_t local = item - s.item0;
   const int h = (int)(local % meta.H);
   const int l = (int)(local / meta.H);
   const int n = s.n, m = s.m;
+  const int chunk = (n + CS - 1) / CS;
+  const int lo = min(n, rank * chunk), hi = min(n, lo + chunk);
   const uint32_t* key =
       reinterpret_cast<const uint32_t*>(scores + ((int64_t)l * meta.H + h) * meta.Ntot + s.off);
   int32_t* out = keep + ((int64_t)l * meta.H + h) * meta.Mtot + s.moff;
-  if (m <= 0) return;
+  if (m <= 0) return;  // (the same for every CTA of the cluster)
   if (m >= n) {
-    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+    for (int i = lo + tid; i < hi; i += kSelThreads) out[i] = i;
     return;
   }
 
   // ---- radix select of the m-th largest bit pattern (11, 11, 10 bits)
-  uint32_t prefix = 0, pmask = 0, k = (uint32_t)m;
+  uint32_t prefix = 0, pmask = 0, k = (uint32_t)m, my_gt = 0, my_eq = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
@@ -74,17 +91,17 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int i = lane; i < kWarpWords; i += 32) wh[i] = 0;
     __syncwarp();
 #pragma unroll 1
-    for (int tile = 0; tile < n; tile += kTileElems) {
+    for (int tile = lo; tile < hi; tile += kTileElems) {
       uint32_t u[kU];
 #pragma unroll
       for (int q = 0; q < kU; ++q) {
         const int i = tile + q * kSelThreads + tid;
-        u[q] = (i < n) ? __ldg(key + i) : 0u;
+        u[q] = (i < hi) ? __ldg(key + i) : 0u;
       }
 #pragma unroll
       for (int q = 0; q < kU; ++q) {
         const int i = tile + q * kSelThreads + tid;
-        if (i < n && (u[q] & pmask) == prefix) {
+        if (i < hi && (u[q] & pmask) == prefix) {
           const uint32_t d = (u[q] >> sh) & dmask;
           atomicAdd(&wh[d >> 1], (d & 1u) ? 0x10000u : 1u);
         }
@@ -97,13 +114,23 @@ __global__ void __launch_bounds__(kSelThreads)
       for (int w = 0; w < kWarps; ++w) c += (whist[w * kWarpWords + (b >> 1)] >> ((b & 1) * 16)) & 0xFFFFu;
       hist[b] = c;
     }
+    if constexpr (CS > 1) {
+      cg::this_cluster().sync();  // every CTA's counts are in place
+      for (int b = tid; b < nbins; b += kSelThreads) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) c += cg::this_cluster().map_shared_rank(hist, r)[b];
+        ghist[b] = c;
+      }
+    }
     __syncthreads();
+    const uint32_t* H = CS > 1 ? ghist : hist;
     if (warp == 0) {
       // lane 0 owns the highest bins; find the digit where the count from the top reaches k
       const int per = nbins / 32;
-      const int hi = nbins - 1 - lane * per;  // this lane covers digits (hi - per, hi]
+      const int hi_b = nbins - 1 - lane * per;  // this lane covers digits (hi_b - per, hi_b]
       uint32_t sum = 0;
-      for (int j = 0; j < per; ++j) sum += hist[hi - j];
+      for (int j = 0; j < per; ++j) sum += H[hi_b - j];
       uint32_t incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -114,9 +141,9 @@ __global__ void __launch_bounds__(kSelThreads)
       if (excl < k && incl >= k) {
         uint32_t acc = excl;
         for (int j = 0; j < per; ++j) {
-          const uint32_t c = hist[hi - j];
+          const uint32_t c = H[hi_b - j];
           if (acc + c >= k) {
-            sh_digit = (uint32_t)(hi - j);
+            sh_digit = (uint32_t)(hi_b - j);
             sh_k = k - acc;
             break;
           }
@@ -125,7 +152,22 @@ __global__ void __launch_bounds__(kSelThreads)
       }
     }
     __syncthreads();
-    prefix |= sh_digit << sh;
+    const uint32_t digit = sh_digit;
+    if constexpr (CS > 1) {
+      // this CTA's elements above the chosen digit are > T; at the last digit, == T
+      uint32_t above = 0;
+      for (int b = (int)digit + 1 + tid; b < nbins; b += kSelThreads) above += hist[b];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+      if (tid == 0) sh_above = 0;
+      __syncthreads();
+      if (lane == 0 && above) atomicAdd(&sh_above, above);
+      __syncthreads();
+      my_gt += sh_above;
+      if (pass == 2) my_eq = hist[digit];
+      cg::this_cluster().sync();  // no CTA rewrites its counts while a peer reads them
+    }
+    prefix |= digit << sh;
     pmask |= dmask << sh;
     k = sh_k;
     __syncthreads();
@@ -135,21 +177,34 @@ __global__ void __launch_bounds__(kSelThreads)
 
   // ---- order-preserving compaction: rank = #(> T before) + min(#(== T before), k_eq)
   uint32_t base_gt = 0, base_eq = 0;
+  if constexpr (CS > 1) {
+    if (tid == 0) {
+      sh_cnt[0] = my_gt;
+      sh_cnt[1] = my_eq;
+    }
+    cg::this_cluster().sync();
+    for (int r = 0; r < rank; ++r) {
+      const uint32_t* pc = cg::this_cluster().map_shared_rank(sh_cnt, r);
+      base_gt += pc[0];
+      base_eq += pc[1];
+    }
+    cg::this_cluster().sync();  // peers may exit once every CTA has read their counts
+  }
   const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll 1
-  for (int tile = 0; tile < n; tile += kTileElems) {
+  for (int tile = lo; tile < hi; tile += kTileElems) {
     uint32_t u[kU];
 #pragma unroll
     for (int q = 0; q < kU; ++q) {
       const int i = tile + q * kSelThreads + tid;
-      u[q] = (i < n) ? __ldg(key + i) : 0u;
+      u[q] = (i < hi) ? __ldg(key + i) : 0u;
     }
     unsigned bg[kU], be[kU];
 #pragma unroll
     for (int q = 0; q < kU; ++q) {
       const int i = tile + q * kSelThreads + tid;
-      bg[q] = __ballot_sync(0xffffffffu, i < n && u[q] > T);
-      be[q] = __ballot_sync(0xffffffffu, i < n && u[q] == T);
+      bg[q] = __ballot_sync(0xffffffffu, i < hi && u[q] > T);
+      be[q] = __ballot_sync(0xffffffffu, i < hi && u[q] == T);
       if (lane == 0) {
         pre_gt[q * kWarps + warp] = __popc(bg[q]);
         pre_eq[q * kWarps + warp] = __popc(be[q]);
@@ -190,8 +245,8 @@ __global__ void __launch_bounds__(kSelThreads)
       const uint32_t gt_before = base_gt + pre_gt[q * kWarps + warp] + __popc(bg[q] & lt_mask);
       const uint32_t eq_before = base_eq + pre_eq[q * kWarps + warp] + __popc(be[q] & lt_mask);
       const bool gt = (bg[q] >> lane) & 1u, eq = (be[q] >> lane) & 1u;
-      const uint32_t rank = gt_before + min(eq_before, k_eq);
-      if ((gt || (eq && eq_before < k_eq)) && rank < (uint32_t)m) out[rank] = i;
+      const uint32_t rnk = gt_before + min(eq_before, k_eq);
+      if ((gt || (eq && eq_before < k_eq)) && rnk < (uint32_t)m) out[rnk] = i;
     }
     base_gt += sh_tot_gt;
     base_eq += sh_tot_eq;
@@ -207,14 +262,36 @@ cudaError_t launch_select(const SelectLaunch& sl, cudaStream_t stream) {
   cudaError_t e0 = cudaGetDevice(&dev);
   if (e0 != cudaSuccess) return e0;
   if (dev >= 64 || !attr_set[dev]) {
-    e0 = cudaFuncSetAttribute(select_topm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmem);
-    if (e0 != cudaSuccess) return e0;
+    for (const void* k : {reinterpret_cast<const void*>(select_topm_kernel<1>),
+                          reinterpret_cast<const void*>(select_topm_kernel<2>),
+                          reinterpret_cast<const void*>(select_topm_kernel<4>),
+                          reinterpret_cast<const void*>(select_topm_kernel<8>)}) {
+      e0 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmem);
+      if (e0 != cudaSuccess) return e0;
+    }
     if (dev < 64) attr_set[dev] = true;
   }
   for (size_t c = 0; c < sl.chunks; ++c) {
     const LaunchMeta& m = sl.meta[c];
     if (m.items <= 0) continue;
-    select_topm_kernel<<<(unsigned)m.items, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
+    // CTAs per unit: a cluster only when the units are too few to fill the GPU twice
+    // over (each CTA pays a fixed histogram cost per pass), with at least kSelSlice
+    // positions per CTA, at most 8 (a portable cluster)
+    int max_n = 0;
+    for (int i = 0; i < m.nseq; ++i) max_n = max(max_n, m.seq[i].n);
+    const int by_size = (max_n + kSelSlice - 1) / kSelSlice;
+    const int by_fill = (int)std::max<int64_t>(1, (2 * (int64_t)sl.num_sms) / std::max<int64_t>(1, m.items));
+    const int want = min(by_size, by_fill);
+    const int cs = want >= 8 ? 8 : (want >= 4 ? 4 : (want >= 2 ? 2 : 1));
+    const unsigned grid = (unsigned)(m.items * cs);
+    if (cs == 8)
+      select_topm_kernel<8><<<grid, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
+    else if (cs == 4)
+      select_topm_kernel<4><<<grid, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
+    else if (cs == 2)
+      select_topm_kernel<2><<<grid, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
+    else
+      select_topm_kernel<1><<<grid, kSelThreads, kSelSmem, stream>>>(m, sl.scores, sl.keep);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch();

@@ -264,3 +264,31 @@ def test_exact_ties_keep_lowest_positions(distinct):
         noff, moff = PT.unit_offsets(case, m)
         for b in range(sp.B):
             assert np.array_equal(k_gpu[0, 0, moff[b]:moff[b + 1]], np.arange(m[b]))
+
+
+@pytest.mark.parametrize("lengths,tied", [
+    ((9000, 20000), True),             # one CTA, then a cluster of 2
+    ((70000,), True),                  # a cluster of 4: ties straddle the CTAs' slices
+    ((140000, 3000, 65536), True),     # a cluster of 8 for every unit of the launch
+    ((140000, 33000), False),          # continuous scores
+])
+def test_selection_across_cluster_sizes(lengths, tied):
+    """The selection alone, on seeded scores fed in directly: segments long enough that a unit
+    is split across a thread-block cluster of 1, 2, 4 or 8 CTAs.  With few distinct score
+    levels the m-th score ties across CTA boundaries, and the lower positions must win across
+    the cluster; the keep sets equal the oracle's sort-based top-m exactly."""
+    sp = workloads.custom(L=1, H=2, G=2, d=64, P=16, q=2, lengths=lengths)
+    case = workloads.build(sp, 4, DEV, with_q=False)
+    m = [oracle.budget_ratio(n, 0.2) for n in PT.seg_lengths(case)]
+    cp = PT.compactor(case, m)
+    g = torch.Generator(device=DEV).manual_seed(77)
+    if tied:
+        s = torch.randint(0, 12, (sp.L, sp.H, cp.Ntot), generator=g, device=DEV).float() / 8.0
+    else:
+        s = torch.rand((sp.L, sp.H, cp.Ntot), generator=g, device=DEV)
+    cp.scores[:, :, :cp.Ntot] = s
+    cp.select()
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    keep_orc = oracle.select_cache(s.cpu().numpy().astype(np.float64), case.seg_start, case.seg_end, m)
+    assert np.array_equal(cp.keep.cpu().numpy()[:, :, :cp.Mtot], keep_orc)
