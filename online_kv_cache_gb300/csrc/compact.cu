@@ -14,6 +14,7 @@
 //   move k (k < c_out): keep[k] -> t_k;  holes k in [c_out, c_out + X P - m): dead
 // Every move is computed independently (two binary searches), so the planner
 // is one thread per hole with no scan.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -277,15 +278,21 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Installs the new block-table rows, lowers nblocks, and pushes the freed
-// pages onto the free stack (CTA nseq).  A push that would overflow the
-// stack's capacity sets KVC_DEV_FREE_STACK and pushes nothing.
-__global__ void __launch_bounds__(256)
+// Installs the new block-table rows and lowers nblocks (one CTA per sequence),
+// and pushes the freed pages onto the free stack (the last cluster of
+// kPushCluster CTAs: rank 0 reads the stack top and checks the capacity, every
+// rank pushes a slice, rank 0 moves the top once all have).  A push that would
+// overflow the stack's capacity sets KVC_DEV_FREE_STACK and pushes nothing.
+constexpr int kPushCluster = 8;
+
+__global__ void __cluster_dims__(kPushCluster, 1, 1) __launch_bounds__(256)
     free_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ new_rows,
                 const int32_t* __restrict__ freed, int32_t* __restrict__ block_table,
                 int32_t* __restrict__ nblocks, int32_t* __restrict__ free_ids,
                 int32_t* __restrict__ free_top, int32_t capacity, unsigned* status) {
-  if ((int)blockIdx.x < meta.nseq) {
+  const int seq_ctas = (meta.nseq + kPushCluster - 1) / kPushCluster * kPushCluster;
+  if ((int)blockIdx.x < seq_ctas) {
+    if ((int)blockIdx.x >= meta.nseq) return;
     const SeqMeta& s = meta.seq[blockIdx.x];
     const int f = s.nb - s.X;
     if (f <= 0) return;
@@ -294,21 +301,29 @@ __global__ void __launch_bounds__(256)
     if (threadIdx.x == 0) nblocks[s.b] -= f;
     return;
   }
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
   __shared__ int sh_top;
   __shared__ int sh_ok;
   const int64_t f0 = meta.seq[0].foff;
   const int64_t count = meta.Ftot;  // pages freed by this launch's sequences
-  if (threadIdx.x == 0) {
+  if (rank == 0 && threadIdx.x == 0) {
     const int top = *free_top;
     sh_top = top;
     sh_ok = (top >= 0 && (int64_t)top + count <= capacity) ? 1 : 0;
     if (!sh_ok) atomicOr(status, KVC_DEV_FREE_STACK);
   }
-  __syncthreads();
-  if (!sh_ok) return;
-  copy_ints8(free_ids + sh_top, freed + f0, count);
-  __syncthreads();
-  if (threadIdx.x == 0) *free_top = sh_top + (int)count;
+  cluster.sync();
+  const int top = *cluster.map_shared_rank(&sh_top, 0);
+  const int ok = *cluster.map_shared_rank(&sh_ok, 0);
+  if (ok) {
+    const int64_t chunk = (count + kPushCluster - 1) / kPushCluster;
+    const int64_t lo = std::min<int64_t>(count, rank * chunk), hi = std::min<int64_t>(count, lo + chunk);
+    copy_ints8(free_ids + top + lo, freed + f0 + lo, hi - lo);
+  }
+  cluster.sync();  // every slice is pushed and rank 0's top has been read
+  if (rank == 0 && threadIdx.x == 0 && ok) *free_top = top + (int)count;
 }
 
 }  // namespace
@@ -364,7 +379,8 @@ cudaError_t launch_free(const CompactLaunch& cl, cudaStream_t stream) {
   for (size_t c = 0; c < cl.chunks; ++c) {
     const LaunchMeta& m = cl.free_meta[c];
     if (m.nseq <= 0) continue;
-    free_kernel<<<(unsigned)(m.nseq + 1), 256, 0, stream>>>(m, cl.new_rows, cl.freed, cl.block_table_mut,
+    const int seq_ctas = (m.nseq + kPushCluster - 1) / kPushCluster * kPushCluster;
+    free_kernel<<<(unsigned)(seq_ctas + kPushCluster), 256, 0, stream>>>(m, cl.new_rows, cl.freed, cl.block_table_mut,
                                                             cl.nblocks, cl.free_ids, cl.free_top,
                                                             cl.capacity, cl.status);
     const cudaError_t e = cudaGetLastError();

@@ -292,3 +292,23 @@ def test_selection_across_cluster_sizes(lengths, tied):
     PT.device_status_clean()
     keep_orc = oracle.select_cache(s.cpu().numpy().astype(np.float64), case.seg_start, case.seg_end, m)
     assert np.array_equal(cp.keep.cpu().numpy()[:, :, :cp.Mtot], keep_orc)
+
+
+def test_free_stack_overflow_pushes_nothing():
+    """A free stack with room for fewer pages than the release returns (the push runs as a
+    cluster of CTAs that share the stack top): KVC_DEV_FREE_STACK is set, no page id is written
+    and the stack top stays."""
+    sp = workloads.custom(L=1, H=2, G=2, d=64, P=16, q=2, lengths=(700, 333, 96), shuffle_pages=True)
+    case = workloads.build(sp, 13, DEV, with_q=False)
+    m = [oracle.budget_ratio(n, 0.2) for n in PT.seg_lengths(case)]
+    keep = workloads.random_keep(case, m, 5)
+    cp = PT.compactor(case, m)
+    cp.plan_compact(keep.contiguous())
+    top = int(case.free_top.item())
+    small = kvc.Allocator(case.free_ids[:top + 2], case.free_top)  # capacity top + 2
+    ids_before = case.free_ids.cpu().clone()
+    kvc.kvc_free_pages(cp.cache, cp.segs, cp.m, small, cp.plan)
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status(clear=True) == kvc.KVC_DEV_FREE_STACK
+    assert int(case.free_top.item()) == top
+    assert torch.equal(case.free_ids.cpu(), ids_before)
