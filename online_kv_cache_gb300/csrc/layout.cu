@@ -13,6 +13,7 @@
 // blocks of the segment go back to the stack.  The plan fills an ordinary
 // kvc_plan (moves and dead slots), which kvc_compact executes; the commit
 // pops the fresh pages, pushes the old ones and installs the new rows.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -25,6 +26,9 @@
 namespace kvc {
 
 namespace {
+
+constexpr int kStackCluster = 8;  // CTAs of the fresh-page stack push (one cluster)
+
 
 constexpr int kSentinelChunk = 4096;       // positions per sentinel block
 constexpr int kFreshMovesPerBlock = 1024;  // moves per fresh-plan block
@@ -195,16 +199,21 @@ __global__ void __launch_bounds__(256)
     for (int i = threadIdx.x; i < s.nb; i += blockDim.x) freed[s.foff + i] = row[sb + i];
 }
 
-// Fresh commit, one block for the whole call: unless the status word
-// already holds KVC_DEV_FREE_STACK, pops the call's Xtot pages and pushes the
-// Ftot returned ones in their list order; a stack that cannot take them sets
-// KVC_DEV_FREE_STACK and changes nothing.
-__global__ void __launch_bounds__(256)
+// Fresh commit, one cluster of kStackCluster CTAs for the whole call: unless the
+// status word already holds KVC_DEV_FREE_STACK, pops the call's Xtot pages and
+// pushes the Ftot returned ones in their list order (rank 0 reads and checks the
+// stack top, every rank pushes a slice, rank 0 moves the top after a cluster
+// barrier); a stack that cannot take them sets KVC_DEV_FREE_STACK and changes
+// nothing.
+__global__ void __cluster_dims__(kStackCluster, 1, 1) __launch_bounds__(256)
     fresh_stack_kernel(int64_t Xtot, int64_t Ftot, const int32_t* __restrict__ freed,
                        int32_t* __restrict__ free_ids, int32_t* __restrict__ free_top, int32_t capacity,
                        unsigned* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
   __shared__ int sh_base, sh_ok;
-  if (threadIdx.x == 0) {
+  if (rank == 0 && threadIdx.x == 0) {
     const unsigned st = *reinterpret_cast<volatile unsigned*>(status);
     const int top = *free_top;
     const int64_t base = (int64_t)top - Xtot;
@@ -212,11 +221,16 @@ __global__ void __launch_bounds__(256)
     if (!(st & KVC_DEV_FREE_STACK) && !sh_ok) atomicOr(status, KVC_DEV_FREE_STACK);
     sh_base = (int)base;
   }
-  __syncthreads();
-  if (!sh_ok) return;
-  copy_ints8(free_ids + sh_base, freed, Ftot);
-  __syncthreads();
-  if (threadIdx.x == 0) *free_top = sh_base + (int)Ftot;
+  cluster.sync();
+  const int base = *cluster.map_shared_rank(&sh_base, 0);
+  const int ok = *cluster.map_shared_rank(&sh_ok, 0);
+  if (ok) {  // every rank pushes one slice
+    const int64_t chunk = (Ftot + kStackCluster - 1) / kStackCluster;
+    const int64_t lo = std::min<int64_t>(Ftot, rank * chunk), hi = std::min<int64_t>(Ftot, lo + chunk);
+    copy_ints8(free_ids + base + lo, freed + lo, hi - lo);
+  }
+  cluster.sync();  // every slice is pushed and rank 0's values have been read
+  if (rank == 0 && threadIdx.x == 0 && ok) *free_top = base + (int)Ftot;
 }
 
 // Fresh commit, one block per sequence (after fresh_stack_kernel): installs
@@ -279,7 +293,7 @@ cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream) {
 
 cudaError_t launch_fresh_commit(const LayoutLaunch& ll, cudaStream_t stream) {
   if (ll.chunks == 0) return cudaSuccess;
-  fresh_stack_kernel<<<1, 256, 0, stream>>>(ll.rows[0].Xtot, ll.Ftot_all, ll.freed, ll.free_ids,
+  fresh_stack_kernel<<<kStackCluster, 256, 0, stream>>>(ll.rows[0].Xtot, ll.Ftot_all, ll.freed, ll.free_ids,
                                             ll.free_top, ll.capacity, ll.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
