@@ -173,12 +173,17 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // Block-table rows after the release and the list of freed pages (sequence
-// order, ascending block order).  One CTA per sequence.
+// order, ascending block order).  kRowSplit CTAs per sequence, each taking every
+// kRowSplit-th stretch of 256 entries (every entry is independent).
+constexpr int kRowSplit = 8;
+
 __global__ void __launch_bounds__(256)
     rows_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
                 const int32_t* __restrict__ nblocks, int32_t* __restrict__ freed,
                 int32_t* __restrict__ new_rows, unsigned* status) {
-  const SeqMeta& s = meta.seq[blockIdx.x];
+  const SeqMeta& s = meta.seq[blockIdx.x / kRowSplit];
+  const int j0 = (int)(blockIdx.x % kRowSplit) * blockDim.x + threadIdx.x;
+  const int js = kRowSplit * blockDim.x;
   const int P = meta.P;
   const int f = s.nb - s.X;
   const int sb = s.s0 / P;
@@ -186,17 +191,17 @@ __global__ void __launch_bounds__(256)
   int32_t* out = new_rows + (int64_t)s.b * meta.max_blocks;
   const int nold = __ldg(nblocks + s.b);
   if (nold < sb + s.nb || nold > meta.max_blocks) {
-    if (threadIdx.x == 0) atomicOr(status, KVC_DEV_BAD_PAGE);
-    for (int j = threadIdx.x; j < meta.max_blocks; j += blockDim.x) out[j] = row[j];
+    if (j0 == 0) atomicOr(status, KVC_DEV_BAD_PAGE);
+    for (int j = j0; j < meta.max_blocks; j += js) out[j] = row[j];
     return;
   }
-  for (int j = threadIdx.x; j < meta.max_blocks; j += blockDim.x) {
+  for (int j = j0; j < meta.max_blocks; j += js) {
     int32_t v = row[j];
     if (j >= sb && j < nold - f) v = row[j + f];
     else if (j >= nold - f && j < nold) v = -1;
     out[j] = v;
   }
-  for (int i = threadIdx.x; i < f; i += blockDim.x) freed[s.foff + i] = row[sb + i];
+  for (int i = j0; i < f; i += js) freed[s.foff + i] = row[sb + i];
 }
 
 // One parallel copy.  A block copies up to kMovesPerBlock moves of one unit
@@ -346,7 +351,7 @@ cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
     }
     const LaunchMeta& r = cl.rows_meta[c];
     if (r.nseq > 0) {
-      rows_kernel<<<(unsigned)r.nseq, 256, 0, stream>>>(r, cl.block_table, cl.nblocks, cl.freed,
+      rows_kernel<<<(unsigned)(r.nseq * kRowSplit), 256, 0, stream>>>(r, cl.block_table, cl.nblocks, cl.freed,
                                                         cl.new_rows, cl.status);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
