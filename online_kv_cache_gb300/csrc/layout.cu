@@ -28,6 +28,7 @@ namespace kvc {
 namespace {
 
 constexpr int kStackCluster = 8;  // CTAs of the fresh-page stack push (one cluster)
+constexpr int kRowSplit = 8;      // CTAs per sequence for block-table rows (independent entries)
 
 
 constexpr int kSentinelChunk = 4096;       // positions per sentinel block
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Fresh plan, one block per sequence: the block-table row after the commit
+// Fresh plan, kRowSplit blocks per sequence: the block-table row after the commit
 // (the segment's nb entries replaced by the X fresh pages, later entries
 // shifted down by nb - X, vacated entries -1) and the sequence's nb old
 // pages at its offset of the call's return list.
@@ -174,7 +175,9 @@ __global__ void __launch_bounds__(256)
                       const int32_t* __restrict__ nblocks, const int32_t* __restrict__ free_ids,
                       const int32_t* __restrict__ free_top, int32_t* __restrict__ freed,
                       int32_t* __restrict__ new_rows, unsigned* status) {
-  const SeqMeta& s = meta.seq[blockIdx.x];
+  const SeqMeta& s = meta.seq[blockIdx.x / kRowSplit];
+  const int j0 = (int)(blockIdx.x % kRowSplit) * blockDim.x + threadIdx.x;
+  const int js = kRowSplit * blockDim.x;
   const int P = meta.P;
   const int32_t* row = block_table + (int64_t)s.b * meta.max_blocks;
   int32_t* out = new_rows + (int64_t)s.b * meta.max_blocks;
@@ -183,10 +186,10 @@ __global__ void __launch_bounds__(256)
   const int sb = s.s0 / P, f = s.nb - s.X;
   const bool active = s.m < s.n && top >= meta.Xtot;
   if (active && (nold < sb + s.nb || nold > meta.max_blocks)) {
-    if (threadIdx.x == 0) atomicOr(status, KVC_DEV_BAD_PAGE);
+    if (j0 == 0) atomicOr(status, KVC_DEV_BAD_PAGE);
   }
   const bool go = active && nold >= sb + s.nb && nold <= meta.max_blocks;
-  for (int jb = threadIdx.x; jb < meta.max_blocks; jb += blockDim.x) {
+  for (int jb = j0; jb < meta.max_blocks; jb += js) {
     int32_t v = row[jb];
     if (go) {
       if (jb >= sb && jb < sb + s.X) v = fresh_page(free_ids, top, (int64_t)s.xoff + (jb - sb));
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(256)
     out[jb] = v;
   }
   if (go)
-    for (int i = threadIdx.x; i < s.nb; i += blockDim.x) freed[s.foff + i] = row[sb + i];
+    for (int i = j0; i < s.nb; i += js) freed[s.foff + i] = row[sb + i];
 }
 
 // Fresh commit, one cluster of kStackCluster CTAs for the whole call: unless the
@@ -233,18 +236,20 @@ __global__ void __cluster_dims__(kStackCluster, 1, 1) __launch_bounds__(256)
   if (rank == 0 && threadIdx.x == 0 && ok) *free_top = base + (int)Ftot;
 }
 
-// Fresh commit, one block per sequence (after fresh_stack_kernel): installs
+// Fresh commit, kRowSplit blocks per sequence (after fresh_stack_kernel): installs
 // the planned row and lowers nblocks by nb - X, unless the stack step failed.
 __global__ void __launch_bounds__(256)
     fresh_install_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ new_rows,
                          int32_t* __restrict__ block_table, int32_t* __restrict__ nblocks,
                          const unsigned* status) {
-  const SeqMeta& s = meta.seq[blockIdx.x];
+  const SeqMeta& s = meta.seq[blockIdx.x / kRowSplit];
+  const int j0 = (int)(blockIdx.x % kRowSplit) * blockDim.x + threadIdx.x;
+  const int js = kRowSplit * blockDim.x;
   if (!(s.m < s.n)) return;
   if (*reinterpret_cast<const volatile unsigned*>(status) & KVC_DEV_FREE_STACK) return;
   const int64_t ro = (int64_t)s.b * meta.max_blocks;
-  for (int jb = threadIdx.x; jb < meta.max_blocks; jb += blockDim.x) block_table[ro + jb] = new_rows[ro + jb];
-  if (threadIdx.x == 0) nblocks[s.b] -= s.nb - s.X;
+  for (int jb = j0; jb < meta.max_blocks; jb += js) block_table[ro + jb] = new_rows[ro + jb];
+  if (j0 == 0) nblocks[s.b] -= s.nb - s.X;
 }
 
 }  // namespace
@@ -281,7 +286,7 @@ cudaError_t launch_fresh_plan(const LayoutLaunch& ll, cudaStream_t stream) {
     }
     const LaunchMeta& r = ll.rows[c];
     if (r.nseq > 0) {
-      fresh_rows_kernel<<<(unsigned)r.nseq, 256, 0, stream>>>(r, ll.block_table, ll.nblocks, ll.free_ids,
+      fresh_rows_kernel<<<(unsigned)(r.nseq * kRowSplit), 256, 0, stream>>>(r, ll.block_table, ll.nblocks, ll.free_ids,
                                                               ll.free_top, ll.freed, ll.new_rows, ll.status);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
@@ -301,7 +306,7 @@ cudaError_t launch_fresh_commit(const LayoutLaunch& ll, cudaStream_t stream) {
   for (size_t c = 0; c < ll.chunks; ++c) {
     const LaunchMeta& r = ll.rows[c];
     if (r.nseq <= 0) continue;
-    fresh_install_kernel<<<(unsigned)r.nseq, 256, 0, stream>>>(r, ll.new_rows, ll.block_table_mut,
+    fresh_install_kernel<<<(unsigned)(r.nseq * kRowSplit), 256, 0, stream>>>(r, ll.new_rows, ll.block_table_mut,
                                                                ll.nblocks, ll.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launch();
