@@ -250,7 +250,8 @@ kvc_status kvc_select_workspace_size(const kvc_cache *cache, const kvc_segments 
  * in ascending position order, segment-relative.
  * scores fp32 [L][H][Ntot] as written by kvc_score.
  * keep   out int32 [L][H][Mtot]; sequence b at offset sum_{b'<b} min(m_b', n_b').
- * Segments of fewer than 2^20 positions (KVC_ERR_UNSUPPORTED otherwise). */
+ * Segments of at most 2^20 - 4096 = 1044480 positions (KVC_ERR_UNSUPPORTED
+ * otherwise). */
 kvc_status kvc_select_topm(const kvc_cache *cache, const kvc_segments *segs, const float *scores,
                            const int32_t *m, int32_t *keep, void *ws, size_t ws_bytes,
                            kvc_stream_t stream);

@@ -674,8 +674,8 @@ kvc_status kvc_select_topm(const kvc_cache* cache, const kvc_segments* segs, con
   if (p.seqs.empty() || p.Mtot == 0) return ok();
   if (scores == nullptr || keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "scores or keep is NULL");
   for (const Seq& q : p.seqs)
-    if (q.n >= kSelectMaxSegment)
-      return fail(KVC_ERR_UNSUPPORTED, "segment of %d positions: selection takes fewer than %d", q.n,
+    if (q.n > kSelectMaxSegment)
+      return fail(KVC_ERR_UNSUPPORTED, "segment of %d positions: selection takes at most %d", q.n,
                   kSelectMaxSegment);
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;

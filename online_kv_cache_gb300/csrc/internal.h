@@ -132,9 +132,11 @@ struct LrfuLaunch {
   unsigned* status = nullptr;
 };
 
-// Segments the selection kernel takes: its per-warp 16-bit bin counts see at
-// most n / 16 elements per pass.
-constexpr int kSelectMaxSegment = 1 << 20;
+// Longest segment the selection kernel takes.  Its per-warp 16-bit bin counts
+// must stay below 2^16: with 16-byte loads a warp of the 16 counts 32 of every
+// 512 vectors (128 of every 2048 positions) plus at most 6 unaligned head and
+// tail positions, 510 * 128 + 6 = 65286 for n = 2^20 - 4096.
+constexpr int kSelectMaxSegment = (1 << 20) - 4096;
 
 // Longest segment the LRFU kernel takes: its per-warp 16-bit mass parts stay
 // below 2^32 for up to 2^16 elements per warp (16 warps).

@@ -37,6 +37,7 @@ constexpr int kSelThreads = 512;
 constexpr int kWarps = kSelThreads / 32;
 constexpr int kU = 8;                         // elements per thread per tile
 constexpr int kTileElems = kSelThreads * kU;  // element e of a tile: q * kSelThreads + tid
+constexpr int kV = 4;                         // 16-byte loads per thread in flight (counting passes)
 constexpr int kBins = 2048;
 // warp-private count histograms: two 16-bit bin counts per 32-bit word (a warp
 // sees at most 2^16 - 1 elements of a unit per pass for n < 2^20)
@@ -90,20 +91,35 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
     uint32_t* wh = whist + warp * kWarpWords;
     for (int i = lane; i < kWarpWords; i += 32) wh[i] = 0;
     __syncwarp();
+    // counting ignores order: 16-byte loads over the aligned body (kV in flight per
+    // thread), single elements over the unaligned head and tail
+    auto count = [&](uint32_t x) {
+      if ((x & pmask) == prefix) {
+        const uint32_t d = (x >> sh) & dmask;
+        atomicAdd(&wh[d >> 1], (d & 1u) ? 0x10000u : 1u);
+      }
+    };
+    const int lo_al = min(hi, lo + (int)((4u - (uint32_t)((reinterpret_cast<uintptr_t>(key + lo) >> 2) & 3u)) & 3u));
+    const int hi_al = lo_al + ((hi - lo_al) & ~3);
+    if (lo + tid < lo_al) count(__ldg(key + lo + tid));
+    if (hi_al + tid < hi) count(__ldg(key + hi_al + tid));
+    const uint4* kv = reinterpret_cast<const uint4*>(key + lo_al);
+    const int nv = (hi_al - lo_al) >> 2;
 #pragma unroll 1
-    for (int tile = lo; tile < hi; tile += kTileElems) {
-      uint32_t u[kU];
+    for (int v0 = 0; v0 < nv; v0 += kSelThreads * kV) {
+      uint4 u[kV];
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int i = tile + q * kSelThreads + tid;
-        u[q] = (i < hi) ? __ldg(key + i) : 0u;
+      for (int q = 0; q < kV; ++q) {
+        const int v = v0 + q * kSelThreads + tid;
+        u[q] = (v < nv) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int i = tile + q * kSelThreads + tid;
-        if (i < hi && (u[q] & pmask) == prefix) {
-          const uint32_t d = (u[q] >> sh) & dmask;
-          atomicAdd(&wh[d >> 1], (d & 1u) ? 0x10000u : 1u);
+      for (int q = 0; q < kV; ++q) {
+        if (v0 + q * kSelThreads + tid < nv) {
+          count(u[q].x);
+          count(u[q].y);
+          count(u[q].z);
+          count(u[q].w);
         }
       }
     }

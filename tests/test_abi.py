@@ -148,6 +148,19 @@ def test_budget_and_plan_validation(lib):
                                None) == kvc.KVC_ERR_INVALID_ARG
 
 
+def test_select_rejects_overlong_segments_before_any_launch(lib):
+    """Selection takes segments of at most 2^20 - 4096 positions (its per-warp 16-bit bin counts);
+    one position more is KVC_ERR_UNSUPPORTED, decided on the host."""
+    longest = (1 << 20) - 4096
+    c = fake_cache(L=1, num_pages=16384, H=1, P=64, d=128, max_blocks=16384, batch=1)
+    for n in (longest + 1, 1 << 20):
+        s, keep_alive = segs([0], [n], [n])
+        m = np.array([100], np.int32)
+        st = lib.kvc_select_topm(ctypes.byref(c), ctypes.byref(s), 0x100, m.ctypes.data, 0x200, None, 0, None)
+        assert st == kvc.KVC_ERR_UNSUPPORTED
+        assert str(longest) in kvc.kvc_last_error()
+
+
 def test_status_strings(lib):
     for st in range(-7, 1):
         assert kvc.kvc_status_string(st).startswith("KVC_")
