@@ -405,14 +405,46 @@ __global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, f
   }
 }
 
+// ------------------------------------------------------------------ row ring
+// The descents read one row of a Gram matrix per step.  Rows stream from L2
+// into a ring of kRing shared-memory buffers, kAhead = kRing - 2 steps ahead
+// of use.  The buffer refilled at step st was last read at step st - 2, and
+// every thread has passed step st - 1's barriers before it issues the copy,
+// so no copy lands in a buffer that is still being read.  (Two buffers with
+// the copy one step ahead would refill the buffer of step st - 1 while slower
+// threads may still be reading it.)  Deeper rings (4, 6 buffers) measured no
+// faster.
+constexpr int kRing = 3;
+constexpr int kAhead = kRing - 2;
+
+struct RowRing {
+  float* rows;      // [kRing][m] shared
+  const float* Mx;  // the Gram matrix, leading dimension ld
+  int64_t ld;
+  int m;
+  int row = 0, buf = 0;  // row and buffer of the next copy
+  // Issue the next row's copy when `live`; commit a group either way, so that
+  // group k always belongs to step k.
+  __device__ __forceinline__ void issue(bool live) {
+    if (live) {
+      const float* src = Mx + (int64_t)row * ld;
+      float* dst = rows + buf * m;
+      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(dst + i, src + i);
+    }
+    cp_async_commit();
+    row = (row + 1 == m) ? 0 : row + 1;
+    buf = (buf + 1 == kRing) ? 0 : buf + 1;
+  }
+};
+
 // ------------------------------------------------------------------ mass fit
 // Block = unit.  Projected cyclic coordinate descent on min_{w >= 0} ||E w - s||^2
 // from w = 1: with g = G w - b, coordinate j moves to max(0, w_j - g_j / G_jj)
 // and g follows by the change times column j of G (= row j, G symmetric).
 // Coordinate j moves only when |g_j| > 2^-14 b_j (every term of G w and of
-// b = E^T s is >= 0, so b_j is their scale).  Row j + 1 of G streams into
-// shared memory while step j runs.  Two barriers per step: every thread reads
-// g_j and w_j before any of them is updated.
+// b = E^T s is >= 0, so b_j is their scale).  Rows of G stream through the
+// row ring.  Two barriers per step: every thread reads g_j and w_j before any
+// of them is updated.
 // Writes w (workspace), beta = ln w (-inf at 0) to `beta` and to the per-slot
 // state of each kept entry.
 __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
@@ -425,7 +457,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
   float* w = g + m;           // [m]
   float* diag = w + m;        // [m]
   float* bvec = diag + m;     // [m] b = E^T s
-  float* rows = bvec + m;     // [2][m]
+  float* rows = bvec + m;     // [kRing][m]
   const float* G = u.base + am_off_G(meta.R, u.ldE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < m; i += kAmThreads / 32) {  // g = G 1 - b, one warp per row
@@ -442,29 +474,24 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
     }
   }
   const int64_t steps = (int64_t)meta.sweeps * m;
-  if (steps > 0) {
-    for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + i, G + i);
-    cp_async_commit();
-  }
+  RowRing ring{rows, G, u.ldE, m};
+  for (int p = 0; p < kAhead; ++p) ring.issue(p < steps);
+  int j = 0, cb = 0;  // step st's row and ring buffer
   for (int64_t st = 0; st < steps; ++st) {
-    const int j = (int)(st % m);
-    const int buf = (int)(st & 1);
-    if (st + 1 < steps) {  // prefetch the next step's row (its buffer was read in step st - 1)
-      const float* nr = G + (int64_t)((st + 1) % m) * u.ldE;
-      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + (buf ^ 1) * m + i, nr + i);
-    }
-    cp_async_commit();
-    cp_async_wait_group<1>();
+    ring.issue(st + kAhead < steps);
+    cp_async_wait_group<kAhead>();  // this thread's copies of step st's row are in
     __syncthreads();
     const float gj = g[j], wj = w[j], Gjj = diag[j];
     const float nw = (Gjj > 0.0f && fabsf(gj) > kAmGuard * bvec[j]) ? fmaxf(0.0f, wj - gj / Gjj) : wj;
     const float dl = nw - wj;
     __syncthreads();
     if (dl != 0.0f) {
-      const float* rj = rows + buf * m;
+      const float* rj = rows + cb * m;
       for (int i = threadIdx.x; i < m; i += kAmThreads) g[i] = fmaf(dl, rj[i], g[i]);
       if (threadIdx.x == 0) w[j] = nw;
     }
+    j = (j + 1 == m) ? 0 : j + 1;
+    cb = (cb + 1 == kRing) ? 0 : cb + 1;
   }
   cp_async_wait_all();
   __syncthreads();
@@ -505,9 +532,11 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
 constexpr int kValueCols = 8;  // value-fit columns per block (32 row slices x 8 columns)
 
 __host__ __device__ constexpr int value_smem_bytes(int m) {
-  return (2 * m * kValueCols + 4 * m + (kAmThreads / kValueCols + 1) * kValueCols) * 4;
+  return (2 * m * kValueCols + (2 + kRing) * m + (kAmThreads / kValueCols + 1) * kValueCols) * 4;
 }
-__host__ __device__ constexpr int mass_smem_bytes(int m) { return 6 * m * 4; }
+__host__ __device__ constexpr int mass_smem_bytes(int m) { return (4 + kRing) * m * 4; }
+static_assert(value_smem_bytes(kAmMaxM) <= 227 * 1024 && mass_smem_bytes(kAmMaxM) <= 227 * 1024,
+              "descent working sets fit one CTA's shared memory at the largest m");
 
 // ------------------------------------------------------------------ value fit
 // Block = (unit, 8 of the d value columns).  The columns are independent
@@ -515,8 +544,8 @@ __host__ __device__ constexpr int mass_smem_bytes(int m) { return 6 * m * 4; }
 // X = the kept values, gradient Gv = H X - Bm kept in shared memory; row j of
 // X moves by -Gv_j / H_jj and Gv follows by column j of H (= row j) times the
 // change, when |Gv_jc| > 2^-14 pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic|
-// + max_k |X0_kc|: the scale of the gradient's terms in column c).  Row j + 1
-// of H streams in while step j runs.  At the end V_C is
+// + max_k |X0_kc|: the scale of the gradient's terms in column c).  Rows of H
+// stream through the row ring.  At the end V_C is
 // written to `vc` (fp32) and over the kept entries' V rows (bf16, round to
 // nearest even).
 template <int D>
@@ -532,8 +561,8 @@ __global__ void __launch_bounds__(kAmThreads) am_value_kernel(const AmMeta meta,
   float* X = Gv + m * kValueCols;      // [m][8]
   float* hdiag = X + m * kValueCols;   // [m]
   float* pi = hdiag + m;               // [m]
-  float* rows = pi + m;                // [2][m]
-  float* red = rows + 2 * m;           // [32][8] partial column scales, then S[8]
+  float* rows = pi + m;                // [kRing][m]
+  float* red = rows + kRing * m;       // [32][8] partial column scales, then S[8]
   const float* Hm = u.base + am_off_G(meta.R, u.ldE);
   const float* Bm = u.base + am_off_Bm(meta.R, m, u.ldE, D);
   const int c = threadIdx.x & (kValueCols - 1), r = threadIdx.x / kValueCols;
@@ -584,29 +613,24 @@ __global__ void __launch_bounds__(kAmThreads) am_value_kernel(const AmMeta meta,
   __syncthreads();
   const float Sc = red[kSlices * kValueCols + c];
   const int64_t steps = (int64_t)meta.sweeps * m;
-  if (steps > 0) {
-    for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + i, Hm + i);
-    cp_async_commit();
-  }
+  RowRing ring{rows, Hm, u.ldE, m};
+  for (int p = 0; p < kAhead; ++p) ring.issue(p < steps);
+  int j = 0, cb = 0;  // step st's row and ring buffer
   for (int64_t st = 0; st < steps; ++st) {
-    const int j = (int)(st % m);
-    const int buf = (int)(st & 1);
-    if (st + 1 < steps) {
-      const float* nr = Hm + (int64_t)((st + 1) % m) * u.ldE;
-      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(rows + (buf ^ 1) * m + i, nr + i);
-    }
-    cp_async_commit();
-    cp_async_wait_group<1>();
+    ring.issue(st + kAhead < steps);
+    cp_async_wait_group<kAhead>();  // this thread's copies of step st's row are in
     __syncthreads();
     const float Hjj = hdiag[j];
     const float gv = Gv[j * kValueCols + c];
     const float dl = (Hjj > 0.0f && fabsf(gv) > kAmGuard * pi[j] * Sc) ? -gv / Hjj : 0.0f;
     __syncthreads();
     if (dl != 0.0f) {
-      const float* rj = rows + buf * m;
+      const float* rj = rows + cb * m;
       for (int i = r; i < m; i += kSlices) Gv[i * kValueCols + c] = fmaf(rj[i], dl, Gv[i * kValueCols + c]);
       if (r == 0) X[j * kValueCols + c] += dl;
     }
+    j = (j + 1 == m) ? 0 : j + 1;
+    cb = (cb + 1 == kRing) ? 0 : cb + 1;
   }
   cp_async_wait_all();
   __syncthreads();
