@@ -164,15 +164,31 @@ __device__ __forceinline__ float sum16(float v) {
   return v;
 }
 
+// Targets tiling: 128 proxy rows per block, keys in tiles of 64.
+constexpr int kTgRows = 128;
+constexpr int kTgKeys = 64;
+constexpr int kTgPs = kTgRows + 1;  // row stride of the probability tile (fewer bank conflicts)
+
 template <int D>
-constexpr int targets_smem_bytes() {
-  return (2 * 64 * (D + 1) + 64 * D + 64 * 65) * 4;
+constexpr int targets_kp_floats() {  // Kt [D][64], later Pt [64][129] in the same place
+  return D * kTgKeys > kTgKeys * kTgPs ? D * kTgKeys : kTgKeys * kTgPs;
+}
+
+template <int D>
+constexpr int targets_smem_bytes() {  // Qt [D][128], Kt / Pt, Vs [64][D]
+  return (D * kTgRows + targets_kp_floats<D>() + kTgKeys * D) * 4;
 }
 
 // ------------------------------------------------------------------ targets
-// Block = (unit, 64 proxy rows).  Online softmax over all n keys of the
-// segment: per row the running max, the running sum and Y = sum_j p_ij v_j.
-// Writes LSE (natural log) and Y = softmax(L) V to the unit's workspace.
+// Block = (unit, 128 proxy rows), 16 x 16 threads.  Online softmax over all n
+// keys of the segment in tiles of 64.  Thread (ty, tx) forms the logits of rows
+// 8 ty .. 8 ty + 7 against keys 4 tx .. 4 tx + 3 of the tile from Q and K held
+// dimension-major in shared memory (three 128-bit loads per 32 multiply-adds),
+// keeps the rows' running max (common to the 16 threads of a row, through
+// shuffles) and its own share of their running sums, and accumulates Y rows
+// 8 ty .. 8 ty + 7, columns tx D/16 .. tx D/16 + D/16 - 1 from the tile's
+// probabilities (key-major, over the key tile once the logits are formed) and
+// values.  Writes LSE (natural log) and Y = softmax(L) V to the unit's workspace.
 template <int D>
 __global__ void __launch_bounds__(kAmThreads) am_targets_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
                                                                 const uint16_t* __restrict__ kp,
@@ -180,95 +196,148 @@ __global__ void __launch_bounds__(kAmThreads) am_targets_kernel(const AmMeta met
                                                                 const uint16_t* __restrict__ q, float* ws,
                                                                 unsigned* status) {
   extern __shared__ __align__(16) float am_smem[];
-  float* Qs = am_smem;                 // [64][D + 1]
-  float* Ks = Qs + 64 * (D + 1);       // [64][D + 1]
-  float* Vs = Ks + 64 * (D + 1);       // [64][D]
-  float* Ps = Vs + 64 * D;             // [64][65]
-  const int rb = (meta.R + 63) / 64;
+  constexpr int kCpt = D / 16;  // Y columns per thread
+  constexpr int kChunks = D / 8;
+  float* Qt = am_smem;                            // [D][128]
+  float* Kt = Qt + D * kTgRows;                   // [D][64]
+  float* Pt = Kt;                                 // [64][129]
+  float* Vs = Kt + targets_kp_floats<D>();        // [64][D]
+  const int rb = (meta.R + kTgRows - 1) / kTgRows;
   const int64_t unit = blockIdx.x / rb;
-  const int r0 = (int)(blockIdx.x % rb) * 64;
+  const int r0 = (int)(blockIdx.x % rb) * kTgRows;
   const AmUnit u = am_unit(meta, unit, ws);
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   const int64_t qrow0 = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
-  load_rows64<D>(Qs, q, [&](int i) -> int64_t { return r0 + i < meta.R ? qrow0 + r0 + i : -1; });
-  const float c2 = meta.scale * kLog2e;
-  float mx[4], sm[4], y[4][D / 16];
+  for (int ci = threadIdx.x; ci < kTgRows * kChunks; ci += kAmThreads) {  // Q (zero past R)
+    const int i = ci % kTgRows, dc = ci / kTgRows;
+    float v[8];
+    if (r0 + i < meta.R) {
+      unpack8(*reinterpret_cast<const uint4*>(q + (qrow0 + r0 + i) * D + dc * 8), v);
+    } else {
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
+      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Qt[(dc * 8 + e) * kTgRows + i] = v[e];
+  }
+  const float c2 = meta.scale * kLog2e;
+  float mx[8], sm[8], y[8][kCpt];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
     mx[a] = -INFINITY;
     sm[a] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < D / 16; ++e) y[a][e] = 0.0f;
+    for (int e = 0; e < kCpt; ++e) y[a][e] = 0.0f;
   }
-  for (int j0 = 0; j0 < u.n; j0 += 64) {
-    __syncthreads();  // previous tile's Ks, Vs, Ps fully read
-    auto row_of = [&](int i) -> int64_t { return j0 + i < u.n ? am_row(meta, u, bt, j0 + i, status) : -1; };
-    load_rows64<D>(Ks, kp, row_of);
-    {  // values, row stride D
-      constexpr int kChunks = D / 8;
-      for (int ci = threadIdx.x; ci < 64 * kChunks; ci += kAmThreads) {
-        const int i = ci / kChunks, dc = ci % kChunks;
-        const int64_t row = row_of(i);
-        float v[8];
-        if (row >= 0) {
-          unpack8(*reinterpret_cast<const uint4*>(vp + row * D + dc * 8), v);
-        } else {
+  // The next tile's keys and values are loaded into registers while this
+  // tile's products run (kLd 16-byte chunks of each per thread).
+  constexpr int kLd = kTgKeys * kChunks / kAmThreads;
+  static_assert(kLd * kAmThreads == kTgKeys * kChunks, "tile chunks split evenly over the threads");
+  uint4 kr[kLd], vr[kLd];
+  auto fetch = [&](int t0) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = 0.0f;
-        }
+    for (int c = 0; c < kLd; ++c) {
+      const int ci = threadIdx.x + c * kAmThreads;
+      const int ik = ci % kTgKeys, dk = ci / kTgKeys;  // keys: consecutive threads on consecutive keys
+      const int iv = ci / kChunks, dv = ci % kChunks;  // values: consecutive threads along a row
+      const int64_t rk = t0 + ik < u.n ? am_row(meta, u, bt, t0 + ik, status) : -1;
+      const int64_t rv = t0 + iv < u.n ? am_row(meta, u, bt, t0 + iv, status) : -1;
+      kr[c] = rk >= 0 ? *reinterpret_cast<const uint4*>(kp + rk * D + dk * 8) : make_uint4(0u, 0u, 0u, 0u);
+      vr[c] = rv >= 0 ? *reinterpret_cast<const uint4*>(vp + rv * D + dv * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  fetch(0);
+  for (int j0 = 0; j0 < u.n; j0 += kTgKeys) {
+    __syncthreads();  // the previous tile's Pt and Vs are fully read
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Vs[i * D + dc * 8 + e] = v[e];
-      }
+    for (int c = 0; c < kLd; ++c) {  // keys dimension-major, values key-major; bf16 bits -> fp32 (zero rows stay zero)
+      const int ci = threadIdx.x + c * kAmThreads;
+      const int ik = ci % kTgKeys, dk = ci / kTgKeys;
+      const int iv = ci / kChunks, dv = ci % kChunks;
+      float v[8];
+      unpack8(kr[c], v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) Kt[(dk * 8 + e) * kTgKeys + ik] = v[e];
+      unpack8(vr[c], v);
+      float4* dst = reinterpret_cast<float4*>(Vs + iv * D + dv * 8);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
     __syncthreads();
-    float acc[4][4];
-    dot64<D>(Qs, Ks, ty, tx, acc);
+    if (j0 + kTgKeys < u.n) fetch(j0 + kTgKeys);
+    float acc[8][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+#pragma unroll 2
+    for (int k = 0; k < D; ++k) {
+      const float4 q0 = *reinterpret_cast<const float4*>(Qt + k * kTgRows + ty * 8);
+      const float4 q1 = *reinterpret_cast<const float4*>(Qt + k * kTgRows + ty * 8 + 4);
+      const float4 k0 = *reinterpret_cast<const float4*>(Kt + k * kTgKeys + tx * 4);
+      const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      const float kv[4] = {k0.x, k0.y, k0.z, k0.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], kv[b], acc[a][b]);
+    }
+    __syncthreads();  // every thread's logits are formed: Kt is free for Pt
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
       float t[4], tmax = -INFINITY;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        t[b] = (j0 + tx + 16 * b < u.n) ? acc[a][b] * c2 : -INFINITY;
+        t[b] = (j0 + tx * 4 + b < u.n) ? acc[a][b] * c2 : -INFINITY;
         tmax = fmaxf(tmax, t[b]);
       }
-      const float mnew = fmaxf(mx[a], max16(tmax));
-      const float alpha = exp2f(mx[a] - mnew);  // 0 on the first tile (mx = -inf)
+      const float mnew = fmaxf(mx[a], max16(tmax));  // finite: key j0 is in the segment
+      const float alpha = exp2f(mx[a] - mnew);        // 0 on the first tile (mx = -inf)
       float ps = 0.0f;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const float p = exp2f(t[b] - mnew);
-        Ps[(ty + 16 * a) * 65 + tx + 16 * b] = p;
+        Pt[(tx * 4 + b) * kTgPs + ty * 8 + a] = p;
         ps += p;
       }
-      sm[a] = sm[a] * alpha + sum16(ps);
+      sm[a] = sm[a] * alpha + ps;
       mx[a] = mnew;
 #pragma unroll
-      for (int e = 0; e < D / 16; ++e) y[a][e] *= alpha;
+      for (int e = 0; e < kCpt; ++e) y[a][e] *= alpha;
     }
     __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < 64; ++j) {
-      float pv[4];
+#pragma unroll 2
+    for (int j = 0; j < kTgKeys; ++j) {
+      float pv[8], vv[kCpt];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) pv[a] = Ps[(ty + 16 * a) * 65 + j];
+      for (int a = 0; a < 8; ++a) pv[a] = Pt[j * kTgPs + ty * 8 + a];
 #pragma unroll
-      for (int e = 0; e < D / 16; ++e) {
-        const float v = Vs[j * D + tx + 16 * e];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) y[a][e] = fmaf(pv[a], v, y[a][e]);
+      for (int e = 0; e < kCpt; e += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * D + tx * kCpt + e);
+        vv[e] = v4.x;
+        vv[e + 1] = v4.y;
+        vv[e + 2] = v4.z;
+        vv[e + 3] = v4.w;
       }
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int e = 0; e < kCpt; ++e) y[a][e] = fmaf(pv[a], vv[e], y[a][e]);
     }
   }
   float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
   float* lse = u.base + am_off_lse(meta.R, u.m, u.ldE, D);
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int i = r0 + ty + 16 * a;
+  for (int a = 0; a < 8; ++a) {
+    const float s = sum16(sm[a]);  // every lane takes part in the shuffles
+    const int i = r0 + ty * 8 + a;
     if (i >= meta.R) continue;
-    const float inv = 1.0f / sm[a];
+    const float inv = 1.0f / s;
 #pragma unroll
-    for (int e = 0; e < D / 16; ++e) Y[(int64_t)i * D + tx + 16 * e] = y[a][e] * inv;
-    if (tx == 0) lse[i] = (mx[a] + log2f(sm[a])) * kLn2;
+    for (int e = 0; e < kCpt; e += 4)
+      *reinterpret_cast<float4*>(Y + (int64_t)i * D + tx * kCpt + e) =
+          make_float4(y[a][e] * inv, y[a][e + 1] * inv, y[a][e + 2] * inv, y[a][e + 3] * inv);
+    if (tx == 0) lse[i] = (mx[a] + log2f(s)) * kLn2;
   }
 }
 
@@ -676,7 +745,8 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if (m.units <= 0) continue;
     const int rb64 = (m.R + 63) / 64;
     const int mt = (m.max_m + 63) / 64;
-    am_targets_kernel<D><<<(unsigned)(m.units * rb64), kAmThreads, targets_smem_bytes<D>(), stream>>>(
+    const int rbt = (m.R + kTgRows - 1) / kTgRows;
+    am_targets_kernel<D><<<(unsigned)(m.units * rbt), kAmThreads, targets_smem_bytes<D>(), stream>>>(
         m, al.block_table, kp, vp, al.q, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_exp_kernel<D><<<(unsigned)(m.units * rb64 * mt), kAmThreads, exp_smem_bytes<D>(), stream>>>(
