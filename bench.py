@@ -58,6 +58,9 @@ def parse_args():
                     help="override the workload's layer count (small profiling cases)")
     ap.add_argument("--seqs", type=int, default=None,
                     help="keep the workload's first N sequences (small profiling cases)")
+    ap.add_argument("--qdist", choices=["normal", "planted4", "aligned"], default=None,
+                    help="override the workload's proxy-query distribution (e.g. diffuse 'normal' "
+                         "queries, where Attention Matching has mass to recover)")
     ap.add_argument("--am-sweeps", type=int, default=0,
                     help="Attention Matching after the selection: fit the bias and the compact "
                          "values of the kept entries with this many coordinate-descent sweeps "
@@ -352,6 +355,8 @@ def our_arm(args):
     sp = workloads.spec(args.workload, args.seed)
     if args.layers:
         sp = dataclasses.replace(sp, L=args.layers)
+    if args.qdist:
+        sp = dataclasses.replace(sp, qdist=args.qdist)
     if args.seqs:
         bud = sp.budget if sp.budget[0] != "actkv" else ("actkv", sp.budget[1][:args.seqs])
         sp = dataclasses.replace(sp, lengths=sp.lengths[:args.seqs], budget=bud)

@@ -169,11 +169,14 @@ def test_keep_all_reproduces_the_full_attention():
         assert np.sqrt(am.mass_objective(u["E"], u["s"], np.exp(beta[l, h]))) <= RES_TOL * np.linalg.norm(u["s"])
 
 
-def test_am_multi_turn_shape_sampled():
+@pytest.mark.parametrize("qdist", ["planted4", "normal"])
+def test_am_multi_turn_shape_sampled(qdist):
     """The delay-1 multi-turn compaction shape (28 layers, 2 KV heads, 16 query heads x 128 rows:
     R = 2048 > m = 307), 8 sweeps, in the launch configuration the benchmark times; six units
-    sampled for the oracle."""
-    sp = workloads.spec("multi-turn")
+    sampled for the oracle.  With the planted proxy queries token eviction already holds the
+    mass (the fits stay at their start); with diffuse ones every coordinate moves."""
+    import dataclasses
+    sp = dataclasses.replace(workloads.spec("multi-turn"), qdist=qdist)
     case = workloads.build(sp, 0, DEV)
     m = [oracle.budget_ratio(n, 0.2) for n in PT.seg_lengths(case)]
     s_orc, _ = oracle.score_cache(case.k_pool, case.block_table, case.nblocks, case.seg_start, case.seg_end,
