@@ -312,3 +312,54 @@ def test_free_stack_overflow_pushes_nothing():
     assert kvc.kvc_read_device_status(clear=True) == kvc.KVC_DEV_FREE_STACK
     assert int(case.free_top.item()) == top
     assert torch.equal(case.free_ids.cpu(), ids_before)
+
+
+def test_selection_at_the_longest_segment():
+    """Selection at its longest segment, 2^20 - 4096 positions, with 304 units (8 KV heads x 38
+    sequences), so that each unit runs in one CTA: the case where a warp's 16-bit bin counts
+    come closest to 2^16.  Sequences of even index hold one score everywhere (every count of a
+    pass lands in one bin; the lowest m positions win), the others seeded uniform scores.  The
+    oracle's sort-based top-m is compared on three sampled units; on every unit the properties
+    that hold at any size: m strictly ascending positions inside the segment, every kept score
+    >= every evicted one, and among scores equal to the smallest kept one the kept positions
+    come first.  Selection reads only the scores, so the pools are a token page."""
+    n, B, H, P = (1 << 20) - 4096, 38, 8, 64
+    nb = n // P
+    k_pool = torch.zeros((1, 1, H, P, 64), dtype=torch.bfloat16, device=DEV)
+    v_pool = torch.zeros_like(k_pool)
+    tags = torch.zeros((1, 1, H, P), dtype=torch.int32, device=DEV)
+    block_table = torch.zeros((B, nb), dtype=torch.int32, device=DEV)
+    nblocks = torch.full((B,), nb, dtype=torch.int32, device=DEV)
+    cache = kvc.Cache(k_pool, v_pool, tags, block_table, nblocks)
+    segs = kvc.Segments([0] * B, [n] * B, [n] * B)
+    mb = oracle.budget_ratio(n, 0.2)
+    m = [mb] * B
+    g = torch.Generator(device=DEV).manual_seed(2024)
+    scores = torch.rand((1, H, B * n), generator=g, device=DEV)
+    for b in range(0, B, 2):
+        scores[:, :, b * n:(b + 1) * n] = 0.5
+    keep = torch.full((1, H, B * mb), -1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(256, kvc.kvc_select_workspace_size(cache, segs, m)), dtype=torch.uint8, device=DEV)
+    kvc.kvc_select_topm(cache, segs, scores, m, keep, ws)
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    lowest = torch.arange(mb, dtype=torch.int32, device=DEV)
+    for h in range(H):
+        for b in range(B):
+            s = scores[0, h, b * n:(b + 1) * n]
+            k = keep[0, h, b * mb:(b + 1) * mb]
+            if b % 2 == 0:
+                assert torch.equal(k, lowest), (h, b)
+                continue
+            assert int(k[0]) >= 0 and int(k[-1]) < n and bool((k[1:] > k[:-1]).all()), (h, b)
+            kept = torch.zeros(n, dtype=torch.bool, device=DEV)
+            kept[k.long()] = True
+            t = s[k.long()].min()
+            assert bool((s[~kept] <= t).all()), (h, b)
+            tie = s == t
+            if bool((tie & ~kept).any()):
+                assert int(torch.nonzero(tie & kept).max()) < int(torch.nonzero(tie & ~kept).min()), (h, b)
+    for (h, b) in ((0, 1), (5, 19), (7, 37)):
+        s = scores[0, h, b * n:(b + 1) * n].cpu().numpy().astype(np.float64)
+        want = oracle.select_cache(s[None, None, :], [0], [n], [mb])[0, 0]
+        assert np.array_equal(keep[0, h, b * mb:(b + 1) * mb].cpu().numpy(), want), (h, b)
