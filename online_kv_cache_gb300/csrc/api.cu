@@ -744,7 +744,16 @@ kvc_status check_plan(const kvc_cache* cache, const Plan& p, const kvc_plan* pla
   return KVC_OK;
 }
 
-void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta>* plan_m,
+// Moves per copy block: 128, or fewer (down to 16) when the launch moves too
+// little to give every SM 16 blocks: a small compaction is bound by the latency
+// of each warp's chain of dependent loads, not by bandwidth.
+int copy_moves_per_block(int64_t moves, int num_sms) {
+  int mpb = 128;
+  while (mpb > 16 && ceil_div(moves, mpb) < (int64_t)num_sms * 16) mpb >>= 1;
+  return mpb;
+}
+
+void compact_metas(const kvc_cache* cache, const Plan& p, int num_sms, std::vector<LaunchMeta>* plan_m,
                    std::vector<LaunchMeta>* rows_m, std::vector<LaunchMeta>* copy_m,
                    std::vector<LaunchMeta>* free_m) {
   const int64_t LH = (int64_t)cache->num_layers * cache->num_kv_heads;
@@ -754,6 +763,9 @@ void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta
                f = base_meta(cache, p);
     const int nseq = (int)(hi - lo);
     a.nseq = r.nseq = c.nseq = f.nseq = nseq;
+    int64_t moves = 0;
+    for (size_t i = lo; i < hi; ++i) moves += LH * p.seqs[i].m;
+    c.mpb = copy_moves_per_block(moves, num_sms);
     int64_t ia = 0, ic = 0, fc = 0;
     for (size_t i = lo; i < hi; ++i) {
       const size_t j = i - lo;
@@ -762,8 +774,8 @@ void compact_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta
       a.seq[j].item0 = ia;
       ia += LH;  // one planning CTA per unit
       a.words = std::max<int32_t>(a.words, (int32_t)ceil_div((int64_t)q.X * P, 32));
-      c.seq[j].item0 = ic;  // copy blocks: one per (unit, 128 moves)
-      ic += LH * std::max<int64_t>(1, ceil_div(q.m, 128));
+      c.seq[j].item0 = ic;  // copy blocks: one per (unit, mpb moves)
+      ic += LH * std::max<int64_t>(1, ceil_div(q.m, c.mpb));
       fc += q.nb - q.X;
     }
     a.items = ia;
@@ -796,7 +808,7 @@ kvc_status kvc_plan_compact(const kvc_cache* cache, const kvc_segments* segs, co
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
   std::vector<LaunchMeta> pm, rm, cm, fm;
-  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  compact_metas(cache, p, di.num_sms, &pm, &rm, &cm, &fm);
   CompactLaunch cl;
   cl.num_sms = di.num_sms;
   cl.chunks = pm.size();
@@ -830,7 +842,7 @@ kvc_status kvc_compact(const kvc_cache* cache, const kvc_segments* segs, const i
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
   std::vector<LaunchMeta> pm, rm, cm, fm;
-  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  compact_metas(cache, p, di.num_sms, &pm, &rm, &cm, &fm);
   CompactLaunch cl;
   cl.num_sms = di.num_sms;
   cl.chunks = cm.size();
@@ -864,7 +876,7 @@ kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, cons
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
   std::vector<LaunchMeta> pm, rm, cm, fm;
-  compact_metas(cache, p, &pm, &rm, &cm, &fm);
+  compact_metas(cache, p, di.num_sms, &pm, &rm, &cm, &fm);
   CompactLaunch cl;
   cl.num_sms = di.num_sms;
   cl.chunks = fm.size();

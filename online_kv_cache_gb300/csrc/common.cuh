@@ -45,6 +45,7 @@ struct LaunchMeta {
   int32_t qbytes;   // shared-memory bytes of one resident row group
   int32_t log2P;    // log2(P)
   int32_t words;    // plan: 32-bit bitmap words covering the largest target region
+  int32_t mpb;      // copy: moves per block
   float scale;      // logit scale
   float pw;         // score pass 2: power of alpha summed per key (2: eviction score, 1: action attention)
   int64_t Ntot, Mtot, Ftot;

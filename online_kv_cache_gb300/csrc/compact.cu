@@ -29,7 +29,6 @@ namespace kvc {
 namespace {
 
 constexpr int kPlanThreads = 512;
-constexpr int kMovesPerBlock = 128;
 
 __device__ __forceinline__ int32_t phys_slot(const int32_t* bt_row, int slot, int P, int num_pages,
                                              unsigned* status) {
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(256)
   for (int i = j0; i < f; i += js) freed[s.foff + i] = row[sb + i];
 }
 
-// One parallel copy.  A block copies up to kMovesPerBlock moves of one unit
+// One parallel copy.  A block copies up to meta.mpb moves of one unit
 // (the unit is decoded once per block): each move moves a K row and a V row
 // (d bf16 each, 16-byte vectors, D/4 lanes per move), the tag and, when the
 // cache has one, the per-slot aux value; U moves are
@@ -224,7 +223,7 @@ __global__ void __launch_bounds__(256)
   const int64_t item = blockIdx.x;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
-  const int per = max(1, (s.m + kMovesPerBlock - 1) / kMovesPerBlock);
+  const int per = max(1, (s.m + meta.mpb - 1) / meta.mpb);
   const int64_t local = item - s.item0;
   const int chunk = (int)(local % per);
   const int64_t lh = local / per;
@@ -234,7 +233,7 @@ __global__ void __launch_bounds__(256)
   const int64_t HP = (int64_t)meta.H * P;
   const int64_t lbase = (int64_t)l * meta.num_pages * HP + (int64_t)h * P;
   const int cnt = __ldg(move_count + u);
-  const int k0 = chunk * kMovesPerBlock, k1 = min(k0 + kMovesPerBlock, cnt);
+  const int k0 = chunk * meta.mpb, k1 = min(k0 + meta.mpb, cnt);
   const int2* mv = reinterpret_cast<const int2*>(moves) + (lh * meta.Mtot + s.moff);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
