@@ -363,3 +363,30 @@ def test_selection_at_the_longest_segment():
         s = scores[0, h, b * n:(b + 1) * n].cpu().numpy().astype(np.float64)
         want = oracle.select_cache(s[None, None, :], [0], [n], [mb])[0, 0]
         assert np.array_equal(keep[0, h, b * mb:(b + 1) * mb].cpu().numpy(), want), (h, b)
+
+
+@pytest.mark.parametrize("lengths,tied", [
+    ((2, 3, 17, 1024), True),    # every unit sorted whole (the launch's longest segment <= 1024)
+    ((2, 3, 17, 1024), False),
+    ((1025, 40), True),          # one position more: the radix path for the whole launch
+])
+def test_short_unit_selection(lengths, tied):
+    """The selection of short units (sorted whole in shared memory) and just above its limit
+    (radix passes), on seeded scores fed in directly, with exact ties: the keep sets equal the
+    oracle's sort-based top-m exactly, budgets 1 .. n - 1 included."""
+    sp = workloads.custom(L=2, H=2, G=2, d=64, P=16, q=2, lengths=lengths)
+    case = workloads.build(sp, 6, DEV, with_q=False)
+    n = PT.seg_lengths(case)
+    m = [max(1, min(x - 1, oracle.budget_ratio(x, 0.3))) for x in n]
+    cp = PT.compactor(case, m)
+    g = torch.Generator(device=DEV).manual_seed(91)
+    if tied:
+        s = torch.randint(0, 6, (sp.L, sp.H, cp.Ntot), generator=g, device=DEV).float() / 4.0
+    else:
+        s = torch.rand((sp.L, sp.H, cp.Ntot), generator=g, device=DEV)
+    cp.scores[:, :, :cp.Ntot] = s
+    cp.select()
+    torch.cuda.synchronize()
+    PT.device_status_clean()
+    keep_orc = oracle.select_cache(s.cpu().numpy().astype(np.float64), case.seg_start, case.seg_end, m)
+    assert np.array_equal(cp.keep.cpu().numpy()[:, :, :cp.Mtot], keep_orc)
