@@ -29,16 +29,7 @@ namespace kvc {
 namespace {
 
 constexpr int kPlanThreads = 512;
-
-__device__ __forceinline__ int32_t phys_slot(const int32_t* bt_row, int slot, int P, int num_pages,
-                                             unsigned* status) {
-  const int32_t page = __ldg(bt_row + slot / P);
-  if (page < 0 || page >= num_pages) {
-    atomicOr(status, KVC_DEV_BAD_PAGE);
-    return -1;
-  }
-  return page * P + slot % P;
-}
+constexpr int kEmitWords = 4;  // plan: bitmap words a warp emits at once
 
 // Block-wide exclusive prefix sum of one value per thread (kPlanThreads threads);
 // returns the exclusive prefix and writes the block total to *total.
@@ -81,6 +72,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   extern __shared__ uint32_t bitmap[];  // meta.words words
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t sh_total;
+  __shared__ uint32_t word_holes[kPlanThreads], word_first[kPlanThreads];
   const int64_t item = blockIdx.x;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
@@ -123,6 +115,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   const int words = (XP + 31) >> 5;
   for (int w = tid; w < words; w += kPlanThreads) bitmap[w] = 0u;
   __syncthreads();
+#pragma unroll 4
   for (int i = c_out + tid; i < m; i += kPlanThreads) {
     const int32_t pos = __ldg(ku + i);
     const int rel = pos - Bs;
@@ -134,9 +127,14 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
   __syncthreads();
 
-  // number the holes and emit moves / dead slots
+  // number the holes and emit moves / dead slots: kPlanThreads bitmap words at a
+  // time, a block scan numbers each word's first hole.  A full round of words
+  // keeps every thread busy on its own word's holes; a partial one (few words:
+  // most threads would idle) hands each word to a warp, lane b taking bit b, so
+  // a word's holes need one round of loads rather than one per hole
   const int32_t* bt_row = block_table + (int64_t)s.b * meta.max_blocks;
   const int ndead = XP - m;
+  const int lane = tid & 31, warp = tid >> 5;
   uint32_t base = 0;
   for (int w0 = 0; w0 < words; w0 += kPlanThreads) {
     const int w = w0 + tid;
@@ -148,26 +146,84 @@ __global__ void __launch_bounds__(kPlanThreads)
     }
     const uint32_t before = block_exclusive_scan(__popc(holes), warp_sums, &sh_total);
     const uint32_t total = sh_total;
-    uint32_t k = base + before;
-    while (holes != 0u) {
-      const int bit = __ffs(holes) - 1;
-      holes &= holes - 1u;
-      const int t = Bs + (w << 5) + bit;
-      if ((int)k < c_out + ndead) {
-        const int32_t dst = phys_slot(bt_row, s.s0 + t, P, meta.num_pages, status);
-        if ((int)k < c_out) {
-          const int32_t pos = __ldg(ku + k);
+    word_holes[tid] = holes;
+    word_first[tid] = base + before;
+    __syncthreads();
+    const int nw = min(kPlanThreads, words - w0);
+    if (nw == kPlanThreads) {  // a full round: every thread emits its own word's holes in turn
+      uint32_t k = base + before;
+      while (holes != 0u) {
+        const int bit = __ffs(holes) - 1;
+        holes &= holes - 1u;
+        if ((int)k < c_out + ndead) {
+          const int t = s.s0 + Bs + (w << 5) + bit;
+          const int32_t dpage = __ldg(bt_row + t / P);
+          int32_t dst = -1;
+          if (dpage < 0 || dpage >= meta.num_pages) atomicOr(status, KVC_DEV_BAD_PAGE);
+          else dst = dpage * P + t % P;
+          if ((int)k < c_out) {
+            const int32_t pos = __ldg(ku + k);
+            int32_t src = -1;
+            if (pos < 0 || pos >= s.n) {
+              atomicOr(status, KVC_DEV_BAD_KEEP);
+            } else {
+              const int32_t spage = __ldg(bt_row + (s.s0 + pos) / P);
+              if (spage < 0 || spage >= meta.num_pages) atomicOr(status, KVC_DEV_BAD_PAGE);
+              else src = spage * P + (s.s0 + pos) % P;
+            }
+            reinterpret_cast<int2*>(moves)[lh * meta.Mtot + s.moff + k] = make_int2(src, dst);
+          } else {
+            dead[u * P + (k - c_out)] = dst;
+          }
+        }
+        ++k;
+      }
+    }
+    // a partial round: each warp takes kEmitWords words at once, their loads issued together
+    for (int i0 = warp; nw < kPlanThreads && i0 < nw; i0 += kEmitWords * (kPlanThreads / 32)) {
+      int k[kEmitWords], t[kEmitWords], pos[kEmitWords];
+      int32_t dpage[kEmitWords], spage[kEmitWords];
+#pragma unroll
+      for (int q = 0; q < kEmitWords; ++q) {
+        const int i = i0 + q * (kPlanThreads / 32);
+        const uint32_t hw = i < nw ? word_holes[i] : 0u;
+        k[q] = -1;
+        if ((hw >> lane) & 1u) {
+          const int kk = (int)(word_first[i] + __popc(hw & ((1u << lane) - 1u)));
+          if (kk < c_out + ndead) k[q] = kk;
+        }
+        t[q] = s.s0 + Bs + ((w0 + i) << 5) + lane;
+        dpage[q] = k[q] >= 0 ? __ldg(bt_row + t[q] / P) : -1;
+        pos[q] = (k[q] >= 0 && k[q] < c_out) ? __ldg(ku + k[q]) : -1;
+      }
+#pragma unroll
+      for (int q = 0; q < kEmitWords; ++q) {
+        spage[q] = -1;
+        if (k[q] >= 0 && k[q] < c_out && pos[q] >= 0 && pos[q] < s.n) spage[q] = __ldg(bt_row + (s.s0 + pos[q]) / P);
+      }
+#pragma unroll
+      for (int q = 0; q < kEmitWords; ++q) {
+        if (k[q] < 0) continue;
+        int32_t dst = -1;
+        if (dpage[q] < 0 || dpage[q] >= meta.num_pages) atomicOr(status, KVC_DEV_BAD_PAGE);
+        else dst = dpage[q] * P + t[q] % P;
+        if (k[q] < c_out) {
           int32_t src = -1;
-          if (pos < 0 || pos >= s.n) atomicOr(status, KVC_DEV_BAD_KEEP);
-          else src = phys_slot(bt_row, s.s0 + pos, P, meta.num_pages, status);
-          reinterpret_cast<int2*>(moves)[lh * meta.Mtot + s.moff + k] = make_int2(src, dst);
+          if (pos[q] < 0 || pos[q] >= s.n) {
+            atomicOr(status, KVC_DEV_BAD_KEEP);
+          } else if (spage[q] < 0 || spage[q] >= meta.num_pages) {
+            atomicOr(status, KVC_DEV_BAD_PAGE);
+          } else {
+            src = spage[q] * P + (s.s0 + pos[q]) % P;
+          }
+          reinterpret_cast<int2*>(moves)[lh * meta.Mtot + s.moff + k[q]] = make_int2(src, dst);
         } else {
-          dead[u * P + (k - c_out)] = dst;
+          dead[u * P + (k[q] - c_out)] = dst;
         }
       }
-      ++k;
     }
     base += total;
+    __syncthreads();  // word_holes / word_first are rewritten by the next round
   }
 }
 
