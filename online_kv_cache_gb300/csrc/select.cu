@@ -59,6 +59,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
   __shared__ uint32_t pre_gt[kU * kWarps], pre_eq[kU * kWarps];
   __shared__ uint32_t sh_digit, sh_k, sh_tot_gt, sh_tot_eq, sh_above;
   __shared__ uint32_t sh_cnt[2];     // this CTA's elements > T and == T (read by the peers)
+  __shared__ uint32_t wsum[kWarps];  // per-warp totals of the digit search's scan
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = CS > 1 ? (int)cg::this_cluster().block_rank() : 0;
@@ -89,7 +90,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
     const uint32_t dmask = (1u << width) - 1u;
     const int nbins = 1 << width;
     uint32_t* wh = whist + warp * kWarpWords;
-    for (int i = lane; i < kWarpWords; i += 32) wh[i] = 0;
+    for (int i = lane; i < kWarpWords / 4; i += 32) reinterpret_cast<uint4*>(wh)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     // counting ignores order: 16-byte loads over the aligned body (kV in flight per
     // thread), single elements over the unaligned head and tail
@@ -124,46 +125,58 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
       }
     }
     __syncthreads();
-    for (int b = tid; b < nbins; b += kSelThreads) {
-      uint32_t c = 0;
+    // thread t owns the bpt bins (hi_b - bpt, hi_b], counted from the top: it merges
+    // them (over the warps, then over the cluster), and a block scan of the owners'
+    // sums in thread order finds the digit where the count from the top reaches k
+    const int bpt = nbins / kSelThreads;
+    const int hi_b = nbins - 1 - tid * bpt;
+    uint32_t own[kBins / kSelThreads];
+#pragma unroll
+    for (int j = 0; j < kBins / kSelThreads; ++j) {
+      own[j] = 0;
+      if (j < bpt) {
+        const int b = hi_b - j;
 #pragma unroll 4
-      for (int w = 0; w < kWarps; ++w) c += (whist[w * kWarpWords + (b >> 1)] >> ((b & 1) * 16)) & 0xFFFFu;
-      hist[b] = c;
+        for (int w = 0; w < kWarps; ++w) own[j] += (whist[w * kWarpWords + (b >> 1)] >> ((b & 1) * 16)) & 0xFFFFu;
+        hist[b] = own[j];
+      }
     }
     if constexpr (CS > 1) {
       cg::this_cluster().sync();  // every CTA's counts are in place
-      for (int b = tid; b < nbins; b += kSelThreads) {
-        uint32_t c = 0;
 #pragma unroll
-        for (int r = 0; r < CS; ++r) c += cg::this_cluster().map_shared_rank(hist, r)[b];
-        ghist[b] = c;
+      for (int j = 0; j < kBins / kSelThreads; ++j) {
+        if (j < bpt) {
+          uint32_t c = 0;
+#pragma unroll
+          for (int r = 0; r < CS; ++r) c += cg::this_cluster().map_shared_rank(hist, r)[hi_b - j];
+          ghist[hi_b - j] = c;
+          own[j] = c;
+        }
       }
     }
-    __syncthreads();
-    const uint32_t* H = CS > 1 ? ghist : hist;
-    if (warp == 0) {
-      // lane 0 owns the highest bins; find the digit where the count from the top reaches k
-      const int per = nbins / 32;
-      const int hi_b = nbins - 1 - lane * per;  // this lane covers digits (hi_b - per, hi_b]
-      uint32_t sum = 0;
-      for (int j = 0; j < per; ++j) sum += H[hi_b - j];
-      uint32_t incl = sum;
+    uint32_t sum = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < k && incl >= k) {
-        uint32_t acc = excl;
-        for (int j = 0; j < per; ++j) {
-          const uint32_t c = H[hi_b - j];
-          if (acc + c >= k) {
+    for (int j = 0; j < kBins / kSelThreads; ++j) sum += own[j];
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();  // also: every bin of hist (and ghist) is in place
+    uint32_t excl = incl - sum;
+    for (int w = 0; w < warp; ++w) excl += wsum[w];
+    if (excl < k && excl + sum >= k) {
+      uint32_t acc = excl;
+#pragma unroll
+      for (int j = 0; j < kBins / kSelThreads; ++j) {
+        if (j < bpt && acc < k) {
+          if (acc + own[j] >= k) {
             sh_digit = (uint32_t)(hi_b - j);
             sh_k = k - acc;
-            break;
           }
-          acc += c;
+          acc += own[j];
         }
       }
     }
