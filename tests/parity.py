@@ -1,7 +1,8 @@
 """Parity helpers shared by the GPU tests: run the CUDA path through the C ABI, run the oracle
 on host copies of the same seeded inputs, compare with the documented rules.
 
-Rules (spec tolerances, readings in the design doc):
+Rules (the stated tolerances of the hot path; the score bound comes from fp32 logits of bf16
+operands and fp32 exp/accumulation):
 * scores: |s_gpu - s_orc| <= 2e-3 * s_orc where s_orc >= 1e-30, else s_gpu <= 1e-27;
 * LSE: |lse_gpu - lse_orc| <= 1e-4 * max(1, |lse_orc|) (fp32 log-sum-exp of fp32 logits);
 * keep sets: identical except positions whose oracle score lies within 1e-4 relative of the
