@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kPlanThreads)
       }
     }
     base += total;
-    __syncthreads();  // word_holes / word_first are rewritten by the next round
+    __syncthreads();  // word_holes / word_first are rewritten for the next 512 words
   }
 }
 
