@@ -83,6 +83,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
 
   // ---- radix select of the m-th largest bit pattern (11, 11, 10 bits)
   uint32_t prefix = 0, pmask = 0, k = (uint32_t)m, my_gt = 0, my_eq = 0;
+  bool crowded = false;  // the previous pass's chosen bin held over a quarter of this slice
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
@@ -114,13 +115,37 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
         const int v = v0 + q * kSelThreads + tid;
         u[q] = (v < nv) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
       }
+      if (crowded) {
+        // most of the filtered elements share few digits (e.g. scores with a handful of
+        // values): one atomic adds the lanes that share the first hitting lane's digit
+        auto count_shared = [&](uint32_t x, bool ok) {
+          const bool hit = ok && (x & pmask) == prefix;
+          const uint32_t d = (x >> sh) & dmask;
+          const unsigned hits = __ballot_sync(0xffffffffu, hit);
+          if (hits == 0u) return;
+          const int src = __ffs(hits) - 1;
+          const uint32_t dl = __shfl_sync(0xffffffffu, d, src);
+          const unsigned same = __ballot_sync(0xffffffffu, hit && d == dl);
+          if (lane == src) atomicAdd(&wh[dl >> 1], (uint32_t)__popc(same) << ((dl & 1u) * 16));
+          if (hit && d != dl) atomicAdd(&wh[d >> 1], (d & 1u) ? 0x10000u : 1u);
+        };
 #pragma unroll
-      for (int q = 0; q < kV; ++q) {
-        if (v0 + q * kSelThreads + tid < nv) {
-          count(u[q].x);
-          count(u[q].y);
-          count(u[q].z);
-          count(u[q].w);
+        for (int q = 0; q < kV; ++q) {
+          const bool ok = v0 + q * kSelThreads + tid < nv;
+          count_shared(u[q].x, ok);
+          count_shared(u[q].y, ok);
+          count_shared(u[q].z, ok);
+          count_shared(u[q].w, ok);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kV; ++q) {
+          if (v0 + q * kSelThreads + tid < nv) {
+            count(u[q].x);
+            count(u[q].y);
+            count(u[q].z);
+            count(u[q].w);
+          }
         }
       }
     }
@@ -182,6 +207,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads)
     }
     __syncthreads();
     const uint32_t digit = sh_digit;
+    crowded = 4u * hist[digit] > (uint32_t)(hi - lo);  // block-uniform: every thread reads the same count
     if constexpr (CS > 1) {
       // this CTA's elements above the chosen digit are > T; at the last digit, == T
       uint32_t above = 0;
