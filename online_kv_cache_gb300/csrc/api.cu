@@ -899,7 +899,6 @@ kvc_status kvc_free_pages(const kvc_cache* cache, const kvc_segments* segs, cons
 namespace {
 
 constexpr int kSentinelChunkHost = 4096;   // positions per sentinel block (layout.cu)
-constexpr int kFreshMovesHost = 1024;      // survivors per fresh-plan block (layout.cu)
 
 bool fresh_active(const Seq& q) { return q.m < q.n; }
 
@@ -956,7 +955,7 @@ void fresh_metas(const kvc_cache* cache, const Plan& p, std::vector<LaunchMeta>*
         foff += q.nb;
       }
       a.seq[j].item0 = it;
-      it += LH * std::max<int64_t>(1, ceil_div(q.m, kFreshMovesHost));
+      it += LH * std::max<int64_t>(1, ceil_div(q.m, kFreshMovesPerBlock));
     }
     a.items = it;
     mv->push_back(a);

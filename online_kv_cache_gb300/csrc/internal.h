@@ -138,6 +138,10 @@ struct LrfuLaunch {
 // tail positions, 510 * 128 + 6 = 65286 for n = 2^20 - 4096.
 constexpr int kSelectMaxSegment = (1 << 20) - 4096;
 
+// Survivors per block of the fresh-page move kernel (the host sizes its grid
+// with the same count).
+constexpr int kFreshMovesPerBlock = 1024;
+
 // Longest segment the LRFU kernel takes: its per-warp 16-bit mass parts stay
 // below 2^32 for up to 2^16 elements per warp (16 warps).
 constexpr int kLrfuMaxSegment = 1 << 20;

@@ -32,7 +32,6 @@ constexpr int kRowSplit = 8;      // CTAs per sequence for block-table rows (ind
 
 
 constexpr int kSentinelChunk = 4096;       // positions per sentinel block
-constexpr int kFreshMovesPerBlock = 1024;  // moves per fresh-plan block
 constexpr uint32_t kSentinelPair = 0xC61CC61Cu;  // two bf16(-10^4) (= -9984)
 
 // First index r in the ascending list a[0..n) with a[r] >= x.
