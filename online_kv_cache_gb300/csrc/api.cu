@@ -272,8 +272,8 @@ ScoreGeom score_geom(int R, int d) {
   g.nchunks = (int)ceil_div(R32, 256);
   g.W = (int)ceil_div(ceil_div(R, g.nchunks), 32) * 32;
   g.R_pad = g.W * g.nchunks;
-  g.rowtiles = (int)ceil_div(R, 128);
-  const int tile_bytes = 128 * d * 2;
+  g.rowtiles = (int)ceil_div(R, kScoreTile);
+  const int tile_bytes = kScoreTile * d * 2;
   const int fixed = score_smem_bytes(0, 0, d);
   g.gsub1 = std::min(4, g.rowtiles);
   g.ngroups1 = (int)ceil_div(g.rowtiles, g.gsub1);
@@ -281,7 +281,7 @@ ScoreGeom score_geom(int R, int d) {
   // group (4) when it has more than two, so the next item's Q is in shared memory
   // before this item's MMAs drain (measured: -3.6% on short items, -0.8% on long
   // ones, although fewer K stages remain), else two
-  g.qbytes1 = (g.gsub1 > 2 ? 4 : 2) * 128 * d * 2;
+  g.qbytes1 = (g.gsub1 > 2 ? 4 : 2) * kScoreTile * d * 2;
   g.kst1 = std::min(8, (kScoreSmemLimit - fixed - g.qbytes1) / tile_bytes);
   g.gsub2 = std::min(g.nchunks, std::max(1, 512 / g.W));
   g.ngroups2 = (int)ceil_div(g.nchunks, g.gsub2);
@@ -300,7 +300,7 @@ int tiles_per_item(const kvc_cache* c, const Plan& p, int ngroups, int num_sms) 
   for (int tpi = 2; tpi <= 48; ++tpi) {
     int64_t items = 0, max_tiles = 0;
     for (const Seq& q : p.seqs) {
-      const int64_t T = ceil_div(q.n, 128);
+      const int64_t T = ceil_div(q.n, kScoreTile);
       const int64_t split = std::min<int64_t>(T, ceil_div(T, tpi));
       items += LHg * split;
       max_tiles = std::max<int64_t>(max_tiles, ceil_div(T, split));
@@ -351,7 +351,7 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
     for (size_t i = lo; i < hi; ++i) {
       const size_t j = i - lo;
       for (LaunchMeta* lm : {&a, &k, &z}) fill_seq(&lm->seq[j], p, i);
-      const int T = (int)ceil_div(p.seqs[i].n, 128);
+      const int T = (int)ceil_div(p.seqs[i].n, kScoreTile);
       const int split1 = (int)std::min<int64_t>(T, ceil_div(T, tpi1));
       const int split2 = (int)std::min<int64_t>(T, ceil_div(T, tpi2));
       a.seq[j].split = split1;
@@ -373,7 +373,7 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
     sp->comb.push_back(k);
     sp->p2.push_back(z);
   }
-  sp->part_bytes = (size_t)max_p1 * 2 * 4 * 128 * sizeof(float2);
+  sp->part_bytes = (size_t)max_p1 * 2 * 4 * kScoreTile * sizeof(float2);
   sp->obias_bytes = (size_t)c->batch * LH * g.R_pad * sizeof(float);
   sp->part2_bytes = g.ngroups2 > 1 ? (size_t)g.ngroups2 * LH * p.Ntot * sizeof(float) : 0;
 }
@@ -525,7 +525,7 @@ kvc_status score_common(const char* where, unsigned phases, float pw, const kvc_
   if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
   CUtensorMap tmK, tmQ1, tmQ2;
   if ((st = make_kmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
-  if ((st = make_tmap(&tmQ1, q, qrows, cache->head_dim, 128)) != KVC_OK) return st;
+  if ((st = make_tmap(&tmQ1, q, qrows, cache->head_dim, kScoreTile)) != KVC_OK) return st;
   if ((st = make_tmap(&tmQ2, q, qrows, cache->head_dim, g.W)) != KVC_OK) return st;
 
   ScoreLaunch sl;

@@ -14,6 +14,10 @@ namespace kvc {
 
 constexpr int kMaxSeqPerLaunch = 128;
 
+// Keys per K tile and rows per Q row tile of the scoring passes, as the host
+// sizes their work split, workspaces and tensor-map boxes (score.cu's kTile).
+constexpr int kScoreTile = 128;
+
 struct SeqMeta {
   int32_t b;      // sequence index (block-table row)
   int32_t s0;     // first slot of the segment
