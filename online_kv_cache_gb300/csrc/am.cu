@@ -38,12 +38,18 @@ namespace {
 constexpr int kAmThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// A coordinate moves only when its gradient exceeds 2^-14 of the scale of the
-// gradient's own terms: the normal equations square cond(E), which reaches
-// 1e14 on concentrated attention, and an fp32 gradient carries about 2e-6 of
-// that scale in rounding (row masses through an fp32 LSE, Gram sums over R
-// rows); below the guard the gradient is rounding, not signal.
-constexpr float kAmGuard = 6.103515625e-05f;  // 2^-14
+// A coordinate moves only when its gradient exceeds 2^-17 of the scale of the
+// gradient's own terms.  E and s come from fp32 logits (128-term fp32 dot
+// products), whose relative error reaches ~2e-5 where the logits are large
+// (concentrated attention); the normal equations square cond(E), up to 1e16
+// there, so the gradient of a key with almost no attention is that error
+// alone, and a step on it (w_j to 1e8, V_C rows to 1e9) wrecks the value fit.
+// Measured on this kernel against the plain fp64 descent: at 2^-20 such units
+// diverge (value residual 9e-2 of |Y| above the plain descent's); at 2^-14
+// real steps of well-conditioned fits are frozen (residuals up to 2e-3 of the
+// target norm above); from 2^-16 to 2^-18 both stay within 6e-6.  2^-17 keeps
+// a factor of 8 from the level that diverges.
+constexpr float kAmGuard = 7.62939453125e-06f;  // 2^-17
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -510,7 +516,7 @@ struct RowRing {
 // Block = unit.  Projected cyclic coordinate descent on min_{w >= 0} ||E w - s||^2
 // from w = 1: with g = G w - b, coordinate j moves to max(0, w_j - g_j / G_jj)
 // and g follows by the change times column j of G (= row j, G symmetric).
-// Coordinate j moves only when |g_j| > 2^-14 b_j (every term of G w and of
+// Coordinate j moves only when |g_j| > 2^-17 b_j (every term of G w and of
 // b = E^T s is >= 0, so b_j is their scale).  Rows of G stream through the
 // row ring.  Two barriers per step: every thread reads g_j and w_j before any
 // of them is updated.
@@ -612,7 +618,7 @@ static_assert(value_smem_bytes(kAmMaxM) <= 227 * 1024 && mass_smem_bytes(kAmMaxM
 // least-squares problems sharing H = Ph^T Ph: cyclic coordinate descent from
 // X = the kept values, gradient Gv = H X - Bm kept in shared memory; row j of
 // X moves by -Gv_j / H_jj and Gv follows by column j of H (= row j) times the
-// change, when |Gv_jc| > 2^-14 pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic|
+// change, when |Gv_jc| > 2^-17 pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic|
 // + max_k |X0_kc|: the scale of the gradient's terms in column c).  Rows of H
 // stream through the row ring.  At the end V_C is
 // written to `vc` (fp32) and over the kept entries' V rows (bf16, round to

@@ -5,14 +5,29 @@ Source: "Practical Online KV Cache Compaction for LLM Agents: An Empirical Study
 tutorial page), section on the two compaction families: min ||exp(Q K_C^T + beta) 1_m -
 exp(Q K^T) 1_n||^2 and min ||A_hat(Q; K_C, beta, V_C) - A(Q; K, V)||_F^2.
 
-The fits are ill-conditioned (exp of logits: cond(E) reaches 1e14 on these inputs), so their
-minimisers are not unique to fp32 and the individual beta_j and V_C rows are not compared.  What
-is compared is unique: the residual norms the fits reach after the same sweeps, each evaluated in
-fp64 by the oracle on its own problem (E, s, Y) at the GPU's outputs, against the oracle's own
-fit.  Tolerance: the GPU forms E, the Gram matrices and the descent in fp32 (unit roundoff
-2^-24 ~ 6e-8); the logit error of an fp32 dot product over d = 128 bf16 products and the Gram
-sums over R rows put the residual's floor near 1e-6 of the target norm (an fp32 re-run of the
-same steps on the CPU lands within 6e-7 of the fp64 residuals); the bound is 3e-5 of it.
+What is compared depends on how well the unit's problem is conditioned:
+
+* Well-conditioned units (cond(E) <= 1e8: diffuse or aligned proxy queries): the residual norm
+  each fit reaches after the same sweeps, evaluated in fp64 by the oracle on its own problem
+  (E, s, Y) at the GPU's outputs, must equal the oracle's own to RES_TOL = 1e-5 of the target
+  norm (mass: |s|; value: |Y|).  Derivation: the GPU forms E and s from fp32 logits (128-term
+  fp32 dot products: relative error ~1e-6 on diffuse rows), the Gram matrices over R rows and
+  the descent in fp32, and freezes coordinates whose gradient is below 2^-17 of its terms'
+  scale; on every unit of these cases and of the multi-turn shape's three query recipes the
+  measured gap is at most 5.4e-6; the bound leaves a factor of ~2.
+  Where R > m and the fit is small, w and V_C themselves are compared element by element:
+  |w_gpu - w_orc| <= W_TOL max(1, |w_orc|) and |V_gpu - V_orc| <= VC_TOL max |V_orc| (measured
+  3.4e-5 and 1.2e-4; the bounds are 2e-4 and 5e-4).  On the multi-turn shape (m = 307 keys,
+  8 sweeps, far from converged) the same rounding moves individual entries by up to a few
+  percent while the residuals agree, so there only the residuals are compared.
+* Concentrated units (cond(E) > 1e8, up to 1e18 with planted proxy queries): the gradient of a
+  key with almost no attention is rounding in any precision, and the plain fp64 descent itself
+  takes steps of that size (w_j to 1e3), after which its value residual can stand above token
+  eviction's.  Neither side's value fit is unique there.  The mass residual is still compared
+  two-sided at RES_TOL; the GPU's value residual must not exceed the oracle's by more than
+  RES_TOL (it may be lower).  Without the kernel's rounding guard an fp32 descent diverges on
+  these units (value residual 1e-2 of |Y| above the oracle's), which this check catches.
+
 The keep sets come from the oracle's own token-eviction scores, and every value the tests
 expect comes from the oracle.
 """
@@ -28,7 +43,10 @@ from tests import parity as PT
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-RES_TOL = 3e-5
+RES_TOL = 1e-5
+W_TOL = 2e-4
+VC_TOL = 5e-4
+COND_WELL = 1e8
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -61,31 +79,49 @@ def run_gpu(case, m, keep_np, sweeps, aux):
     return beta.cpu().numpy().astype(np.float64), vc.cpu().numpy().astype(np.float64)
 
 
-def check_units(units, m, beta, vc, sweeps, sample=None):
-    """Residuals of both fits at the GPU's outputs against the oracle's, per unit."""
+def check_units(units, m, beta, vc, sweeps, sample=None, elementwise=False):
+    """Residuals of both fits at the GPU's outputs against the oracle's, per unit (two-sided on
+    well-conditioned units, one-sided for the value fit on concentrated ones); w and V_C element
+    by element when asked."""
     moff = np.concatenate([[0], np.cumsum(m)])
-    worst = [0.0, 0.0]
+    worst = {"mass": 0.0, "value": 0.0, "value_excess": 0.0, "w": 0.0, "vc": 0.0}
+    kinds = {"well": 0, "concentrated": 0}
     keys = sorted(units) if sample is None else sample
     for (b, l, h) in keys:
         u = units[(b, l, h)]
         sl = slice(moff[b], moff[b + 1])
         bg = beta[l, h, sl]
         assert not np.any(np.isnan(bg)) and not np.any(bg == np.inf)
+        assert np.all(np.isfinite(vc[l, h, sl]))
         wg = np.exp(bg)  # exp(-inf) = 0: a masked key
+        well = u["E"].shape[1] == 0 or np.linalg.cond(u["E"]) <= COND_WELL
+        kinds["well" if well else "concentrated"] += 1
         s_norm = np.linalg.norm(u["s"])
         r_gpu = np.sqrt(am.mass_objective(u["E"], u["s"], wg))
         r_orc = np.sqrt(am.mass_objective(u["E"], u["s"], u["w"]))
-        r_te = np.sqrt(am.mass_objective(u["E"], u["s"], np.ones_like(wg)))
         dm = abs(r_gpu - r_orc) / s_norm
         assert dm <= RES_TOL, f"unit {(b, l, h)}: mass residual {r_gpu:.4e} vs oracle {r_orc:.4e} (|s| {s_norm:.3e})"
-        assert r_gpu <= r_te + RES_TOL * s_norm  # never worse than token eviction's beta = 0
         y_norm = np.linalg.norm(u["Y"])
         v_gpu = np.sqrt(am.value_objective(u["E"], u["Y"], wg, vc[l, h, sl]))
         v_orc = np.sqrt(am.value_objective(u["E"], u["Y"], u["w"], u["vc"]))
-        dv = abs(v_gpu - v_orc) / y_norm
-        assert dv <= RES_TOL, f"unit {(b, l, h)}: value residual {v_gpu:.4e} vs oracle {v_orc:.4e} (|Y| {y_norm:.3e})"
-        worst = [max(worst[0], dm), max(worst[1], dv)]
-    print(f"sweeps={sweeps}: worst mass / value residual gap {worst[0]:.2e} / {worst[1]:.2e} of the target norm")
+        if well:
+            dv = abs(v_gpu - v_orc) / y_norm
+            assert dv <= RES_TOL, f"unit {(b, l, h)}: value residual {v_gpu:.4e} vs oracle {v_orc:.4e} (|Y| {y_norm:.3e})"
+            worst["value"] = max(worst["value"], dv)
+        else:
+            ex = (v_gpu - v_orc) / y_norm
+            assert ex <= RES_TOL, f"unit {(b, l, h)}: value residual {v_gpu:.4e} above the oracle's {v_orc:.4e} (|Y| {y_norm:.3e})"
+            worst["value_excess"] = max(worst["value_excess"], ex)
+        worst["mass"] = max(worst["mass"], dm)
+        if elementwise and u["E"].shape[1] > 0:
+            assert well
+            ew = np.max(np.abs(wg - u["w"]) / np.maximum(1.0, np.abs(u["w"])))
+            ev = np.max(np.abs(vc[l, h, sl] - u["vc"])) / np.abs(u["vc"]).max()
+            assert ew <= W_TOL, f"unit {(b, l, h)}: w differs by {ew:.3e} of max(1, |w|)"
+            assert ev <= VC_TOL, f"unit {(b, l, h)}: V_C differs by {ev:.3e} of max |V_C|"
+            worst["w"], worst["vc"] = max(worst["w"], ew), max(worst["vc"], ev)
+    print(f"sweeps={sweeps} units {kinds}: worst gaps " + ", ".join(f"{k} {v:.2e}" for k, v in worst.items()))
+    return kinds
 
 
 def check_writes(case, m, keep_np, beta, vc, before_v, before_k, before_aux, aux):
@@ -115,13 +151,14 @@ def check_writes(case, m, keep_np, beta, vc, before_v, before_k, before_aux, aux
     assert np.array_equal(got_aux[fin], want_aux[fin].astype(np.float32))
 
 
-@pytest.mark.parametrize("d,P,G,q,lengths,ratio,sweeps,qdist", [
-    (128, 16, 4, 8, (300, 129), 0.2, 8, "planted4"),   # R = 32 < m, concentrated attention
-    (128, 16, 4, 8, (300, 129), 0.2, 8, "normal"),     # diffuse attention: the fits do real work
-    (64, 32, 2, 40, (200, 65, 1), 0.2, 8, "normal"),   # R = 80 > m, a one-key unit
-    (128, 16, 8, 16, (700,), 0.1, 3, "planted4"),      # R = 128 > m = 70, two key tiles of rows
+@pytest.mark.parametrize("d,P,G,q,lengths,ratio,sweeps,qdist,elementwise", [
+    (128, 16, 4, 8, (300, 129), 0.2, 8, "planted4", False),  # R = 32 < m, concentrated (cond(E) ~1e15)
+    (128, 16, 4, 8, (300, 129), 0.2, 8, "normal", False),    # diffuse attention, m > R: many minimisers
+    (64, 32, 2, 40, (200, 65, 1), 0.2, 8, "normal", True),   # R = 80 > m, a one-key unit: w, V_C compared
+    (64, 16, 4, 32, (160, 97), 0.2, 8, "normal", True),      # R = 128 > m, two sequences
+    (128, 16, 8, 16, (700,), 0.1, 3, "aligned", False),      # Q-aligned heavy hitters, two key tiles of rows
 ])
-def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist):
+def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist, elementwise):
     sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, shuffle_pages=True,
                           qdist=qdist)
     case = workloads.build(sp, 5, DEV)
@@ -134,7 +171,11 @@ def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist):
     beta, vc = run_gpu(case, m, keep_np, sweeps, aux)
     _, _, units = am.cache(kb, vb, qb, case.block_table.cpu().numpy(), case.seg_start, case.seg_end, keep_np, m,
                            sp.scale, sweeps)
-    check_units(units, m, beta, vc, sweeps)
+    kinds = check_units(units, m, beta, vc, sweeps, elementwise=elementwise)
+    if qdist == "planted4":
+        assert kinds["concentrated"] > 0  # the regime the guard is for
+    else:
+        assert kinds["concentrated"] == 0
     check_writes(case, m, keep_np, beta, vc, *before, aux)
 
 
@@ -169,12 +210,13 @@ def test_keep_all_reproduces_the_full_attention():
         assert np.sqrt(am.mass_objective(u["E"], u["s"], np.exp(beta[l, h]))) <= RES_TOL * np.linalg.norm(u["s"])
 
 
-@pytest.mark.parametrize("qdist", ["planted4", "normal"])
+@pytest.mark.parametrize("qdist", ["planted4", "normal", "aligned"])
 def test_am_multi_turn_shape_sampled(qdist):
     """The delay-1 multi-turn compaction shape (28 layers, 2 KV heads, 16 query heads x 128 rows:
     R = 2048 > m = 307), 8 sweeps, in the launch configuration the benchmark times; six units
-    sampled for the oracle.  With the planted proxy queries token eviction already holds the
-    mass (the fits stay at their start); with diffuse ones every coordinate moves."""
+    sampled for the oracle.  With the planted proxy queries token eviction already holds all
+    but ~1e-11 of the mass (concentrated units); with diffuse or Q-aligned ones every coordinate
+    moves (the aligned recipe is where a coarser rounding guard froze real steps)."""
     import dataclasses
     sp = dataclasses.replace(workloads.spec("multi-turn"), qdist=qdist)
     case = workloads.build(sp, 0, DEV)
@@ -192,4 +234,5 @@ def test_am_multi_turn_shape_sampled(qdist):
         K = am.gather(kb, bt, l, h, b, 0, sp.lengths[0])
         V = am.gather(vb, bt, l, h, b, 0, sp.lengths[0])
         units[(b, l, h)] = am.unit(am.bf16_to_f64(qb[b, l, h]), K, V, keep_np[l, h, :m[0]], sp.scale, 8)
-    check_units(units, m, beta, vc, 8, sample=sample)
+    kinds = check_units(units, m, beta, vc, 8, sample=sample)
+    assert kinds["concentrated" if qdist == "planted4" else "well"] == len(sample)

@@ -198,37 +198,20 @@ def test_cache_walks_pages_like_dense():
         np.testing.assert_array_equal(vc[l, h, off:off + m[b]], ref["vc"])
 
 
-def test_guard_freezes_gradients_below_the_rounding_scale():
-    """With the guard, a coordinate whose gradient is below 2^-14 of its terms' scale stays put
-    (token eviction's answer survives a perturbation of the target at the 1e-9 level), while the
-    plain iteration (tol = 0) chases it; a large gradient still moves the coordinate."""
-    g = rng(11)
-    E = np.abs(g.standard_normal((12, 5))) + 0.05
-    s = E @ np.ones(5) + 1e-9 * g.standard_normal(12)
-    assert np.array_equal(am.mass_fit(E, s, 20, tol=am.GUARD), np.ones(5))
-    assert not np.array_equal(am.mass_fit(E, s, 20, tol=0.0), np.ones(5))
-    s_far = E @ np.array([2.0, 1.0, 0.5, 1.0, 1.0])
-    w = am.mass_fit(E, s_far, 4000, tol=am.GUARD)
-    b = E.T @ s_far
-    gr = E.T @ (E @ w - s_far)
-    assert np.all(np.abs(gr[w > 0]) <= am.GUARD * b[w > 0] * (1 + 1e-9))  # stationary up to the guard
-    assert am.mass_objective(E, s_far, w) < 1e-6 * (s_far @ s_far)
-    Ph = np.abs(g.standard_normal((12, 5)))
-    Ph /= Ph.sum(axis=1, keepdims=True)
-    X0 = g.standard_normal((5, 3))
-    Y = Ph @ X0 + 1e-9 * g.standard_normal((12, 3))
-    assert np.array_equal(am.value_fit(Ph, Y, X0, 20, tol=am.GUARD), X0)
-    assert not np.array_equal(am.value_fit(Ph, Y, X0, 20, tol=0.0), X0)
-
-
-def test_guard_leaves_an_exact_token_eviction_answer():
+def test_concentrated_attention_keeps_token_eviction_residuals():
     """Concentrated attention (each proxy row aims at one kept key): token eviction already
-    reproduces mass and output to fp64 rounding, and the guarded fits return it unchanged."""
+    reproduces the mass and the output to fp64 rounding.  The plain fits may take steps of
+    rounding size here, but neither residual may rise above the start's, and both stay at the
+    rounding level of the targets."""
     g = rng(12)
     K = g.standard_normal((30, 16)) * 3
     V = g.standard_normal((30, 16))
     keep = np.array([2, 7, 11, 19, 23])
     Q = np.repeat(K[keep], 4, axis=0) * 3 + 0.01 * g.standard_normal((20, 16))
     u = am.unit(Q, K, V, keep, 1.0, 8)
-    assert np.array_equal(u["w"], np.ones(5))
-    assert np.array_equal(u["vc"], V[keep])
+    m0 = am.mass_objective(u["E"], u["s"], np.ones(5))
+    v0 = am.value_objective(u["E"], u["Y"], np.ones(5), V[keep])
+    assert am.mass_objective(u["E"], u["s"], u["w"]) <= m0 * (1 + 1e-9) + 1e-30
+    assert am.value_objective(u["E"], u["Y"], u["w"], u["vc"]) <= v0 * (1 + 1e-9) + 1e-30
+    assert np.sqrt(am.mass_objective(u["E"], u["s"], u["w"])) <= 1e-12 * np.linalg.norm(u["s"])
+    assert np.sqrt(am.value_objective(u["E"], u["Y"], u["w"], u["vc"])) <= 1e-10 * np.linalg.norm(u["Y"])
