@@ -33,6 +33,11 @@
  *   Ownership: the caller owns every buffer; the library allocates no device
  *     or pinned memory and keeps no state across calls except the device
  *     status word (kvc_read_device_status) and cached TMA descriptors.
+ *   Device reset: the device addresses of the library's own device arrays
+ *     (the status word, the kvc_score_noalloc scratch) are looked up once per
+ *     device and kept for the life of the process, so resetting a device
+ *     (cudaDeviceReset) while the library is loaded is not supported: a call
+ *     made after a reset may use a stale address.  Restart the process instead.
  *   Pointers: device pointers unless marked "host".  k_pool, v_pool, q and
  *     workspaces must be 16-byte aligned.
  *   Streams: every call is asynchronous on `stream` (0 = legacy default
@@ -232,7 +237,9 @@ kvc_status kvc_score_alpha(const kvc_cache *cache, const kvc_segments *segs, con
  *     process exits.  A call whose workspace (kvc_score_workspace_size) is
  *     larger returns KVC_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current) and keeps it for the life of the process; make
+ *     that first call before any stream capture.  A device reset while the
+ *     library is loaded is not supported (see "Device reset" above).
  *   - All calls on a device share its array, which keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     may overlap on the GPU (issued on different streams) race on the array:
@@ -429,6 +436,23 @@ uint64_t kvc_launch_count(int32_t reset);
 
 /* Library version string. */
 const char *kvc_version(void);
+
+/* Test support for failure detection; the pages have no counterpart.  Every
+ * wait between the roles of a scoring kernel (producer, MMA issuer, epilogue)
+ * is bounded: when one runs out the kernel records KVC_DEV_WAIT_TIMEOUT in
+ * the device status word, waits (up to 2 s each) for the copies and MMAs it
+ * has already issued, frees its tensor memory and returns, leaving the
+ * context usable.  This call lets a test drive that path without faulting
+ * anything: with stall_ns > 0, the scoring launches made afterwards
+ * (kvc_score, kvc_score_lse, kvc_score_alpha, kvc_score_action,
+ * kvc_score_noalloc) issue no proxy-row load and limit each wait between the
+ * roles to stall_ns nanoseconds, so the MMA issuer's first wait can only run
+ * out.  Such a call still returns KVC_OK (KVC_ERR_DEVICE_CHECK in checked
+ * mode) and its outputs are undefined.  stall_ns = 0 restores normal
+ * operation.  Process-wide, read when a call is made (a launch captured in a
+ * CUDA graph keeps the value it was captured with).  Returns
+ * KVC_ERR_INVALID_ARG unless 0 <= stall_ns <= 1e10. */
+kvc_status kvc_debug_stall_scoring(int64_t stall_ns);
 
 #ifdef __cplusplus
 }

@@ -46,7 +46,7 @@ EXPORTED = (
     "kvc_read_device_status", "kvc_validate_cache_host", "kvc_version", "kvc_score_lse",
     "kvc_score_alpha", "kvc_launch_count", "kvc_score_noalloc", "kvc_evict_sentinel",
     "kvc_plan_fresh_buffer_sizes", "kvc_plan_fresh", "kvc_commit_fresh", "kvc_score_action",
-    "kvc_lrfu_update", "kvc_am_workspace_size", "kvc_am_fit",
+    "kvc_lrfu_update", "kvc_am_workspace_size", "kvc_am_fit", "kvc_debug_stall_scoring",
 )
 
 
@@ -144,6 +144,7 @@ def lib():
             "kvc_lrfu_update": (I32, [C, SG, P, F, F, P, P, P]),
             "kvc_am_workspace_size": (I32, [C, SG, P, I32, ctypes.POINTER(S)]),
             "kvc_am_fit": (I32, [C, SG, P, P, I32, F, P, I32, P, P, P, S, P]),
+            "kvc_debug_stall_scoring": (I32, [I64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -287,6 +288,13 @@ def kvc_score_noalloc(cache: Cache, segs: Segments, q: torch.Tensor, R: int, sca
 
 def kvc_launch_count(reset: bool = False) -> int:
     return int(lib().kvc_launch_count(1 if reset else 0))
+
+
+def kvc_debug_stall_scoring(stall_ns: int) -> None:
+    """Failure-path test of the scoring kernels: stall_ns > 0 makes the scoring launches that follow
+    withhold their proxy-row loads and give up their waits after stall_ns (KVC_DEV_WAIT_TIMEOUT);
+    0 restores normal operation."""
+    _check(lib().kvc_debug_stall_scoring(int(stall_ns)), "kvc_debug_stall_scoring")
 
 
 def kvc_select_workspace_size(cache: Cache, segs: Segments, m) -> int:

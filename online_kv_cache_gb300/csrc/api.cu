@@ -315,6 +315,10 @@ int tiles_per_item(const kvc_cache* c, const Plan& p, int ngroups, int num_sms) 
   return best_tpi;
 }
 
+// Failure-path test of the scoring kernels: > 0 withholds their proxy-row
+// loads and limits the waits between their roles (kvc_debug_stall_scoring).
+std::atomic<int64_t> g_stall_ns{0};
+
 struct ScorePlan {
   std::vector<LaunchMeta> p1, comb, p2;
   size_t part_bytes = 0, obias_bytes = 0, part2_bytes = 0;
@@ -337,6 +341,7 @@ void build_score_plan(const kvc_cache* c, const Plan& p, const ScoreGeom& g, flo
       lm->rowtiles = g.rowtiles;
       lm->scale = scale;
       lm->pw = pw;
+      lm->stall_ns = g_stall_ns.load(std::memory_order_relaxed);
     }
     a.ngroups = g.ngroups1;
     a.gsub = g.gsub1;
@@ -648,6 +653,14 @@ kvc_status kvc_score_noalloc(const kvc_cache* cache, const kvc_segments* segs, c
 
 uint64_t kvc_launch_count(int32_t reset) {
   return reset ? g_launches.exchange(0) : g_launches.load();
+}
+
+kvc_status kvc_debug_stall_scoring(int64_t stall_ns) {
+  if (stall_ns < 0 || stall_ns > 10000000000ll)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_debug_stall_scoring: stall_ns must be in [0, 1e10], got %lld",
+                (long long)stall_ns);
+  g_stall_ns.store(stall_ns, std::memory_order_relaxed);
+  return KVC_OK;
 }
 
 kvc_status kvc_select_workspace_size(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m,

@@ -55,6 +55,8 @@ struct LaunchMeta {
   int64_t Ntot, Mtot, Ftot;
   int64_t Xtot;     // fresh-page compaction: pages popped by the whole call
   int64_t items;    // work items of this launch
+  int64_t stall_ns; // scoring passes, failure-path test only: > 0 withholds the proxy-row loads
+                    // and limits every wait between the kernel's roles to stall_ns (0: normal)
   SeqMeta seq[kMaxSeqPerLaunch];
 };
 

@@ -63,17 +63,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (and raises the CTA's abort flag) if the CTA was aborted by another
-// role or if the wait exceeded kWaitLimitNs (then the device status word gets
+// role or if the wait exceeded limit_ns (then the device status word gets
 // KVC_DEV_WAIT_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* status) {
+                                          unsigned int* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicOr(status, KVC_DEV_WAIT_TIMEOUT);
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;

@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* red_empty = red_full + 2;    // [2] pass 2: `red` may be written again
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 384);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // limit of every wait between the roles (the abort drains keep the default)
+  const unsigned long long wait_ns = meta.stall_ns > 0 ? (unsigned long long)meta.stall_ns : kWaitLimitNs;
   float* red = reinterpret_cast<float*>(smem_raw + 512);           // [2 parity][128] (pass 2)
   int32_t* page_ring = reinterpret_cast<int32_t*>(smem_raw + 1536);  // [kPageRing][16]
 
@@ -301,16 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item qi = decode_item(meta, q_item, total_sub);
         const int qrow = ((qi.u.b * meta.L + qi.u.l) * meta.H + qi.u.h) * meta.R +
                          qi.u.g * meta.gsub * sub_rows;
-        for (int j = 0; j < qi.J && ok; ++j) {
+        // stall_ns > 0 (failure-path test): no proxy-row load is issued, so the
+        // MMA role's wait for them can only run out
+        for (int j = 0; j < qi.J && ok && meta.stall_ns == 0; ++j) {
           // pass 1: staging buffer qc % 2; pass 2: the group's own sub-tile slot j
           const int qs = (PASS == 1) ? (int)(qc & (qst - 1)) : j;
           const uint32_t qpar = (PASS == 1) ? ((qc >> qsh) & 1) : (q_use[j] & 1);
           if (lane == 0) {
-            ok = mbar_wait(&q_empty[qs], qpar ^ 1, abort_flag, status);
+            ok = mbar_wait(&q_empty[qs], qpar ^ 1, abort_flag, status, wait_ns);
             if (ok) mbar_arrive_expect_tx(&q_full[qs], sub_bytes);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (ok && lane < C::KB)  // lane kb: k-block kb of the sub-tile
+          if (!ok) break;  // only issued loads are counted: the abort drain waits for them
+          if (lane < C::KB)  // lane kb: k-block kb of the sub-tile
             tma_load_2d(sQ + (qs * C::KB + lane) * sub_rows * 128, &tmQ, &q_full[qs], lane * 64,
                         qrow + j * sub_rows);
           ++q_use[j];
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       const int ks = pks;
-      if (lane == 0) ok = mbar_wait(&k_empty[ks], pkph ^ 1u, abort_flag, status);
+      if (lane == 0) ok = mbar_wait(&k_empty[ks], pkph ^ 1u, abort_flag, status, wait_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const unsigned valid = __ballot_sync(0xffffffffu, prow >= 0);
@@ -358,7 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait_all();  // no page copy outlives the CTA
-    if (!ok && lane == 0) {  // let issued copies land before the CTA exits
+    // Let the last copies issued land before the CTA exits, whether this role
+    // or another gave up (in a normal run they have landed or are about to:
+    // completion does not depend on any consumer).
+    if (lane == 0) {
       for (uint32_t j = (kcount > (uint32_t)kst ? kcount - kst : 0); j < kcount; ++j)
         mbar_wait(&k_full[j % kst], (j / kst) & 1, nullptr, status);
       if (PASS == 1) {
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the previous item's MMAs read the TMEM copy of Q: let them finish
           if (issued) {
             mma_commit(drain);
-            if (!(ok = mbar_wait(drain, dc & 1, abort_flag, status))) break;
+            if (!(ok = mbar_wait(drain, dc & 1, abort_flag, status, wait_ns))) break;
             ++dc;
             tc_fence_after_sync();
           }
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // measured slower: a copy then waits behind the epilogue's slot release.)
           for (int j = 0; j < it.J && ok; ++j) {
             const uint32_t qs = qc & (qst - 1);
-            if (!(ok = mbar_wait(&q_full[qs], (qc >> qsh) & 1, abort_flag, status))) break;
+            if (!(ok = mbar_wait(&q_full[qs], (qc >> qsh) & 1, abort_flag, status, wait_ns))) break;
             const uint64_t stage = q_desc + ((qs * sub_bytes) >> 4);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
@@ -411,14 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qc;
           }
         } else {
-          for (int j = 0; j < it.J && ok; ++j) ok = mbar_wait(&q_full[j], q_use[j] & 1, abort_flag, status);
+          for (int j = 0; j < it.J && ok; ++j) ok = mbar_wait(&q_full[j], q_use[j] & 1, abort_flag, status, wait_ns);
         }
         if (!ok) break;
         for (int t = it.t0; t < it.t1 && ok; ++t) {
-          if (!(ok = mbar_wait(&k_full[ks], kph, abort_flag, status))) break;
+          if (!(ok = mbar_wait(&k_full[ks], kph, abort_flag, status, wait_ns))) break;
           const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + ks * C::kTileBytes), C::kKGroup);
           for (int j = 0; j < it.J; ++j) {
-            if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status))) break;
+            if (!(ok = mbar_wait(&t_empty[slot], (use & 1) ^ 1, abort_flag, status, wait_ns))) break;
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem + slot * slot_cols;
             if (PASS == 1) {
@@ -486,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  use += (slot == 0)) {
           if ((int)(jc & 1) != wg) continue;
           mine = true;
-          ok = mbar_wait(&t_full[slot], use & 1, abort_flag, status);
+          ok = mbar_wait(&t_full[slot], use & 1, abort_flag, status, wait_ns);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -557,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* rb = red + par * kTile;
             writer = (wg == (int)((jc - 1) & 1));
             if (!writer) {
-              ok = mbar_wait(&red_empty[par], (use & 1) ^ 1, abort_flag, status);
+              ok = mbar_wait(&red_empty[par], (use & 1) ^ 1, abort_flag, status, wait_ns);
               if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&red_full[par]);
             } else {
-              ok = mbar_wait(&red_full[par], use & 1, abort_flag, status);
+              ok = mbar_wait(&red_full[par], use & 1, abort_flag, status, wait_ns);
               if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
