@@ -29,15 +29,24 @@ def built():
     kvc.kvc_read_device_status(clear=True)
 
 
+# Units compared with the oracle at full size, beyond every unit of one seeded layer.  The
+# Qwen3-shaped cache gets the most: its attention sinks make the selection band tightest there.
+EXTRA_UNITS = {"qwen3-30b-a3b": 32, "batched-ragged": 16, "batched-ragged-sinks": 16, "long-context": 16}
+
+
 def sample_units(case, k, seed):
-    """k (b, l, h) units: the first, the last and seeded random ones (active sequences only)."""
+    """Every (b, l, h) unit of one seeded layer, plus k more seeded units (the first and the last
+    unit of the cache among them); active sequences only."""
     sp = case.spec
     active = [b for b in range(sp.B) if case.seg_end[b] > case.seg_start[b]]
     rng = np.random.default_rng(seed)
-    units = {(active[0], 0, 0), (active[-1], sp.L - 1, sp.H - 1)}
-    while len(units) < k:
-        units.add((int(rng.choice(active)), int(rng.integers(sp.L)), int(rng.integers(sp.H))))
-    return sorted(units)
+    layer = int(rng.integers(sp.L))
+    units = {(b, layer, h) for b in active for h in range(sp.H)}
+    extra = {(active[0], 0, 0), (active[-1], sp.L - 1, sp.H - 1)}
+    total = min(len(units) + k, len(active) * sp.L * sp.H)
+    while len(extra - units) < k and len(units | extra) < total:
+        extra.add((int(rng.choice(active)), int(rng.integers(sp.L)), int(rng.integers(sp.H))))
+    return sorted(units | extra)
 
 
 def check_live_tags(case, m, keep_gpu):
@@ -59,7 +68,7 @@ def check_live_tags(case, m, keep_gpu):
         assert torch.equal(live, want), f"sequence {b}: live tags differ from the keep set"
 
 
-@pytest.mark.parametrize("name", ["qwen3-30b-a3b", "batched-ragged", "long-context"])
+@pytest.mark.parametrize("name", ["qwen3-30b-a3b", "batched-ragged", "batched-ragged-sinks", "long-context"])
 def test_full_size(name):
     sp = workloads.spec(name, 0)
     case = workloads.build(sp, 0, DEV)
@@ -95,9 +104,9 @@ def test_full_size(name):
     assert int(case.free_top.item()) == top0 + freed
     assert int((nblocks0 - case.nblocks).sum().item()) == freed
 
-    # sampled units against the oracle
+    # every unit of one layer plus seeded units against the oracle (all host threads)
     case.restore(snap)
-    units = sample_units(case, 4, 1)
+    units = sample_units(case, EXTRA_UNITS[name], 1)
     mask = np.zeros((sp.B, sp.L, sp.H), bool)
     for u in units:
         mask[u] = True
@@ -105,12 +114,15 @@ def test_full_size(name):
     s_gpu_np = s_gpu.cpu().numpy()
     k_gpu_np = k_gpu.cpu().numpy()
     lse_gpu = cp.lse.cpu().numpy()
+    worst, inband = 0.0, 0
     for (b, l, h) in units:
         so = s_orc[l, h, noff[b]:noff[b + 1]]
-        PT.check_scores(s_gpu_np[l, h, noff[b]:noff[b + 1]], so, f"{name} unit {(b, l, h)}")
+        worst = max(worst, PT.check_scores(s_gpu_np[l, h, noff[b]:noff[b + 1]], so, f"{name} unit {(b, l, h)}"))
         PT.check_lse(lse_gpu[b, l, h], lse_orc[b, l, h], f"{name} lse {(b, l, h)}")
         ko = oracle.select(so, m[b])
-        PT.check_keep(k_gpu_np[l, h, moff[b]:moff[b + 1]], ko, so, min(m[b], n[b]), f"{name} keep {(b, l, h)}")
+        inband += PT.check_keep(k_gpu_np[l, h, moff[b]:moff[b + 1]], ko, so, min(m[b], n[b]), f"{name} keep {(b, l, h)}")
+    print(f"{name}: {len(units)} units against the oracle, worst score error {worst:.2e}, "
+          f"{inband} in-band selection differences")
 
     # compaction of the whole cache given a seeded selection, bit-exact, a few layers at a time
     keep = workloads.random_keep(case, m, 11)

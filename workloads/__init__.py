@@ -86,6 +86,12 @@ def spec(name: str, seed: int = 0) -> Spec:
         lengths, ks = _ragged_draw(seed)
         return Spec("batched-ragged", L=1, H=8, G=8, d=128, P=16, q=16, lengths=lengths,
                     budget=("actkv", ks), kv="normal", qdist="normal", shuffle_pages=True)
+    if name == "batched-ragged-sinks":
+        # The batched-ragged shape with the other reading of its K/V distribution: that of the
+        # Qwen3-shaped cache (LogNormal token norms, the first 4 tokens x8 as attention sinks).
+        lengths, ks = _ragged_draw(seed)
+        return Spec("batched-ragged-sinks", L=1, H=8, G=8, d=128, P=16, q=16, lengths=lengths,
+                    budget=("actkv", ks), kv="sinks", qdist="normal", shuffle_pages=True)
     if name == "long-context":
         return Spec("long-context", L=36, H=8, G=8, d=128, P=32, q=32, lengths=(131072,),
                     budget=("ratio", 0.2), kv="normal", qdist="aligned")
@@ -96,7 +102,7 @@ def spec(name: str, seed: int = 0) -> Spec:
     raise KeyError(name)
 
 
-NAMES = ("tiny", "qwen3-30b-a3b", "batched-ragged", "long-context", "multi-turn")
+NAMES = ("tiny", "qwen3-30b-a3b", "batched-ragged", "batched-ragged-sinks", "long-context", "multi-turn")
 
 
 def custom(name="custom", *, L=1, H=2, G=2, d=64, P=16, q=4, lengths=(100,), budget=("ratio", 0.2),
