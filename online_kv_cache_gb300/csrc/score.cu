@@ -92,8 +92,12 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // item -> (unit, row group, key range).  Order: split fastest, then group, head, layer.
-__device__ __forceinline__ Item decode_item(const LaunchMeta& meta, int64_t item, int total_sub) {
+// `rev`: items are taken from the end of the launch's list (the alpha pass
+// does this: the companion LSE pass ended on the last units, so their keys
+// are still in L2 when the alpha pass starts on them).
+__device__ __forceinline__ Item decode_item(const LaunchMeta& meta, int64_t item, int total_sub, bool rev) {
   Item it;
+  if (rev) item = meta.items - 1 - item;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
   // 32-bit arithmetic: a sequence owns fewer than 2^32 items of a launch, and the
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Page-ring cursor: one commit group per key tile of this CTA, in K order;
     // lane p < ppt copies the block-table entry of page p of the tile.
     int64_t pf_item = blockIdx.x;
-    Item pf = pf_item < meta.items ? decode_item(meta, pf_item, total_sub) : Item{};
+    Item pf = pf_item < meta.items ? decode_item(meta, pf_item, total_sub, PASS == 2) : Item{};
     int pf_t = pf.t0;
     uint32_t pf_count = 0;
     auto page_prefetch = [&]() {
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++pf_t >= pf.t1) {
           pf_item += gridDim.x;
           if (pf_item < meta.items) {
-            pf = decode_item(meta, pf_item, total_sub);
+            pf = decode_item(meta, pf_item, total_sub, PASS == 2);
             pf_t = pf.t0;
           }
         }
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPageRing - 1; ++i) page_prefetch();
 
     int64_t k_item = blockIdx.x, q_item = blockIdx.x;
-    Item kit_ = k_item < meta.items ? decode_item(meta, k_item, total_sub) : Item{};
+    Item kit_ = k_item < meta.items ? decode_item(meta, k_item, total_sub, PASS == 2) : Item{};
     int kt = kit_.t0;
 
     while (ok && (k_item < meta.items || q_item < meta.items)) {
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         do_q = __shfl_sync(0xffffffffu, fr, 0) != 0u;
       }
       if (do_q) {
-        const Item qi = decode_item(meta, q_item, total_sub);
+        const Item qi = decode_item(meta, q_item, total_sub, PASS == 2);
         const int qrow = ((qi.u.b * meta.L + qi.u.l) * meta.H + qi.u.h) * meta.R +
                          qi.u.g * meta.gsub * sub_rows;
         // stall_ns > 0 (failure-path test): no proxy-row load is issued, so the
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++kt >= kit_.t1) {
         k_item += gridDim.x;
         if (k_item < meta.items) {
-          kit_ = decode_item(meta, k_item, total_sub);
+          kit_ = decode_item(meta, k_item, total_sub, PASS == 2);
           kt = kit_.t0;
         }
       }
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_desc = sdesc_k_sw128(q_base);
       const uint32_t q_kb_step = (uint32_t)(sub_rows * 128) >> 4;  // one k-block of a Q sub-tile
       for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
-        const Item it = decode_item(meta, item, total_sub);
+        const Item it = decode_item(meta, item, total_sub, PASS == 2);
         if (PASS == 1) {
           // the previous item's MMAs read the TMEM copy of Q: let them finish
           if (issued) {
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t slot = 0, use = 0;  // accumulator slot of job jc and its use count
     bool ok = true;
     for (int64_t item = blockIdx.x; item < meta.items && ok; item += gridDim.x) {
-      const Item it = decode_item(meta, item, total_sub);
+      const Item it = decode_item(meta, item, total_sub, PASS == 2);
       float m_run[4], s_run[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
