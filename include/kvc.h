@@ -376,7 +376,9 @@ kvc_status kvc_commit_fresh(const kvc_cache *cache, const kvc_segments *segs, co
 /* ------------------------------------------------------ Attention Matching */
 
 /* Bytes of workspace kvc_am_fit needs: per (layer, head, sequence with m > 0)
- * about 4 * ((R + m) * (m + 4) + R * (d + 1) + m * (d + 1)) bytes. */
+ * about 4 * ((R + m) * (m + 4) + R * (d + 1) + m * (d + 1)) bytes, plus the
+ * workspace of the LSE pass (kvc_score_workspace_size) and 4 * B * L * H * R
+ * bytes of row LSE; 0 when no sequence keeps an entry. */
 kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                                  int32_t R, size_t *bytes);
 
@@ -391,7 +393,10 @@ kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *seg
  * descent on their normal equations over the kept keys in ascending position
  * order, from token eviction's answer (beta = 0, V_C = the kept V rows), the
  * first projected onto w >= 0; the second uses the fitted beta.  sweeps in
- * [0, 1000]; 0 leaves token eviction's answer.  fp32 throughout (CUDA cores).
+ * [0, 1000]; 0 leaves token eviction's answer.  The full-attention targets
+ * (LSE and softmax(Q K^T) V over all n keys) run on the tensor cores (bf16
+ * Q, K and V as stored, fp32 accumulation, the probabilities in two bf16
+ * parts); the Gram products and descents in fp32 on the CUDA cores.
  * Effects: every kept entry's V row becomes its V_C row (bf16, round to
  * nearest even) and, when cache->aux is not NULL, its per-slot state becomes
  * beta (-inf where w = 0: the key is masked); kvc_compact then moves both with
@@ -402,8 +407,9 @@ kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *seg
  *   beta  out fp32 [L][H][Mtot] or NULL
  *   vc    out fp32 [L][H][Mtot][d] (V_C before rounding) or NULL
  *   ws    kvc_am_workspace_size bytes, 256-byte aligned
- * A keep position outside its segment sets KVC_DEV_BAD_KEEP, a block-table
- * entry outside the pool KVC_DEV_BAD_PAGE (that entry is skipped). */
+ * A keep position outside its segment or out of ascending order sets
+ * KVC_DEV_BAD_KEEP, a block-table entry outside the pool KVC_DEV_BAD_PAGE
+ * (that entry is skipped). */
 kvc_status kvc_am_fit(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                       const uint16_t *q, int32_t R, float scale, const int32_t *keep, int32_t sweeps,
                       float *beta, float *vc, void *ws, size_t ws_bytes, kvc_stream_t stream);

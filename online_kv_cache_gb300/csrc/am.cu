@@ -14,11 +14,15 @@
 // T sweeps over the kept keys in ascending position order; every logit of a
 // unit is shifted by c = max_i LSE_i, which changes neither minimiser.
 //
-// Work is fp32 on the CUDA cores: the fits are ill-conditioned (exp of
+// The targets (the full attention output over all n keys, the one contraction
+// of the size of the scoring passes) run on the tensor cores with bf16 Q, K and
+// V exactly as stored and the probabilities split into two bf16 parts; the
+// rest is fp32 on the CUDA cores: the fits are ill-conditioned (exp of
 // logits), so their Gram matrices cannot take the 8-bit-mantissa rounding of a
 // bf16 or tf32 tensor-core contraction.  Per unit the kernels run
-//   am_targets_kernel  Y = softmax(L) V and LSE over all n keys (online softmax)
-//   am_exp_kernel      E = exp(L_C - c) over the kept keys, s = exp(LSE - c)
+//   (scoring LSE pass) LSE_i over all n keys, the rows' log-sum-exp
+//   am_targets_tc_kernel  Y = softmax(L) V over all n keys on the tensor cores
+//                      and E = exp(L_C - c) over the kept keys, s = exp(LSE - c)
 //   am_atb_kernel      G = E^T [E | s]              (mode 0)
 //   am_mass_kernel     w by projected coordinate descent; beta = ln w
 //   am_probs_kernel    Ph = rows of E diag(w), normalised (in place)
@@ -117,295 +121,321 @@ __device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, cons
   return pos;
 }
 
-// 64 rows x D of a bf16 matrix into shared memory (fp32, row stride D + 1),
-// zero rows where row_of(i) < 0.  16-byte loads, consecutive threads along a row.
-template <int D, typename RowOf>
-__device__ __forceinline__ void load_rows64(float* dst, const uint16_t* src, RowOf row_of) {
-  constexpr int kChunks = D / 8;
-  for (int ci = threadIdx.x; ci < 64 * kChunks; ci += kAmThreads) {
-    const int i = ci / kChunks, dc = ci % kChunks;
-    const int64_t row = row_of(i);
-    float v[8];
-    if (row >= 0) {
-      unpack8(*reinterpret_cast<const uint4*>(src + row * D + dc * 8), v);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[i * (D + 1) + dc * 8 + e] = v[e];
-  }
-}
-
-// acc[a][b] = sum_k A[ty + 16a][k] * B[tx + 16b][k] over 64 x 64 tiles (stride D + 1).
-template <int D>
-__device__ __forceinline__ void dot64(const float* As, const float* Bs, int ty, int tx, float acc[4][4]) {
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
-#pragma unroll 4
-  for (int k = 0; k < D; ++k) {
-    float qa[4], kb[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) qa[a] = As[(ty + 16 * a) * (D + 1) + k];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) kb[b] = Bs[(tx + 16 * b) * (D + 1) + k];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qa[a], kb[b], acc[a][b]);
-  }
-}
-
-__device__ __forceinline__ float max16(float v) {
-#pragma unroll
-  for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float sum16(float v) {
-#pragma unroll
-  for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Targets tiling: 128 proxy rows per block, keys in tiles of 64.
-constexpr int kTgRows = 128;
-constexpr int kTgKeys = 64;
-constexpr int kTgPs = kTgRows + 1;  // row stride of the probability tile (fewer bank conflicts)
+// ------------------------------------------------------------------ targets (tensor cores)
+// Block = (unit, 128 proxy rows), 192 threads:
+//   warp 0      producer: the block's Q rows (two-dimensional TMA, once), then
+//               the K and V tiles of 128 keys, page by page (four-dimensional
+//               TMA: one copy per page lands as 1024-byte atoms of 8 keys x 64
+//               head-dim elements), through a ring of kTcStages; the block-table
+//               entries of the next tile are loaded while this tile is issued
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 2..5  epilogue, one TMEM lane quarter (32 rows) each
+// Per key tile t the issuer forms S = Q K_t^T (bf16 operands, fp32 in TMEM; two
+// S buffers, so tile t+1's logits form while tile t's probabilities are made).
+// The epilogue turns row i of S into p_ij = 2^(c L_ij - lse2_i) with the row's
+// log-sum-exp from the scoring LSE pass, so p <= 1 and no running maximum or
+// rescaling of the output is needed; it splits p into its bf16 rounding and
+// the bf16 of the remainder (16 bits of mantissa together) and stores both into
+// TMEM.  The issuer then accumulates Y += P_hi V_t + P_lo V_t with A read from
+// TMEM and V_t as an MN-major B operand (the pool stores V key by key).  At the
+// end Y = softmax(L) V and the LSE rows go to the unit's workspace.
+// TMEM columns: S0 [0, 128), S1 [128, 256), P_hi [256, 320), P_lo [320, 384),
+// Y [384, 384 + D).
+constexpr int kTcThreads = 192;
+constexpr int kTcStages = 2;
+constexpr int kTcRows = 128;   // proxy rows per block = MMA M
+constexpr int kTcKeys = 128;   // keys per tile
+constexpr int kTcHead = 1024;  // barriers, TMEM address, abort flag
 
 template <int D>
-constexpr int targets_kp_floats() {  // Kt [D][64], later Pt [64][129] in the same place
-  return D * kTgKeys > kTgKeys * kTgPs ? D * kTgKeys : kTgKeys * kTgPs;
+constexpr int tc_tile_bytes() { return kTcKeys * D * 2; }
+template <int D>
+constexpr int tc_smem_bytes() {  // head, alignment slack, Q rows, kTcStages x (K tile, V tile), keep list
+  return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4;
+}
+static_assert(tc_smem_bytes<128>() <= 227 * 1024, "targets working set fits one CTA's shared memory");
+
+// bf16 bits of x (round to nearest even); x finite.
+__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
 template <int D>
-constexpr int targets_smem_bytes() {  // Qt [D][128], Kt / Pt, Vs [64][D]
-  return (D * kTgRows + targets_kp_floats<D>() + kTgKeys * D) * 4;
-}
+__global__ void __launch_bounds__(kTcThreads, 1)
+    am_targets_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ, const AmMeta meta,
+                         const int32_t* __restrict__ bt, const int32_t* __restrict__ keep,
+                         const float* __restrict__ lse_rows, float* ws, unsigned* status) {
+  constexpr int KB = D / 64;                     // 128-byte k-blocks per row
+  constexpr int kTile = tc_tile_bytes<D>();
+  constexpr uint32_t kColP = 256, kColPlo = 320, kColY = 384;
+  extern __shared__ __align__(16) uint8_t tc_smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem);
+  uint64_t* q_full = bars;                        // [1]
+  uint64_t* st_full = bars + 1;                   // [kTcStages] K and V of a tile landed
+  uint64_t* st_empty = st_full + kTcStages;       // [kTcStages] the tile's MMAs are done
+  uint64_t* s_full = st_empty + kTcStages;        // [2] S buffer formed
+  uint64_t* s_empty = s_full + 2;                 // [2] S buffer read (4 epilogue warps)
+  uint64_t* p_full = s_empty + 2;                 // P stored (4 epilogue warps)
+  uint64_t* p_empty = p_full + 1;                 // P read by the output MMAs
+  uint64_t* y_full = p_empty + 1;                 // all output MMAs done
+  uint64_t* drain = y_full + 1;                   // abort: every MMA issued is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tc_smem + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem) + kTcHead + 1023) &
+                                           ~uintptr_t(1023));
+  uint8_t* sKV = sQ + kTcRows * D * 2;            // stage s: K at s * 2 * kTile, V at + kTile
+  int32_t* sKeep = reinterpret_cast<int32_t*>(sKV + kTcStages * 2 * kTile);  // the unit's kept positions
+  float* red = reinterpret_cast<float*>(tc_smem + 576);  // [6] warp maxima of the rows' LSE
 
-// ------------------------------------------------------------------ targets
-// Block = (unit, 128 proxy rows), 16 x 16 threads.  Online softmax over all n
-// keys of the segment in tiles of 64.  Thread (ty, tx) forms the logits of rows
-// 8 ty .. 8 ty + 7 against keys 4 tx .. 4 tx + 3 of the tile from Q and K held
-// dimension-major in shared memory (three 128-bit loads per 32 multiply-adds),
-// keeps the rows' running max (common to the 16 threads of a row, through
-// shuffles) and its own share of their running sums, and accumulates Y rows
-// 8 ty .. 8 ty + 7, columns tx D/16 .. tx D/16 + D/16 - 1 from the tile's
-// probabilities (key-major, over the key tile once the logits are formed) and
-// values.  Writes LSE (natural log) and Y = softmax(L) V to the unit's workspace.
-template <int D>
-__global__ void __launch_bounds__(kAmThreads) am_targets_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
-                                                                const uint16_t* __restrict__ kp,
-                                                                const uint16_t* __restrict__ vp,
-                                                                const uint16_t* __restrict__ q, float* ws,
-                                                                unsigned* status) {
-  extern __shared__ __align__(16) float am_smem[];
-  constexpr int kCpt = D / 16;  // Y columns per thread
-  constexpr int kChunks = D / 8;
-  float* Qt = am_smem;                            // [D][128]
-  float* Kt = Qt + D * kTgRows;                   // [D][64]
-  float* Pt = Kt;                                 // [64][129]
-  float* Vs = Kt + targets_kp_floats<D>();        // [64][D]
-  const int rb = (meta.R + kTgRows - 1) / kTgRows;
-  const int64_t unit = blockIdx.x / rb;
-  const int r0 = (int)(blockIdx.x % rb) * kTgRows;
-  const AmUnit u = am_unit(meta, unit, ws);
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  const int64_t qrow0 = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
-  for (int ci = threadIdx.x; ci < kTgRows * kChunks; ci += kAmThreads) {  // Q (zero past R)
-    const int i = ci % kTgRows, dc = ci / kTgRows;
-    float v[8];
-    if (r0 + i < meta.R) {
-      unpack8(*reinterpret_cast<const uint4*>(q + (qrow0 + r0 + i) * D + dc * 8), v);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) Qt[(dc * 8 + e) * kTgRows + i] = v[e];
-  }
-  const float c2 = meta.scale * kLog2e;
-  float mx[8], sm[8], y[8][kCpt];
-#pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    mx[a] = -INFINITY;
-    sm[a] = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kCpt; ++e) y[a][e] = 0.0f;
-  }
-  // The next tile's keys and values are loaded into registers while this
-  // tile's products run (kLd 16-byte chunks of each per thread).
-  constexpr int kLd = kTgKeys * kChunks / kAmThreads;
-  static_assert(kLd * kAmThreads == kTgKeys * kChunks, "tile chunks split evenly over the threads");
-  uint4 kr[kLd], vr[kLd];
-  auto fetch = [&](int t0) {
-#pragma unroll
-    for (int c = 0; c < kLd; ++c) {
-      const int ci = threadIdx.x + c * kAmThreads;
-      const int ik = ci % kTgKeys, dk = ci / kTgKeys;  // keys: consecutive threads on consecutive keys
-      const int iv = ci / kChunks, dv = ci % kChunks;  // values: consecutive threads along a row
-      const int64_t rk = t0 + ik < u.n ? am_row(meta, u, bt, t0 + ik, status) : -1;
-      const int64_t rv = t0 + iv < u.n ? am_row(meta, u, bt, t0 + iv, status) : -1;
-      kr[c] = rk >= 0 ? *reinterpret_cast<const uint4*>(kp + rk * D + dk * 8) : make_uint4(0u, 0u, 0u, 0u);
-      vr[c] = rv >= 0 ? *reinterpret_cast<const uint4*>(vp + rv * D + dv * 8) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  fetch(0);
-  for (int j0 = 0; j0 < u.n; j0 += kTgKeys) {
-    __syncthreads();  // the previous tile's Pt and Vs are fully read
-#pragma unroll
-    for (int c = 0; c < kLd; ++c) {  // keys dimension-major, values key-major; bf16 bits -> fp32 (zero rows stay zero)
-      const int ci = threadIdx.x + c * kAmThreads;
-      const int ik = ci % kTgKeys, dk = ci / kTgKeys;
-      const int iv = ci / kChunks, dv = ci % kChunks;
-      float v[8];
-      unpack8(kr[c], v);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) Kt[(dk * 8 + e) * kTgKeys + ik] = v[e];
-      unpack8(vr[c], v);
-      float4* dst = reinterpret_cast<float4*>(Vs + iv * D + dv * 8);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
-    __syncthreads();
-    if (j0 + kTgKeys < u.n) fetch(j0 + kTgKeys);
-    float acc[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
-#pragma unroll 2
-    for (int k = 0; k < D; ++k) {
-      const float4 q0 = *reinterpret_cast<const float4*>(Qt + k * kTgRows + ty * 8);
-      const float4 q1 = *reinterpret_cast<const float4*>(Qt + k * kTgRows + ty * 8 + 4);
-      const float4 k0 = *reinterpret_cast<const float4*>(Kt + k * kTgKeys + tx * 4);
-      const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      const float kv[4] = {k0.x, k0.y, k0.z, k0.w};
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], kv[b], acc[a][b]);
-    }
-    __syncthreads();  // every thread's logits are formed: Kt is free for Pt
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      float t[4], tmax = -INFINITY;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        t[b] = (j0 + tx * 4 + b < u.n) ? acc[a][b] * c2 : -INFINITY;
-        tmax = fmaxf(tmax, t[b]);
-      }
-      const float mnew = fmaxf(mx[a], max16(tmax));  // finite: key j0 is in the segment
-      const float alpha = exp2f(mx[a] - mnew);        // 0 on the first tile (mx = -inf)
-      float ps = 0.0f;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const float p = exp2f(t[b] - mnew);
-        Pt[(tx * 4 + b) * kTgPs + ty * 8 + a] = p;
-        ps += p;
-      }
-      sm[a] = sm[a] * alpha + ps;
-      mx[a] = mnew;
-#pragma unroll
-      for (int e = 0; e < kCpt; ++e) y[a][e] *= alpha;
-    }
-    __syncthreads();
-#pragma unroll 2
-    for (int j = 0; j < kTgKeys; ++j) {
-      float pv[8], vv[kCpt];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) pv[a] = Pt[j * kTgPs + ty * 8 + a];
-#pragma unroll
-      for (int e = 0; e < kCpt; e += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * D + tx * kCpt + e);
-        vv[e] = v4.x;
-        vv[e + 1] = v4.y;
-        vv[e + 2] = v4.z;
-        vv[e + 3] = v4.w;
-      }
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int e = 0; e < kCpt; ++e) y[a][e] = fmaf(pv[a], vv[e], y[a][e]);
-    }
-  }
-  float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
-  float* lse = u.base + am_off_lse(meta.R, u.m, u.ldE, D);
-#pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const float s = sum16(sm[a]);  // every lane takes part in the shuffles
-    const int i = r0 + ty * 8 + a;
-    if (i >= meta.R) continue;
-    const float inv = 1.0f / s;
-#pragma unroll
-    for (int e = 0; e < kCpt; e += 4)
-      *reinterpret_cast<float4*>(Y + (int64_t)i * D + tx * kCpt + e) =
-          make_float4(y[a][e] * inv, y[a][e + 1] * inv, y[a][e + 2] * inv, y[a][e + 3] * inv);
-    if (tx == 0) lse[i] = (mx[a] + log2f(s)) * kLn2;
-  }
-}
+  const int rb = (meta.R + kTcRows - 1) / kTcRows;
+  const AmUnit u = am_unit(meta, blockIdx.x / rb, ws);
+  const int r0 = (int)(blockIdx.x % rb) * kTcRows;
+  const int T = (u.n + kTcKeys - 1) / kTcKeys;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-template <int D>
-constexpr int exp_smem_bytes() {
-  return (2 * 64 * (D + 1) + 8) * 4;
-}
-
-// ------------------------------------------------------------------ exp
-// Block = (unit, 64 proxy rows, 64 kept keys): E[i][j] = exp(L_ij - c) with
-// c = max_i LSE_i, and (key block 0) column m = s_i = exp(LSE_i - c).
-template <int D>
-__global__ void __launch_bounds__(kAmThreads) am_exp_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
-                                                            const uint16_t* __restrict__ kp,
-                                                            const uint16_t* __restrict__ q,
-                                                            const int32_t* __restrict__ keep, float* ws,
-                                                            unsigned* status) {
-  extern __shared__ __align__(16) float am_smem[];
-  float* Qs = am_smem;            // [64][D + 1]
-  float* Ks = Qs + 64 * (D + 1);  // [64][D + 1]
-  float* red = Ks + 64 * (D + 1); // [8]
-  const int rb = (meta.R + 63) / 64;
-  const int cb = (meta.max_m + 63) / 64;
-  const int cblk = (int)(blockIdx.x % cb);
-  const int64_t rest = blockIdx.x / cb;
-  const int r0 = (int)(rest % rb) * 64;
-  const AmUnit u = am_unit(meta, rest / rb, ws);
-  if (cblk * 64 >= u.m) return;
-  const float* lse = u.base + am_off_lse(meta.R, u.m, u.ldE, D);
-  // c = max_i LSE_i of the unit
-  float c = -INFINITY;
-  for (int i = threadIdx.x; i < meta.R; i += kAmThreads) c = fmaxf(c, lse[i]);
+  // zero the K/V ring: rows of pages past the segment are never loaded and
+  // must hold finite values (their probabilities are 0)
+  for (int i = threadIdx.x; i < kTcStages * 2 * kTile / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(sKV)[i] = make_uint4(0u, 0u, 0u, 0u);
+  // the unit's kept positions (ascending) and the shift c = max_i LSE_i of its rows
+  const int64_t krow0 = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
+  for (int k = threadIdx.x; k < u.m; k += kTcThreads) {
+    const int32_t pos = __ldg(keep + krow0 + k);
+    // the tile walk below needs the positions inside the segment and strictly ascending
+    if (pos < 0 || pos >= u.n || (k > 0 && pos <= __ldg(keep + krow0 + k - 1))) atomicOr(status, KVC_DEV_BAD_KEEP);
+    sKeep[k] = pos;
+  }
+  const int64_t lrow = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
+  float cmax = -INFINITY;
+  for (int k = threadIdx.x; k < meta.R; k += kTcThreads) cmax = fmaxf(cmax, __ldg(lse_rows + lrow + k));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  const int64_t qrow0 = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
-  load_rows64<D>(Qs, q, [&](int i) -> int64_t { return r0 + i < meta.R ? qrow0 + r0 + i : -1; });
-  const int j0 = cblk * 64;
-  load_rows64<D>(Ks, kp, [&](int i) -> int64_t {
-    if (j0 + i >= u.m) return -1;
-    const int pos = am_kept(meta, u, keep, j0 + i, status);
-    return pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
-  });
+  for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cmax;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kTcStages; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4); }
+    mbar_init(p_full, 4);
+    mbar_init(p_empty, 1);
+    mbar_init(y_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed ring, for the tensor cores
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, 512);
+  }
+  tc_fence_before_sync();
   __syncthreads();
-  c = red[0];
-#pragma unroll
-  for (int w = 1; w < kAmThreads / 32; ++w) c = fmaxf(c, red[w]);
-  float acc[4][4];
-  dot64<D>(Qs, Ks, ty, tx, acc);
-  const float c2 = meta.scale * kLog2e, cc = c * kLog2e;
-  float* E = u.base;
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int i = r0 + ty + 16 * a;
-    if (i >= meta.R) continue;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int j = j0 + tx + 16 * b;
-      if (j < u.m) E[(int64_t)i * u.ldE + j] = exp2f(fmaf(acc[a][b], c2, -cc));
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    bool ok = true;
+    uint32_t issued = 0;  // tiles whose copies were issued
+    const int64_t qrow = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R + r0;
+    if (lane == 0) mbar_arrive_expect_tx(q_full, KB * kTcRows * 128);
+    __syncwarp();
+    if (lane < KB) tma_load_2d(sQ + lane * kTcRows * 128, &tmQ, q_full, lane * 64, (int32_t)qrow);
+    const int ppt = kTcKeys / meta.P;  // pages per tile (<= 16)
+    const int32_t* bt_row = bt + (int64_t)u.b * meta.max_blocks;
+    auto page_of = [&](int t) -> int32_t {
+      const int slot = t * kTcKeys + lane * meta.P;
+      if (lane >= ppt || slot >= u.n) return -1;
+      const int32_t pg = __ldg(bt_row + (u.s0 + slot) / meta.P);
+      if (pg < 0 || pg >= meta.num_pages) {
+        atomicOr(status, KVC_DEV_BAD_PAGE);  // outside the pool: reported, not read
+        return -1;
+      }
+      return pg;
+    };
+    int32_t pg_next = page_of(0);
+    for (int t = 0; t < T && ok; ++t) {
+      const int32_t pg = pg_next;
+      if (t + 1 < T) pg_next = page_of(t + 1);
+      const int st = t % kTcStages;
+      if (lane == 0) ok = mbar_wait(&st_empty[st], ((t / kTcStages) & 1) ^ 1, abort_flag, status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
+      if (lane == 0) mbar_arrive_expect_tx(&st_full[st], __popc(valid) * 2u * KB * meta.P * 128u);
+      __syncwarp();
+      if (pg >= 0) {
+        const int32_t prow = (int32_t)((((int64_t)u.l * meta.num_pages + pg) * meta.H + u.h) * meta.P);
+        uint8_t* dk = sKV + st * 2 * kTile + lane * meta.P * D * 2;
+        tma_load_4d(dk, &tmK, &st_full[st], 0, 0, 0, prow >> 3);
+        tma_load_4d(dk + kTile, &tmV, &st_full[st], 0, 0, 0, prow >> 3);
+      }
+      ++issued;
     }
-    if (cblk == 0 && tx == 0) E[(int64_t)i * u.ldE + u.m] = exp2f((lse[i] - c) * kLog2e);
+    // let the copies issued land before the CTA exits, whichever role gave up
+    if (lane == 0) {
+      mbar_wait(q_full, 0, nullptr, status);
+      for (uint32_t t = issued > (uint32_t)kTcStages ? issued - kTcStages : 0; t < issued; ++t)
+        mbar_wait(&st_full[t % kTcStages], (t / kTcStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag, status);
+      bool issued = false;
+      const uint32_t idesc_s = idesc_bf16_f32(kTcRows, kTcKeys);
+      const uint32_t idesc_y = idesc_bf16_f32(kTcRows, D) | (1u << 16);  // B (V) MN-major
+      const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ));
+      auto issue_s = [&](int t) {  // S[t & 1] = Q K_t^T
+        const int st = t % kTcStages;
+        const uint64_t k_desc = sdesc_k_sw128(smem_u32(sKV + st * 2 * kTile), KB * 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + (uint32_t)(t & 1) * 128u,
+                   q_desc + ((uint64_t)((k >> 2) * (kTcRows * 128) + (k & 3) * 32) >> 4),
+                   k_desc + ((uint64_t)((k >> 2) * 1024 + (k & 3) * 32) >> 4), idesc_s, k > 0);
+        mma_commit(&s_full[t & 1]);
+        issued = true;
+      };
+      for (int t = 0; t <= T && ok; ++t) {
+        // S of tile t (ahead of tile t - 1's output MMAs)
+        if (t < T) {
+          if (!(ok = mbar_wait(&st_full[t % kTcStages], (t / kTcStages) & 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait(&s_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, status))) break;
+          tc_fence_after_sync();
+          issue_s(t);
+        }
+        if (t == 0) continue;
+        // output of tile t - 1: Y += P_hi V + P_lo V
+        const int tp = t - 1;
+        if (!(ok = mbar_wait(p_full, tp & 1, abort_flag, status))) break;
+        tc_fence_after_sync();
+        const uint32_t v_base = smem_u32(sKV + (tp % kTcStages) * 2 * kTile + kTile);
+#pragma unroll
+        for (int k = 0; k < kTcKeys / 16; ++k) {  // 16 keys = two 8-key atoms per step
+          const uint64_t v_desc = sdesc_mn_sw128(v_base + k * 2 * KB * 1024, 1024, KB * 1024);
+          mma_bf16_tmem_a(tmem + kColY, tmem + kColP + 8 * k, v_desc, idesc_y, (tp > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kTcKeys / 16; ++k) {
+          const uint64_t v_desc = sdesc_mn_sw128(v_base + k * 2 * KB * 1024, 1024, KB * 1024);
+          mma_bf16_tmem_a(tmem + kColY, tmem + kColPlo + 8 * k, v_desc, idesc_y, 1u);
+        }
+        mma_commit(p_empty);
+        mma_commit(&st_empty[tp % kTcStages]);
+      }
+      if (ok) {
+        mma_commit(y_full);
+      } else if (issued) {  // one more commit covers every MMA issued
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr, status);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int r = q4 * 32 + lane;          // row within the tile
+    const int i = r0 + r;                  // proxy row
+    const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
+    const float c2 = meta.scale * kLog2e;
+    const float lse = i < meta.R ? lse_rows[lrow + i] : INFINITY;
+    const float lse2 = lse * kLog2e;
+    float c = red[0];
+#pragma unroll
+    for (int w = 1; w < kTcThreads / 32; ++w) c = fmaxf(c, red[w]);
+    const float cc = c * kLog2e;
+    float* Erow = u.base + (int64_t)i * u.ldE;  // E[i][k] = exp(L_i,keep[k] - c), column m = s_i
+    int kk = 0;                                 // first kept position not yet passed
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      ok = mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after_sync();
+      float v[128];
+      tmem_ld128(t_lane + (uint32_t)(t & 1) * 128u, v);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[t & 1]);
+      const int nvalid = min(kTcKeys, u.n - t * kTcKeys);
+      {  // E over the kept keys of this tile, from the same logits as the LSE pass
+        uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;  // kept columns of the tile
+        const int k0 = kk;
+        while (kk < u.m && sKeep[kk] < (t + 1) * kTcKeys) {
+          const int col = sKeep[kk] - t * kTcKeys;
+          const uint32_t bit = col >= 0 ? 1u << (col & 31) : 0u;
+          const int w = col >> 5;
+          m0 |= w == 0 ? bit : 0u;
+          m1 |= w == 1 ? bit : 0u;
+          m2 |= w == 2 ? bit : 0u;
+          m3 |= w == 3 ? bit : 0u;
+          ++kk;
+        }
+        if (i < meta.R && kk > k0) {
+          int k = k0;
+#pragma unroll
+          for (int jj = 0; jj < kTcKeys; ++jj) {
+            const uint32_t mw = jj < 32 ? m0 : jj < 64 ? m1 : jj < 96 ? m2 : m3;
+            if ((mw >> (jj & 31)) & 1u) Erow[k++] = exp2f(fmaf(v[jj], c2, -cc));
+          }
+        }
+      }
+      ok = mbar_wait(p_empty, (t & 1) ^ 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32 keys: 16 packed pairs per half
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j0 = c * 32 + 2 * e;
+          const float p0 = j0 < nvalid ? ex2_approx(fmaf(v[j0], c2, -lse2)) : 0.0f;
+          const float p1 = j0 + 1 < nvalid ? ex2_approx(fmaf(v[j0 + 1], c2, -lse2)) : 0.0f;
+          const uint32_t h0 = bf16_rn_bits(p0), h1 = bf16_rn_bits(p1);
+          hi[e] = h0 | (h1 << 16);
+          lo[e] = bf16_rn_bits(p0 - __uint_as_float(h0 << 16)) | (bf16_rn_bits(p1 - __uint_as_float(h1 << 16)) << 16);
+        }
+        tmem_st16(t_lane + kColP + c * 16, hi);
+        tmem_st16(t_lane + kColPlo + c * 16, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) {
+      ok = mbar_wait(y_full, 0, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        float y[32];
+        tmem_ld32(t_lane + kColY + c, y);
+        if (i < meta.R) {
+          float4* dst = reinterpret_cast<float4*>(Y + (int64_t)i * D + c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+        }
+      }
+      if (i < meta.R) {
+        u.base[am_off_lse(meta.R, u.m, u.ldE, D) + i] = lse;
+        Erow[u.m] = exp2f((lse - c) * kLog2e);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -734,8 +764,7 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set[dev]) {
-    if ((e = set_smem(am_targets_kernel<D>, targets_smem_bytes<D>())) != cudaSuccess) return e;
-    if ((e = set_smem(am_exp_kernel<D>, exp_smem_bytes<D>())) != cudaSuccess) return e;
+    if ((e = set_smem(am_targets_tc_kernel<D>, tc_smem_bytes<D>())) != cudaSuccess) return e;
     if ((e = set_smem(am_mass_kernel, mass_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
     if ((e = set_smem(am_value_kernel<D>, value_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
@@ -749,14 +778,9 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
   for (size_t ci = 0; ci < al.chunks; ++ci) {
     const AmMeta& m = al.meta[ci];
     if (m.units <= 0) continue;
-    const int rb64 = (m.R + 63) / 64;
-    const int mt = (m.max_m + 63) / 64;
-    const int rbt = (m.R + kTgRows - 1) / kTgRows;
-    am_targets_kernel<D><<<(unsigned)(m.units * rbt), kAmThreads, targets_smem_bytes<D>(), stream>>>(
-        m, al.block_table, kp, vp, al.q, al.ws, al.status);
-    if ((e = check()) != cudaSuccess) return e;
-    am_exp_kernel<D><<<(unsigned)(m.units * rb64 * mt), kAmThreads, exp_smem_bytes<D>(), stream>>>(
-        m, al.block_table, kp, al.q, al.keep, al.ws, al.status);
+    const int rbt = (m.R + kTcRows - 1) / kTcRows;
+    am_targets_tc_kernel<D><<<(unsigned)(m.units * rbt), kTcThreads, tc_smem_bytes<D>(), stream>>>(
+        *al.tmK, *al.tmV, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
     const int mt128 = (m.max_m + kAtbTile - 1) / kAtbTile;
     const int nt0 = (m.max_m + 1 + kAtbTile - 1) / kAtbTile;

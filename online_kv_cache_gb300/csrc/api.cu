@@ -1211,6 +1211,15 @@ void build_am_plan(const kvc_cache* c, const Plan& p, int R, float scale, int sw
   out->floats = wsf;
 }
 
+// Attention Matching workspace: the units' fits, then the scoring LSE pass's
+// workspace, then the LSE of every proxy row ([B][L][H][R] floats).
+size_t am_lse_rows_bytes(const kvc_cache* c, int R) {
+  return (size_t)c->batch * c->num_layers * c->num_kv_heads * R * sizeof(float);
+}
+size_t am_workspace_bytes(const kvc_cache* c, const AmPlan& ap, size_t score_bytes, int R) {
+  return align256((size_t)ap.floats * sizeof(float)) + align256(score_bytes) + align256(am_lse_rows_bytes(c, R));
+}
+
 kvc_status check_am_args(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, int32_t R, Plan* p) {
   kvc_status st = check_cache(cache, kNeedK | kNeedV | kNeedBT);
   if (st != KVC_OK) return st;
@@ -1237,7 +1246,13 @@ kvc_status kvc_am_workspace_size(const kvc_cache* cache, const kvc_segments* seg
   if (st != KVC_OK) return st;
   AmPlan ap;
   build_am_plan(cache, p, R, 1.0f, 0, &ap);
-  *bytes = (size_t)ap.floats * sizeof(float);
+  if (p.Mtot == 0) {  // nothing to fit
+    *bytes = 0;
+    return ok();
+  }
+  size_t score_bytes = 0;
+  if ((st = kvc_score_workspace_size(cache, segs, R, &score_bytes)) != KVC_OK) return st;
+  *bytes = am_workspace_bytes(cache, ap, score_bytes, R);
   return ok();
 }
 
@@ -1257,14 +1272,31 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
   AmPlan ap;
   build_am_plan(cache, p, R, scale, sweeps, &ap);
-  const size_t need = (size_t)ap.floats * sizeof(float);
+  size_t score_bytes = 0;
+  if ((st = kvc_score_workspace_size(cache, segs, R, &score_bytes)) != KVC_OK) return st;
+  const size_t need = am_workspace_bytes(cache, ap, score_bytes, R);
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
+  // the LSE of every proxy row over its segment's keys: the scoring LSE pass
+  uint8_t* score_ws = static_cast<uint8_t*>(ws) + align256((size_t)ap.floats * sizeof(float));
+  float* lse_rows = reinterpret_cast<float*>(score_ws + align256(score_bytes));
+  if ((st = score_common("kvc_am_fit", kPhaseLse, 2.0f, cache, segs, q, R, scale, nullptr, lse_rows, nullptr,
+                         score_ws, align256(score_bytes), stream)) != KVC_OK)
+    return st;
+  const int64_t krows = (int64_t)cache->num_layers * cache->num_pages * cache->num_kv_heads * cache->page_size;
+  CUtensorMap tmK, tmV, tmQ;
+  if ((st = make_kmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
+  if ((st = make_kmap(&tmV, cache->v_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
+  if ((st = make_tmap(&tmQ, q, qrows, cache->head_dim, kScoreTile)) != KVC_OK) return st;
   AmLaunch al;
   al.chunks = ap.metas.size();
   al.meta = ap.metas.data();
+  al.tmK = &tmK;
+  al.tmV = &tmV;
+  al.tmQ = &tmQ;
+  al.lse_rows = lse_rows;
   al.block_table = cache->block_table;
   al.k_pool = cache->k_pool;
   al.v_pool = cache->v_pool;

@@ -199,6 +199,10 @@ constexpr int kAmMaxR = 4096;
 struct AmLaunch {
   size_t chunks = 0;
   const AmMeta* meta = nullptr;  // [chunks]
+  const CUtensorMap* tmK = nullptr;  // K pool, one page per box (as the scoring passes)
+  const CUtensorMap* tmV = nullptr;  // V pool, same geometry
+  const CUtensorMap* tmQ = nullptr;  // Q, box {64, 128}
+  const float* lse_rows = nullptr;   // [B][L][H][R] natural-log LSE of every proxy row
   const int32_t* block_table = nullptr;
   const void* k_pool = nullptr;
   void* v_pool = nullptr;

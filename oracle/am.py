@@ -129,7 +129,8 @@ def beta_of(w: np.ndarray) -> np.ndarray:
 
 def unit(Q, K, V, keep, scale, sweeps):
     """AM on one (layer, head, sequence): returns a dict with the fitted w, beta, V_C (as vc),
-    and the shifted problem (E, s, Y, c) the objectives are measured on."""
+    the shifted problem (E, s, Y, c) the objectives are measured on, and the value fit's start
+    (x0, the kept keys' values)."""
     keep = np.asarray(keep, np.int64)
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
@@ -139,7 +140,8 @@ def unit(Q, K, V, keep, scale, sweeps):
     E = np.exp(logits(Q, K[keep], scale) - c)
     w = mass_fit(E, s, sweeps)
     vc = value_fit(compact_probs(E, w), Y, V[keep], sweeps)
-    return {"w": w, "beta": beta_of(w), "vc": vc, "E": E, "s": s, "Y": Y, "c": c, "lse": lse}
+    return {"w": w, "beta": beta_of(w), "vc": vc, "E": E, "s": s, "Y": Y, "c": c, "lse": lse,
+            "x0": V[keep]}
 
 
 def mass_objective(E, s, w) -> float:

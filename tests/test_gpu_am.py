@@ -15,11 +15,15 @@ What is compared depends on how well the unit's problem is conditioned:
   the descent in fp32, and freezes coordinates whose gradient is below 2^-17 of its terms'
   scale; on every unit of these cases and of the multi-turn shape's three query recipes the
   measured gap is at most 5.4e-6; the bound leaves a factor of ~2.
-  Where R > m and the fit is small, w and V_C themselves are compared element by element:
-  |w_gpu - w_orc| <= W_TOL max(1, |w_orc|) and |V_gpu - V_orc| <= VC_TOL max |V_orc| (measured
-  3.4e-5 and 1.2e-4; the bounds are 2e-4 and 5e-4).  On the multi-turn shape (m = 307 keys,
-  8 sweeps, far from converged) the same rounding moves individual entries by up to a few
-  percent while the residuals agree, so there only the residuals are compared.
+  Where R > m and the fit is small, w and V_C themselves are compared element by element,
+  against a per-unit bound the oracle derives: it re-runs both fits with E, s and Y perturbed by
+  independent relative noise of EPS = 1e-5 (a few times the rounding the GPU's inputs to the
+  fits carry: fp32-accumulated logits, the probabilities held as two bf16 parts, the LSE
+  normalisation) and takes the largest change of w (relative to max(1, |w|)) and of V_C
+  (relative to max |V_C|) over ENV_DRAWS draws; the GPU's w and V_C must lie within ENV_FACTOR
+  times that envelope of the oracle's.  After 8 sweeps V_C moves by up to ~100x the input noise
+  on these units (the descent has not converged and Ph is not well conditioned), so a fixed
+  bound would measure the fit's conditioning rather than the kernel.
 * Concentrated units (cond(E) > 1e8, up to 1e18 with planted proxy queries): the gradient of a
   key with almost no attention is rounding in any precision, and the plain fp64 descent itself
   takes steps of that size (w_j to 1e3), after which its value residual can stand above token
@@ -44,8 +48,9 @@ from tests import parity as PT
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 RES_TOL = 1e-5
-W_TOL = 2e-4
-VC_TOL = 5e-4
+EPS = 1e-5
+ENV_DRAWS = 6
+ENV_FACTOR = 3.0
 COND_WELL = 1e8
 
 
@@ -77,6 +82,23 @@ def run_gpu(case, m, keep_np, sweeps, aux):
     torch.cuda.synchronize()
     PT.device_status_clean()
     return beta.cpu().numpy().astype(np.float64), vc.cpu().numpy().astype(np.float64)
+
+
+def envelope(u, sweeps, key):
+    """Largest change of the oracle's w and V_C when its inputs E, s and Y carry independent
+    relative noise of EPS (seeded per unit)."""
+    rng = np.random.default_rng(abs(hash(key)) % (2 ** 32))
+    X0 = u["x0"]
+    ew = ev = 0.0
+    for _ in range(ENV_DRAWS):
+        E = u["E"] * (1 + EPS * rng.standard_normal(u["E"].shape))
+        s = u["s"] * (1 + EPS * rng.standard_normal(u["s"].shape))
+        Y = u["Y"] * (1 + EPS * rng.standard_normal(u["Y"].shape))
+        w = am.mass_fit(E, s, sweeps)
+        X = am.value_fit(am.compact_probs(E, w), Y, X0, sweeps)
+        ew = max(ew, np.max(np.abs(w - u["w"]) / np.maximum(1.0, np.abs(u["w"]))))
+        ev = max(ev, np.max(np.abs(X - u["vc"])) / np.abs(u["vc"]).max())
+    return ew, ev
 
 
 def check_units(units, m, beta, vc, sweeps, sample=None, elementwise=False):
@@ -115,12 +137,16 @@ def check_units(units, m, beta, vc, sweeps, sample=None, elementwise=False):
         worst["mass"] = max(worst["mass"], dm)
         if elementwise and u["E"].shape[1] > 0:
             assert well
+            env_w, env_v = envelope(u, sweeps, (b, l, h))
             ew = np.max(np.abs(wg - u["w"]) / np.maximum(1.0, np.abs(u["w"])))
             ev = np.max(np.abs(vc[l, h, sl] - u["vc"])) / np.abs(u["vc"]).max()
-            assert ew <= W_TOL, f"unit {(b, l, h)}: w differs by {ew:.3e} of max(1, |w|)"
-            assert ev <= VC_TOL, f"unit {(b, l, h)}: V_C differs by {ev:.3e} of max |V_C|"
-            worst["w"], worst["vc"] = max(worst["w"], ew), max(worst["vc"], ev)
-    print(f"sweeps={sweeps} units {kinds}: worst gaps " + ", ".join(f"{k} {v:.2e}" for k, v in worst.items()))
+            assert ew <= ENV_FACTOR * env_w + 1e-7, \
+                f"unit {(b, l, h)}: w differs by {ew:.3e} of max(1, |w|) (envelope {env_w:.3e})"
+            assert ev <= ENV_FACTOR * env_v + 1e-7, \
+                f"unit {(b, l, h)}: V_C differs by {ev:.3e} of max |V_C| (envelope {env_v:.3e})"
+            worst["w"], worst["vc"] = max(worst["w"], ew / (env_w + 1e-12)), max(worst["vc"], ev / (env_v + 1e-12))
+    print(f"sweeps={sweeps} units {kinds}: worst gaps " + ", ".join(f"{k} {v:.2e}" for k, v in worst.items())
+          + " (w, vc: in units of the unit's envelope)")
     return kinds
 
 
