@@ -41,7 +41,6 @@ namespace {
 
 constexpr int kAmThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 // A coordinate moves only when its gradient exceeds 2^-17 of the scale of the
 // gradient's own terms.  E and s come from fp32 logits (128-term fp32 dot
 // products), whose relative error reaches ~2e-5 where the logits are large
@@ -414,11 +413,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after_sync();
       float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int col = 0; col < D; col += 32) {
         float y[32];
-        tmem_ld32(t_lane + kColY + c, y);
+        tmem_ld32(t_lane + kColY + col, y);
         if (i < meta.R) {
-          float4* dst = reinterpret_cast<float4*>(Y + (int64_t)i * D + c);
+          float4* dst = reinterpret_cast<float4*>(Y + (int64_t)i * D + col);
 #pragma unroll
           for (int e = 0; e < 8; ++e) dst[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
         }
@@ -769,7 +768,6 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if ((e = set_smem(am_value_kernel<D>, value_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  const uint16_t* kp = static_cast<const uint16_t*>(al.k_pool);
   uint16_t* vp = static_cast<uint16_t*>(al.v_pool);
   auto check = [&]() {
     count_launch();
