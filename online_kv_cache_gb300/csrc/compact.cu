@@ -64,16 +64,14 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 // are marked in a shared-memory bitmap of the target region T; a block scan over
 // the bitmap words numbers the holes of T in ascending slot order; hole k takes
 // the k-th outside survivor (k < c_out) or is dead.
-__global__ void __launch_bounds__(kPlanThreads)
-    plan_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
-                const int32_t* __restrict__ keep, int32_t* __restrict__ moves,
-                int32_t* __restrict__ move_count, int32_t* __restrict__ dead,
-                int32_t* __restrict__ dead_count, unsigned* status) {
+__device__ __forceinline__ void plan_block(const LaunchMeta& meta, int64_t item, const int32_t* __restrict__ block_table,
+                                           const int32_t* __restrict__ keep, int32_t* __restrict__ moves,
+                                           int32_t* __restrict__ move_count, int32_t* __restrict__ dead,
+                                           int32_t* __restrict__ dead_count, unsigned* status) {
   extern __shared__ uint32_t bitmap[];  // meta.words words
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t sh_total;
   __shared__ uint32_t word_holes[kPlanThreads], word_first[kPlanThreads];
-  const int64_t item = blockIdx.x;
   const int si = find_seq(meta, item);
   const SeqMeta& s = meta.seq[si];
   const int P = meta.P;
@@ -232,12 +230,11 @@ __global__ void __launch_bounds__(kPlanThreads)
 // kRowSplit-th stretch of 256 entries (every entry is independent).
 constexpr int kRowSplit = 8;
 
-__global__ void __launch_bounds__(256)
-    rows_kernel(const __grid_constant__ LaunchMeta meta, const int32_t* __restrict__ block_table,
-                const int32_t* __restrict__ nblocks, int32_t* __restrict__ freed,
-                int32_t* __restrict__ new_rows, unsigned* status) {
-  const SeqMeta& s = meta.seq[blockIdx.x / kRowSplit];
-  const int j0 = (int)(blockIdx.x % kRowSplit) * blockDim.x + threadIdx.x;
+__device__ __forceinline__ void rows_block(const LaunchMeta& meta, int blk, const int32_t* __restrict__ block_table,
+                                           const int32_t* __restrict__ nblocks, int32_t* __restrict__ freed,
+                                           int32_t* __restrict__ new_rows, unsigned* status) {
+  const SeqMeta& s = meta.seq[blk / kRowSplit];
+  const int j0 = (blk % kRowSplit) * blockDim.x + threadIdx.x;
   const int js = kRowSplit * blockDim.x;
   const int P = meta.P;
   const int f = s.nb - s.X;
@@ -257,6 +254,23 @@ __global__ void __launch_bounds__(256)
     out[j] = v;
   }
   for (int i = j0; i < f; i += js) freed[s.foff + i] = row[sb + i];
+}
+
+// The slot plan and the block-table rows in one launch: blocks [0, plan.items)
+// plan one unit each, the next rows.nseq * kRowSplit blocks build the new
+// block-table rows and the freed lists (the two read the same block table and
+// write disjoint buffers).
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_rows_kernel(const __grid_constant__ LaunchMeta plan, const __grid_constant__ LaunchMeta rows,
+                     const int32_t* __restrict__ block_table, const int32_t* __restrict__ nblocks,
+                     const int32_t* __restrict__ keep, int32_t* __restrict__ moves,
+                     int32_t* __restrict__ move_count, int32_t* __restrict__ dead,
+                     int32_t* __restrict__ dead_count, int32_t* __restrict__ freed,
+                     int32_t* __restrict__ new_rows, unsigned* status) {
+  if ((int64_t)blockIdx.x < plan.items)
+    plan_block(plan, blockIdx.x, block_table, keep, moves, move_count, dead, dead_count, status);
+  else
+    rows_block(rows, (int)(blockIdx.x - plan.items), block_table, nblocks, freed, new_rows, status);
 }
 
 // One parallel copy.  A block copies up to meta.mpb moves of one unit
@@ -391,27 +405,20 @@ __global__ void __cluster_dims__(kPushCluster, 1, 1) __launch_bounds__(256)
 cudaError_t launch_plan(const CompactLaunch& cl, cudaStream_t stream) {
   for (size_t c = 0; c < cl.chunks; ++c) {
     const LaunchMeta& m = cl.plan_meta[c];
-    if (m.items > 0) {
-      const size_t smem = (size_t)std::max(1, m.words) * sizeof(uint32_t);
-      if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-      }
-      plan_kernel<<<(unsigned)m.items, kPlanThreads, smem, stream>>>(
-          m, cl.block_table, cl.keep, cl.moves, cl.move_count, cl.dead, cl.dead_count, cl.status);
-      cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-      count_launch();
-    }
     const LaunchMeta& r = cl.rows_meta[c];
-    if (r.nseq > 0) {
-      rows_kernel<<<(unsigned)(r.nseq * kRowSplit), 256, 0, stream>>>(r, cl.block_table, cl.nblocks, cl.freed,
-                                                        cl.new_rows, cl.status);
-      cudaError_t e = cudaGetLastError();
+    const int64_t blocks = m.items + (int64_t)r.nseq * kRowSplit;
+    if (blocks <= 0) continue;
+    const size_t smem = (size_t)std::max(1, m.words) * sizeof(uint32_t);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(plan_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      count_launch();
     }
+    plan_rows_kernel<<<(unsigned)blocks, kPlanThreads, smem, stream>>>(
+        m, r, cl.block_table, cl.nblocks, cl.keep, cl.moves, cl.move_count, cl.dead, cl.dead_count, cl.freed,
+        cl.new_rows, cl.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launch();
   }
   return cudaSuccess;
 }
