@@ -154,11 +154,6 @@ constexpr int tc_smem_bytes() {  // head, alignment slack, Q rows, kTcStages x (
 }
 static_assert(tc_smem_bytes<128>() <= 227 * 1024, "targets working set fits one CTA's shared memory");
 
-// bf16 bits of x (round to nearest even); x finite.
-__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -354,48 +349,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after_sync();
+      const uint32_t s_col = t_lane + (uint32_t)(t & 1) * 128u;
+      {  // E over the kept keys of this tile, from the same logits as the LSE pass: a kept
+         // key's column is the same for the whole warp, so it is read straight from TMEM,
+         // eight columns per load-and-wait
+        int k_end = kk;
+        while (k_end < u.m && sKeep[k_end] < (t + 1) * kTcKeys) ++k_end;
+        for (int k0 = kk; k0 < k_end; k0 += 8) {
+          uint32_t a[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int k = min(k0 + e, k_end - 1);
+            a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
+          }
+          float ev[8];
+          tmem_ld1x8(a, ev);
+          if (i < meta.R) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (k0 + e < k_end) Erow[k0 + e] = exp2f(fmaf(ev[e], c2, -cc));
+          }
+        }
+        kk = k_end;
+      }
       float v[128];
-      tmem_ld128(t_lane + (uint32_t)(t & 1) * 128u, v);
+      tmem_ld128(s_col, v);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[t & 1]);
-      const int nvalid = min(kTcKeys, u.n - t * kTcKeys);
-      {  // E over the kept keys of this tile, from the same logits as the LSE pass
-        uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;  // kept columns of the tile
-        const int k0 = kk;
-        while (kk < u.m && sKeep[kk] < (t + 1) * kTcKeys) {
-          const int col = sKeep[kk] - t * kTcKeys;
-          const uint32_t bit = col >= 0 ? 1u << (col & 31) : 0u;
-          const int w = col >> 5;
-          m0 |= w == 0 ? bit : 0u;
-          m1 |= w == 1 ? bit : 0u;
-          m2 |= w == 2 ? bit : 0u;
-          m3 |= w == 3 ? bit : 0u;
-          ++kk;
-        }
-        if (i < meta.R && kk > k0) {
-          int k = k0;
+      const int nvalid = u.n - t * kTcKeys;
+      if (nvalid < kTcKeys) {  // keys past the segment: p = 0
 #pragma unroll
-          for (int jj = 0; jj < kTcKeys; ++jj) {
-            const uint32_t mw = jj < 32 ? m0 : jj < 64 ? m1 : jj < 96 ? m2 : m3;
-            if ((mw >> (jj & 31)) & 1u) Erow[k++] = exp2f(fmaf(v[jj], c2, -cc));
-          }
-        }
+        for (int jj = 0; jj < kTcKeys; ++jj)
+          if (jj >= nvalid) v[jj] = -INFINITY;
       }
       ok = mbar_wait(p_empty, (t & 1) ^ 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after_sync();
+      const float2 cc2 = make_float2(c2, c2), nl2 = make_float2(-lse2, -lse2), neg = make_float2(-1.0f, -1.0f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 keys: 16 packed pairs per half
+      for (int c = 0; c < 4; ++c) {  // 32 keys: 16 packed pairs into each of P_hi and P_lo
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int j0 = c * 32 + 2 * e;
-          const float p0 = j0 < nvalid ? ex2_approx(fmaf(v[j0], c2, -lse2)) : 0.0f;
-          const float p1 = j0 + 1 < nvalid ? ex2_approx(fmaf(v[j0 + 1], c2, -lse2)) : 0.0f;
-          const uint32_t h0 = bf16_rn_bits(p0), h1 = bf16_rn_bits(p1);
-          hi[e] = h0 | (h1 << 16);
-          lo[e] = bf16_rn_bits(p0 - __uint_as_float(h0 << 16)) | (bf16_rn_bits(p1 - __uint_as_float(h1 << 16)) << 16);
+          const float2 x = __ffma2_rn(make_float2(v[j0], v[j0 + 1]), cc2, nl2);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          const __nv_bfloat162 h = __float22bfloat162_rn(p);  // .x (the low half) is the even key
+          const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+          const float2 hf = make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
+          const __nv_bfloat162 l = __float22bfloat162_rn(__ffma2_rn(hf, neg, p));  // p - hi, rounded
+          hi[e] = hb;
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
         }
         tmem_st16(t_lane + kColP + c * 16, hi);
         tmem_st16(t_lane + kColPlo + c * 16, lo);

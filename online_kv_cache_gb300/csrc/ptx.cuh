@@ -233,6 +233,29 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Loads one 32-bit column of this thread's TMEM lane at each of eight column
+// addresses (shape 32x32b, .x1, warp-collective: each address must be the same
+// across the warp) and waits for all eight in the same statement, so no use of
+// a value can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld1x8(const uint32_t (&a)[8], float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%8];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%9];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%2}, [%10];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%3}, [%11];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%4}, [%12];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%5}, [%13];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%6}, [%14];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%7}, [%15];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Loads 32 consecutive fp32 columns of this thread's TMEM lane and waits for them.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
