@@ -14,19 +14,20 @@
 // T sweeps over the kept keys in ascending position order; every logit of a
 // unit is shifted by c = max_i LSE_i, which changes neither minimiser.
 //
-// The targets (the full attention output over all n keys, the one contraction
-// of the size of the scoring passes) run on the tensor cores with bf16 Q, K and
-// V exactly as stored and the probabilities split into two bf16 parts; the
-// rest is fp32 on the CUDA cores: the fits are ill-conditioned (exp of
-// logits), so their Gram matrices cannot take the 8-bit-mantissa rounding of a
-// bf16 or tf32 tensor-core contraction.  Per unit the kernels run
+// The contractions run on the tensor cores: the targets (the full attention
+// output over all n keys) with bf16 Q, K and V exactly as stored and the
+// probabilities split into two bf16 parts; the Gram products, which the
+// ill-conditioned fits need to fp32 accuracy (a single bf16 or tf32 rounding
+// would put ~1e-3 into them), with every fp32 operand split into three bf16
+// parts.  The coordinate descents are fp32 on the CUDA cores.  Per unit the
+// kernels run
 //   (scoring LSE pass) LSE_i over all n keys, the rows' log-sum-exp
 //   am_targets_tc_kernel  Y = softmax(L) V over all n keys on the tensor cores
 //                      and E = exp(L_C - c) over the kept keys, s = exp(LSE - c)
-//   am_atb_kernel      G = E^T [E | s]              (mode 0)
+//   am_atb_tc_kernel   G = E^T [E | s]              (mode 0, tensor cores)
 //   am_mass_kernel     w by projected coordinate descent; beta = ln w
 //   am_probs_kernel    Ph = rows of E diag(w), normalised (in place)
-//   am_atb_kernel      H = Ph^T Ph, Bm = Ph^T Y     (modes 1, 2)
+//   am_atb_tc_kernel   H = Ph^T Ph, Bm = Ph^T Y     (modes 1, 2)
 //   am_value_kernel    V_C by coordinate descent; written to the pool (bf16)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -443,27 +444,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------ A^T B
-// Block = (unit, 128 x 128 tile of C): C[p][q] = sum_i A[i][p] B[i][q] over the
-// R proxy rows, 16 rows per step through shared memory; each thread holds an
-// 8 x 8 sub-tile (rows ty*4 + {0..3, 64..67}, columns tx*4 + {0..3, 64..67}) and
-// reads its operands with 128-bit shared loads (4 loads per 64 multiply-adds).
+// ------------------------------------------------------------------ A^T B on the tensor cores
+// C[p][q] = sum_i A[i][p] B[i][q] over the R proxy rows, for the three Gram
+// products of the fits:
 //   mode 0: A = E (m columns), B = [E | s] (m + 1), C = G        (stride ldE)
 //   mode 1: A = B = Ph (m columns),                 C = H in G's place
 //   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d)
-constexpr int kAtbTile = 128;
+// on tcgen05 with fp32-level accuracy: every fp32 value
+// x is split into three bf16 parts (x0 = bf16(x), x1 = bf16(x - x0),
+// x2 = bf16(x - x0 - x1): 8 + 8 + 8 significant bits, x0 + x1 + x2 = x to the
+// last bit of x's significand), and the six part products whose weight is
+// above 2^-24 are accumulated in fp32 in TMEM: a0b0 + a0b1 + a1b0 + a1b1 +
+// a0b2 + a2b0 (each product of two 8-bit significands is exact).  Block =
+// (unit, 128 p, 128 q), 256 threads: per chunk of 64 rows every thread loads
+// 8 consecutive fp32 values at a time, splits them with the packed fp32->bf16x2
+// conversion and writes the parts into shared memory as MN-major operands
+// (1024-byte atoms of 8 rows x 64 elements along p or q: LBO = 1024 B along
+// p/q, SBO = 2048 B along the rows); thread 0 issues the chunk's 24 MMAs
+// (M = N = 128, K = 16, both operands MN-major).  Two chunk buffers: the
+// conversion of chunk c + 1 overlaps the MMAs of chunk c.
+constexpr int kTbThreads = 256;
+constexpr int kTbRows = 64;                                // proxy rows per chunk
+constexpr int kTbPart = kTbRows * 128 * 2;                 // one bf16 part of one operand: 16 KB
+constexpr int kTbBuf = 6 * kTbPart;                        // A0 A1 A2 B0 B1 B2
+constexpr int kTbSmem = 1024 + 1024 + 2 * kTbBuf;          // head, alignment slack, two buffers
+static_assert(kTbSmem <= 227 * 1024, "two chunk buffers fit one CTA's shared memory");
 
-__global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, float* ws, int mode) {
-  __shared__ __align__(16) float As[16][kAtbTile];
-  __shared__ __align__(16) float Bs[16][kAtbTile];
-  const int mt = (meta.max_m + kAtbTile - 1) / kAtbTile;
-  const int nt = mode == 2 ? (meta.d + kAtbTile - 1) / kAtbTile : (meta.max_m + 1 + kAtbTile - 1) / kAtbTile;
+__device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
+  const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(a, b));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kTbThreads, 1)
+    am_atb_tc_kernel(const AmMeta meta, float* ws, int mode, unsigned* status) {
+  extern __shared__ __align__(16) uint8_t tb_smem[];
+  uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [2] a buffer's MMAs are done
+  uint64_t* fin = done + 2;                                // every MMA is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tb_smem + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* bufs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tb_smem) + 1024 + 1023) &
+                                             ~uintptr_t(1023));
+  const int mt = (meta.max_m + 127) / 128;
+  const int nt = mode == 2 ? (meta.d + 127) / 128 : (meta.max_m + 1 + 127) / 128;
   const int ni = (int)(blockIdx.x % nt);
   const int mi = (int)((blockIdx.x / nt) % mt);
   const AmUnit u = am_unit(meta, blockIdx.x / ((int64_t)nt * mt), ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
-  const int p0 = mi * kAtbTile, q0 = ni * kAtbTile;
+  const int p0 = mi * 128, q0 = ni * 128;
   if (p0 >= M || q0 >= N) return;
   const float* A = u.base;
   const int lda = u.ldE;
@@ -471,48 +499,116 @@ __global__ void __launch_bounds__(kAmThreads) am_atb_kernel(const AmMeta meta, f
   const int ldb = mode == 2 ? meta.d : u.ldE;
   float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
   const int ldc = mode == 2 ? meta.d : u.ldE;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  float acc[8][8];
-#pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
-  for (int i0 = 0; i0 < meta.R; i0 += 16) {
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {  // 16 x 128 of A and of B, consecutive threads along a row
-      const int e = threadIdx.x + r * kAmThreads;
-      const int ii = e >> 7, pp = e & 127;
-      const bool in = i0 + ii < meta.R;
-      As[ii][pp] = (in && p0 + pp < M) ? A[(int64_t)(i0 + ii) * lda + p0 + pp] : 0.0f;
-      Bs[ii][pp] = (in && q0 + pp < N) ? B[(int64_t)(i0 + ii) * ldb + q0 + pp] : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[i][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[i][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[i][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[i][64 + tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
-    }
-    __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&done[0], 1);
+    mbar_init(&done[1], 1);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-#pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const int p = p0 + (a < 4 ? ty * 4 + a : 64 + ty * 4 + a - 4);
-    if (p >= M) continue;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int qq = q0 + (b < 4 ? tx * 4 + b : 64 + tx * 4 + b - 4);
-      if (qq < N) C[(int64_t)p * ldc + qq] = acc[a][b];
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, 128);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  // both operands MN-major (transpose bits), bf16 x bf16 -> fp32, M = N = 128
+  const uint32_t idesc = idesc_bf16_f32(128, 128) | (1u << 15) | (1u << 16);
+  const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
+  bool ok = true;
+  for (int c = 0; c < nchunks && ok; ++c) {
+    uint8_t* buf = bufs + (c & 1) * kTbBuf;
+    if (c >= 2) {  // the MMAs of chunk c - 2 have read this buffer
+      ok = mbar_wait(&done[c & 1], ((c >> 1) - 1) & 1, abort_flag, status);
+      if (!__syncthreads_and(ok)) { ok = false; break; }
     }
+    const int i0 = c * kTbRows;
+#pragma unroll 2
+    for (int e = 0; e < 8; ++e) {  // 2 operands x 64 rows x 16 groups of 8 columns, 8 per thread
+      const int w = threadIdx.x + e * kTbThreads;
+      const int op = w >> 10, r = (w >> 4) & 63, g = w & 15;
+      const float* X = op ? B : A;
+      const int ld = op ? ldb : lda;
+      const int ncol = op ? N : M;
+      const int col = (op ? q0 : p0) + g * 8;
+      float x[8];
+      const int i = i0 + r;
+      if (i < meta.R && col + 8 <= ncol) {
+        const float4 v0 = *reinterpret_cast<const float4*>(X + (int64_t)i * ld + col);
+        const float4 v1 = *reinterpret_cast<const float4*>(X + (int64_t)i * ld + col + 4);
+        x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+        x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = (i < meta.R && col + t < ncol) ? X[(int64_t)i * ld + col + t] : 0.0f;
+      }
+      uint32_t h0[4], h1[4], h2[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float a = x[2 * t], b = x[2 * t + 1];
+        h0[t] = bf2_bits(a, b);
+        const float ra = a - __uint_as_float(h0[t] << 16), rb = b - __uint_as_float(h0[t] & 0xFFFF0000u);
+        h1[t] = bf2_bits(ra, rb);
+        h2[t] = bf2_bits(ra - __uint_as_float(h1[t] << 16), rb - __uint_as_float(h1[t] & 0xFFFF0000u));
+      }
+      // MN-major atom layout: row r, 8 elements at g * 8 along p / q
+      const int off = (r >> 3) * 2048 + (g >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
+      uint8_t* base = buf + op * 3 * kTbPart + off;
+      *reinterpret_cast<uint4*>(base) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+      *reinterpret_cast<uint4*>(base + kTbPart) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+      *reinterpret_cast<uint4*>(base + 2 * kTbPart) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the parts, for the tensor cores
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after_sync();
+      const uint32_t a = smem_u32(buf), b = a + 3 * kTbPart;
+      const int pa[6] = {0, 0, 1, 1, 0, 2}, pb[6] = {0, 1, 0, 1, 2, 0};
+#pragma unroll
+      for (int ks = 0; ks < kTbRows / 16; ++ks) {  // 16 rows = two 8-row atom groups
+#pragma unroll
+        for (int pr = 0; pr < 6; ++pr) {
+          const uint64_t da = sdesc_mn_sw128(a + pa[pr] * kTbPart + ks * 2 * 2048, 1024, 2048);
+          const uint64_t db = sdesc_mn_sw128(b + pb[pr] * kTbPart + ks * 2 * 2048, 1024, 2048);
+          mma_bf16(tmem, da, db, idesc, (c > 0 || ks > 0 || pr > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(&done[c & 1]);
+    }
+  }
+  if (threadIdx.x == 0) mma_commit(fin);  // covers every MMA issued (also after an abort)
+  const bool fin_ok = mbar_wait(fin, 0, nullptr, status);
+  if (ok && fin_ok) {
+    tc_fence_after_sync();
+    const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; columns [64 half, 64 half + 64)
+    const int pr = p0 + q4 * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(half * 64);
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+      float y[32];
+      tmem_ld32(t_lane + cc, y);
+      if (pr < M) {
+        float* dst = C + (int64_t)pr * ldc + q0 + half * 64 + cc;
+        const int qb = q0 + half * 64 + cc;
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (qb + t < N) dst[t] = y[t];
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, 128);
   }
 }
+
+constexpr int kAtbTile = 128;  // output tile of the A^T B products (grid sizing)
 
 // ------------------------------------------------------------------ row ring
 // The descents read one row of a Gram matrix per step.  Rows stream from L2
@@ -769,6 +865,7 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set[dev]) {
     if ((e = set_smem(am_targets_tc_kernel<D>, tc_smem_bytes<D>())) != cudaSuccess) return e;
+    if ((e = set_smem(am_atb_tc_kernel, kTbSmem)) != cudaSuccess) return e;
     if ((e = set_smem(am_mass_kernel, mass_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
     if ((e = set_smem(am_value_kernel<D>, value_smem_bytes(kAmMaxM))) != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
@@ -787,16 +884,17 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if ((e = check()) != cudaSuccess) return e;
     const int mt128 = (m.max_m + kAtbTile - 1) / kAtbTile;
     const int nt0 = (m.max_m + 1 + kAtbTile - 1) / kAtbTile;
-    am_atb_kernel<<<(unsigned)(m.units * mt128 * nt0), kAmThreads, 0, stream>>>(m, al.ws, 0);
+    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * nt0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_kernel<<<(unsigned)(m.units * mt128 * nt0), kAmThreads, 0, stream>>>(m, al.ws, 1);
+    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * nt0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 1, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_kernel<<<(unsigned)(m.units * mt128 * ((D + kAtbTile - 1) / kAtbTile)), kAmThreads, 0, stream>>>(m, al.ws, 2);
+    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * ((D + 127) / 128)), kTbThreads, kTbSmem, stream>>>(m, al.ws, 2,
+                                                                                              al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kValueCols)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);
