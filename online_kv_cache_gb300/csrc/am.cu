@@ -610,96 +610,162 @@ __global__ void __launch_bounds__(kTbThreads, 1)
 
 constexpr int kAtbTile = 128;  // output tile of the A^T B products (grid sizing)
 
-// ------------------------------------------------------------------ row ring
-// The descents read one row of a Gram matrix per step.  Rows stream from L2
-// into a ring of kRing shared-memory buffers, kAhead = kRing - 2 steps ahead
-// of use.  The buffer refilled at step st was last read at step st - 2, and
-// every thread has passed step st - 1's barriers before it issues the copy,
-// so no copy lands in a buffer that is still being read.  (Two buffers with
-// the copy one step ahead would refill the buffer of step st - 1 while slower
-// threads may still be reading it.)  Deeper rings (4, 6 buffers) measured no
-// faster.
-constexpr int kRing = 3;
-constexpr int kAhead = kRing - 2;
+// ------------------------------------------------------------------ blocked descents
+// Both fits are cyclic coordinate descents on normal equations: a step on
+// coordinate j reads gradient row j, moves x_j, and adds the move times row j
+// of the Gram matrix (its column j) to every gradient row.  The kernels take
+// the coordinates 32 at a time, in the same order, and split each block of 32
+// steps between the warps:
+//   * warp 0 runs the 32 steps, keeping the block's own 32 gradient rows
+//     current after every step from the block's 32 x 32 diagonal tile;
+//   * meanwhile warps 1-7 add the previous block's moves to the other rows,
+//     g_i += sum_t M[jp + t][i] dx_t in step order (one pass over the previous
+//     block's 32 rows of M, coalesced along i; none when nothing moved), and
+//     stage the next block's tiles with cp.async.  The current block's own
+//     rows get the previous block's moves first, from a staged 32 x 32 cross
+//     tile, and a named barrier then releases warp 0.
+// Every step sees the gradient of the one-coordinate-at-a-time descent, and
+// every gradient entry receives the same fused multiply-adds in the same order.
+constexpr int kDb = 32;                    // coordinates per block: one warp's lanes
+constexpr int kTileLd = 36;                // row stride of a staged tile (floats, 16-byte rows)
+constexpr int kTile = kDb * kTileLd;       // one staged tile
+constexpr int kHelpers = kAmThreads - 32;  // warps 1-7
 
-struct RowRing {
-  float* rows;      // [kRing][m] shared
-  const float* Mx;  // the Gram matrix, leading dimension ld
-  int64_t ld;
-  int m;
-  int row = 0, buf = 0;  // row and buffer of the next copy
-  // Issue the next row's copy when `live`; commit a group either way, so that
-  // group k always belongs to step k.
-  __device__ __forceinline__ void issue(bool live) {
-    if (live) {
-      const float* src = Mx + (int64_t)row * ld;
-      float* dst = rows + buf * m;
-      for (int i = threadIdx.x; i < m; i += kAmThreads) cp_async_4(dst + i, src + i);
-    }
-    cp_async_commit();
-    row = (row + 1 == m) ? 0 : row + 1;
-    buf = (buf + 1 == kRing) ? 0 : buf + 1;
+// tile[t][k] = M[r0 + t][c0 + k] for t < nr, k < nc, zero elsewhere (16-byte
+// cp.async; rows of M 16-byte aligned), spread over threads tid of nthr.
+__device__ __forceinline__ void stage_tile(float* tile, const float* M, int64_t ld, int r0, int nr, int c0, int nc,
+                                           int tid, int nthr) {
+  for (int e = tid; e < kDb * (kDb / 4); e += nthr) {
+    const int t = e >> 3, q = e & 7;
+    const int valid = t < nr ? max(0, min(4, nc - 4 * q)) : 0;
+    const float* src = valid > 0 ? M + (int64_t)(r0 + t) * ld + c0 + 4 * q : M;
+    cp_async_16z(tile + t * kTileLd + 4 * q, src, valid * 4);
   }
-};
+}
 
 // ------------------------------------------------------------------ mass fit
 // Block = unit.  Projected cyclic coordinate descent on min_{w >= 0} ||E w - s||^2
 // from w = 1: with g = G w - b, coordinate j moves to max(0, w_j - g_j / G_jj)
-// and g follows by the change times column j of G (= row j, G symmetric).
-// Coordinate j moves only when |g_j| > 2^-17 b_j (every term of G w and of
-// b = E^T s is >= 0, so b_j is their scale).  Rows of G stream through the
-// row ring.  Two barriers per step: every thread reads g_j and w_j before any
-// of them is updated.
-// Writes w (workspace), beta = ln w (-inf at 0) to `beta` and to the per-slot
-// state of each kept entry.
+// and g follows by the change times row j of G (G symmetric).  Coordinate j
+// moves only when |g_j| > 2^-17 b_j (every term of G w and of b = E^T s is
+// >= 0, so b_j is their scale).  In a block's steps lane k of warp 0 holds
+// coordinate j0 + k; the coordinate of step t broadcasts its gradient by
+// shuffle.  Writes w (workspace), beta = ln w (-inf at 0) to `beta` and to the
+// per-slot state of each kept entry.
+constexpr int kMassHead = 2 * kDb + 4 * kTile + 4;  // moves [2][32], tiles [2][diag, cross], flags
+__host__ __device__ constexpr int mass_smem_bytes(int m) { return (kMassHead + 4 * m) * 4; }
+
 __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
                                                              const int32_t* __restrict__ keep, float* ws,
                                                              float* aux, float* beta, unsigned* status) {
   extern __shared__ __align__(16) float am_smem[];
   const AmUnit u = am_unit(meta, blockIdx.x, ws);
   const int m = u.m;
-  float* g = am_smem;         // [m]
-  float* w = g + m;           // [m]
-  float* diag = w + m;        // [m]
-  float* bvec = diag + m;     // [m] b = E^T s
-  float* rows = bvec + m;     // [kRing][m]
+  if (m <= 0) return;
+  float* dws = am_smem;                                       // [2][32] moves of the last two blocks
+  float* tiles = dws + 2 * kDb;                               // [2][2][kTile]
+  int* moved = reinterpret_cast<int*>(tiles + 4 * kTile);     // [2] did that block move
+  float* g = am_smem + kMassHead;                             // [m] gradient G w - b
+  float* w = g + m;                                           // [m]
+  float* thr = w + m;                                         // [m] 2^-17 b_j; +inf where G_jj <= 0
+  float* diag = thr + m;                                      // [m] G_jj
   const float* G = u.base + am_off_G(meta.R, u.ldE);
+  const int64_t ld = u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < m; i += kAmThreads / 32) {  // g = G 1 - b, one warp per row
-    const float* gr = G + (int64_t)i * u.ldE;
+    const float* gr = G + (int64_t)i * ld;
     float acc = 0.0f;
     for (int k = lane; k < m; k += 32) acc += gr[k];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
-      g[i] = acc - gr[m];
-      bvec[i] = gr[m];
-      diag[i] = gr[i];
+      const float b = gr[m], d = gr[i];
+      g[i] = acc - b;
       w[i] = 1.0f;
+      thr[i] = d > 0.0f ? kAmGuard * b : INFINITY;
+      diag[i] = d;
     }
   }
-  const int64_t steps = (int64_t)meta.sweeps * m;
-  RowRing ring{rows, G, u.ldE, m};
-  for (int p = 0; p < kAhead; ++p) ring.issue(p < steps);
-  int j = 0, cb = 0;  // step st's row and ring buffer
-  for (int64_t st = 0; st < steps; ++st) {
-    ring.issue(st + kAhead < steps);
-    cp_async_wait_group<kAhead>();  // this thread's copies of step st's row are in
-    __syncthreads();
-    const float gj = g[j], wj = w[j], Gjj = diag[j];
-    const float nw = (Gjj > 0.0f && fabsf(gj) > kAmGuard * bvec[j]) ? fmaxf(0.0f, wj - gj / Gjj) : wj;
-    const float dl = nw - wj;
-    __syncthreads();
-    if (dl != 0.0f) {
-      const float* rj = rows + cb * m;
-      for (int i = threadIdx.x; i < m; i += kAmThreads) g[i] = fmaf(dl, rj[i], g[i]);
-      if (threadIdx.x == 0) w[j] = nw;
-    }
-    j = (j + 1 == m) ? 0 : j + 1;
-    cb = (cb + 1 == kRing) ? 0 : cb + 1;
-  }
+  if (threadIdx.x < 2) moved[threadIdx.x] = 0;
+  const int nb = (m + kDb - 1) / kDb;
+  stage_tile(tiles, G, ld, 0, min(kDb, m), 0, min(kDb, m), threadIdx.x, kAmThreads);  // block 0's diagonal
+  cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
+  const int64_t iters = (int64_t)meta.sweeps * nb;
+  int jp = 0, cntp = 0;  // the previous block
+  for (int64_t it = 0; it < iters; ++it) {
+    const int cur = (int)(it & 1), prev = cur ^ 1;
+    const int j0 = (int)(it % nb) * kDb, cnt = min(kDb, m - j0);
+    const float* dtile = tiles + cur * 2 * kTile;  // diag[t][k] = G[j0 + t][j0 + k]
+    const float* ctile = dtile + kTile;            // cross[t][k] = G[jp + t][j0 + k]
+    if (warp == 0) {
+      bar_sync_n(1, kAmThreads);  // the block's rows have the previous block's moves
+      const bool v = lane < cnt;
+      const int j = j0 + lane;
+      float gk = v ? g[j] : 0.0f;
+      const float w0 = v ? w[j] : 0.0f, tk = v ? thr[j] : INFINITY, dk = v ? diag[j] : 1.0f;
+      float wk = w0, dwk = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kDb; ++t) {
+        if (t >= cnt) break;
+        const float gt = __shfl_sync(0xffffffffu, gk, t);
+        const float wt = __shfl_sync(0xffffffffu, w0, t);  // w of coordinate t before its own step
+        const float tt = __shfl_sync(0xffffffffu, tk, t);
+        const float dt = __shfl_sync(0xffffffffu, dk, t);
+        const float nw = fabsf(gt) > tt ? fmaxf(0.0f, wt - gt / dt) : wt;
+        const float dl = nw - wt;
+        if (dl != 0.0f) {
+          gk = fmaf(dl, dtile[t * kTileLd + lane], gk);
+          if (lane == t) {
+            wk = nw;
+            dwk = dl;
+          }
+        }
+      }
+      if (v) {
+        g[j] = gk;
+        w[j] = wk;
+      }
+      dws[cur * kDb + lane] = dwk;
+      const bool any = __any_sync(0xffffffffu, dwk != 0.0f);
+      if (lane == 0) moved[cur] = any ? 1 : 0;
+    } else {
+      const int tid = threadIdx.x - 32;
+      const float* dwp = dws + prev * kDb;
+      const bool apply = moved[prev] != 0 && nb > 1;
+      if (apply && warp == 1 && lane < cnt) {  // the block's own rows, from the cross tile
+        float acc = g[j0 + lane];
+        for (int t = 0; t < cntp; ++t) acc = fmaf(dwp[t], ctile[t * kTileLd + lane], acc);
+        g[j0 + lane] = acc;
+      }
+      bar_arrive_n(1, kAmThreads);
+      if (apply) {  // every other row, from the previous block's rows of G
+        for (int i = tid; i < m; i += kHelpers) {
+          if ((i >= jp && i < jp + cntp) || (i >= j0 && i < j0 + cnt)) continue;
+          float h[kDb];
+#pragma unroll
+          for (int t = 0; t < kDb; ++t) h[t] = t < cntp ? G[(int64_t)(jp + t) * ld + i] : 0.0f;
+          float acc = g[i];
+#pragma unroll
+          for (int t = 0; t < kDb; ++t)
+            if (t < cntp) acc = fmaf(dwp[t], h[t], acc);
+          g[i] = acc;
+        }
+      }
+      if (it + 1 < iters) {  // the next block's tiles
+        const int jn = (int)((it + 1) % nb) * kDb, cntn = min(kDb, m - jn);
+        float* nt = tiles + prev * 2 * kTile;
+        stage_tile(nt, G, ld, jn, cntn, jn, cntn, tid, kHelpers);
+        stage_tile(nt + kTile, G, ld, j0, cnt, jn, cntn, tid, kHelpers);
+        cp_async_commit();
+        cp_async_wait_all();
+      }
+    }
+    jp = j0;
+    cntp = cnt;
+    __syncthreads();
+  }
   float* wout = u.base + am_off_w(meta.R, m, u.ldE, meta.d);
   const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
   for (int j = threadIdx.x; j < m; j += kAmThreads) {
@@ -734,114 +800,236 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
   for (int j = lane; j < u.m; j += 32) E[j] = E[j] * w[j] * inv;
 }
 
-constexpr int kValueCols = 8;  // value-fit columns per block (32 row slices x 8 columns)
-
-__host__ __device__ constexpr int value_smem_bytes(int m) {
-  return (2 * m * kValueCols + (2 + kRing) * m + (kAmThreads / kValueCols + 1) * kValueCols) * 4;
-}
-__host__ __device__ constexpr int mass_smem_bytes(int m) { return (4 + kRing) * m * 4; }
+// ------------------------------------------------------------------ value fit
+// Block = (unit, 16 of the d value columns).  The columns are independent
+// least-squares problems sharing H = Ph^T Ph: cyclic coordinate descent from
+// X = the kept values with gradient Gv = H X - Bm (shared memory, column-major
+// with an odd stride); row j of X moves by -Gv_j / H_jj when |Gv_jc| > 2^-17
+// pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic| + max_k |X0_kc|: the scale
+// of the gradient's terms in column c).  In a block's steps lane c of warp 0
+// holds column c of the block's 32 gradient rows; the diagonal tile's row t
+// is read as a broadcast.  X lives in the workspace in Bm's place (Bm is read
+// once into the gradient).  At the end V_C is written to `vc` (fp32) and over
+// the kept entries' V rows (bf16, round to nearest even).
+constexpr int kVc = 16;  // value columns per block
+__host__ __device__ constexpr int value_ld(int m) { return m | 1; }
+constexpr int kValueHead = 2 * kDb * kVc + 4 * kTile + 2 * kVc + 4;  // moves, tiles, scales, flags
+__host__ __device__ constexpr int value_smem_bytes(int m) { return (kValueHead + kVc * value_ld(m) + 2 * m) * 4; }
 static_assert(value_smem_bytes(kAmMaxM) <= 227 * 1024 && mass_smem_bytes(kAmMaxM) <= 227 * 1024,
               "descent working sets fit one CTA's shared memory at the largest m");
+static_assert(kValueHead % 4 == 0 && kMassHead % 4 == 0, "the per-row arrays start 16-byte aligned");
 
-// ------------------------------------------------------------------ value fit
-// Block = (unit, 8 of the d value columns).  The columns are independent
-// least-squares problems sharing H = Ph^T Ph: cyclic coordinate descent from
-// X = the kept values, gradient Gv = H X - Bm kept in shared memory; row j of
-// X moves by -Gv_j / H_jj and Gv follows by column j of H (= row j) times the
-// change, when |Gv_jc| > 2^-17 pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic|
-// + max_k |X0_kc|: the scale of the gradient's terms in column c).  Rows of H
-// stream through the row ring.  At the end V_C is
-// written to `vc` (fp32) and over the kept entries' V rows (bf16, round to
-// nearest even).
+// Gs[c][i] += sum_{t < cnt} M[j0 + t][i] dxs[t][c], t in step order, for the
+// rows i outside [e0, e1) and [f0, f1); one thread (tid of nthr) per row.
+__device__ __forceinline__ void value_update(const float* __restrict__ M, int64_t ld, int m, int ldv, int j0, int cnt,
+                                             const float* dxs, float* Gs, int e0, int e1, int f0, int f1, int tid,
+                                             int nthr) {
+  for (int i = tid; i < m; i += nthr) {
+    if ((i >= e0 && i < e1) || (i >= f0 && i < f1)) continue;
+    float h[kDb];
+#pragma unroll
+    for (int t = 0; t < kDb; ++t) h[t] = t < cnt ? M[(int64_t)(j0 + t) * ld + i] : 0.0f;
+    float acc[kVc];
+#pragma unroll
+    for (int c = 0; c < kVc; ++c) acc[c] = Gs[c * ldv + i];
+#pragma unroll
+    for (int t = 0; t < kDb; ++t) {
+      if (t >= cnt) break;
+      const float4* d4 = reinterpret_cast<const float4*>(dxs + t * kVc);
+#pragma unroll
+      for (int q = 0; q < kVc / 4; ++q) {
+        const float4 d = d4[q];
+        acc[4 * q + 0] = fmaf(h[t], d.x, acc[4 * q + 0]);
+        acc[4 * q + 1] = fmaf(h[t], d.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(h[t], d.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(h[t], d.w, acc[4 * q + 3]);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kVc; ++c) Gs[c * ldv + i] = acc[c];
+  }
+}
+
+// X[j0 + t][col0 + c] += dxs[t][c]: the moves of a block's steps into X.
+__device__ __forceinline__ void value_moves(float* X, int ld, int col0, int j0, int cnt, const float* dxs, int tid,
+                                            int nthr) {
+  for (int e = tid; e < cnt * kVc; e += nthr) {
+    const int t = e / kVc, c = e % kVc;
+    X[(int64_t)(j0 + t) * ld + col0 + c] += dxs[e];
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kAmThreads) am_value_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
-                                                              const int32_t* __restrict__ keep, uint16_t* vp,
-                                                              float* ws, float* vc, unsigned* status) {
+__global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                                 const int32_t* __restrict__ keep, uint16_t* vp,
+                                                                 float* ws, float* vc, unsigned* status) {
   extern __shared__ __align__(16) float am_smem[];
-  constexpr int kCb = D / kValueCols;
+  constexpr int kCb = D / kVc;
   const AmUnit u = am_unit(meta, blockIdx.x / kCb, ws);
-  const int col0 = (int)(blockIdx.x % kCb) * kValueCols;
+  const int col0 = (int)(blockIdx.x % kCb) * kVc;
   const int m = u.m;
-  float* Gv = am_smem;                 // [m][8]
-  float* X = Gv + m * kValueCols;      // [m][8]
-  float* hdiag = X + m * kValueCols;   // [m]
-  float* pi = hdiag + m;               // [m]
-  float* rows = pi + m;                // [kRing][m]
-  float* red = rows + kRing * m;       // [32][8] partial column scales, then S[8]
+  if (m <= 0) return;
+  const int ldv = value_ld(m);
+  float* dxs = am_smem;                                    // [2][32][kVc] moves of the last two blocks
+  float* tiles = dxs + 2 * kDb * kVc;                      // [2][2][kTile]
+  float* S = tiles + 4 * kTile;                            // [kVc] column scales
+  float* Sx = S + kVc;                                     // [kVc] max |X0| (bits)
+  int* moved = reinterpret_cast<int*>(Sx + kVc);           // [2] did that block move
+  float* Gs = am_smem + kValueHead;                        // [kVc][ldv] gradient, column-major
+  float* hdiag = Gs + kVc * ldv;                           // [m] H_jj
+  float* thrb = hdiag + m;                                 // [m] 2^-17 pi_j; +inf where H_jj <= 0
   const float* Hm = u.base + am_off_G(meta.R, u.ldE);
-  const float* Bm = u.base + am_off_Bm(meta.R, m, u.ldE, D);
-  const int c = threadIdx.x & (kValueCols - 1), r = threadIdx.x / kValueCols;
-  constexpr int kSlices = kAmThreads / kValueCols;
-  for (int j = threadIdx.x; j < m; j += kAmThreads) {  // start: the kept entries' values
+  const int64_t ld = u.ldE;
+  float* Xg = u.base + am_off_Bm(meta.R, m, u.ldE, D);    // Bm, then X (row stride D)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < m; i += kAmThreads / 32) {  // H_jj and pi_j, one warp per row
+    const float* hr = Hm + (int64_t)i * ld;
+    float ps = 0.0f;
+    for (int k = lane; k < m; k += 32) ps += hr[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    if (lane == 0) {
+      const float d = hr[i];
+      hdiag[i] = d;
+      thrb[i] = d > 0.0f ? kAmGuard * ps : INFINITY;
+    }
+  }
+  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {  // Gv = -Bm to start
+    const int i = e / kVc, c = e % kVc;
+    Gs[c * ldv + i] = -Xg[(int64_t)i * D + col0 + c];
+  }
+  if (threadIdx.x < 2 * kVc) S[threadIdx.x] = 0.0f;  // S: max |Y| bits, Sx: max |X0| bits
+  if (threadIdx.x < 2) moved[threadIdx.x] = 0;
+  __syncthreads();
+  {
+    const int c = threadIdx.x % kVc;
+    const float* Y = u.base + am_off_Y(meta.R, m, u.ldE);
+    float ym = 0.0f;
+    for (int i = threadIdx.x / kVc; i < meta.R; i += kAmThreads / kVc)
+      ym = fmaxf(ym, fabsf(Y[(int64_t)i * D + col0 + c]));
+    atomicMax(reinterpret_cast<int*>(S) + c, __float_as_int(ym));  // non-negative floats order as ints
+  }
+  for (int j = threadIdx.x; j < m; j += kAmThreads) {  // X = the kept entries' values
     const int pos = am_kept(meta, u, keep, j, status);
     const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
-    float v[8];
+    float v[kVc];
     if (row >= 0) {
       unpack8(*reinterpret_cast<const uint4*>(vp + row * D + col0), v);
+      unpack8(*reinterpret_cast<const uint4*>(vp + row * D + col0 + 8), v + 8);
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+      for (int e = 0; e < kVc; ++e) v[e] = 0.0f;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) X[j * kValueCols + e] = v[e];
-    hdiag[j] = Hm[(int64_t)j * u.ldE + j];
+    for (int e = 0; e < kVc; ++e) {
+      Xg[(int64_t)j * D + col0 + e] = v[e];
+      atomicMax(reinterpret_cast<int*>(Sx) + e, __float_as_int(fabsf(v[e])));
+    }
   }
   __syncthreads();
-  {  // S_c = max_i |Y_ic| + max_k |X0_kc|
-    const float* Y = u.base + am_off_Y(meta.R, m, u.ldE);
-    float ym = 0.0f, xm = 0.0f;
-    for (int i = r; i < meta.R; i += kSlices) ym = fmaxf(ym, fabsf(Y[(int64_t)i * D + col0 + c]));
-    for (int k = r; k < m; k += kSlices) xm = fmaxf(xm, fabsf(X[k * kValueCols + c]));
-    red[r * kValueCols + c] = ym;
-    __syncthreads();
-    if (r == 0) {
-      for (int t = 1; t < kSlices; ++t) ym = fmaxf(ym, red[t * kValueCols + c]);
+  if (threadIdx.x < kVc) S[threadIdx.x] += Sx[threadIdx.x];
+  const int nb = (m + kDb - 1) / kDb;
+  for (int b = 0; b < nb; ++b) {  // Gv += H X0, 32 coordinates at a time
+    const int j0 = b * kDb, cnt = min(kDb, m - j0);
+    for (int e = threadIdx.x; e < kDb * kVc; e += kAmThreads) {
+      const int t = e / kVc, c = e % kVc;
+      dxs[e] = t < cnt ? Xg[(int64_t)(j0 + t) * D + col0 + c] : 0.0f;
     }
     __syncthreads();
-    red[r * kValueCols + c] = xm;
+    value_update(Hm, ld, m, ldv, j0, cnt, dxs, Gs, 0, 0, 0, 0, threadIdx.x, kAmThreads);
     __syncthreads();
-    if (r == 0) {
-      for (int t = 1; t < kSlices; ++t) xm = fmaxf(xm, red[t * kValueCols + c]);
-      red[kSlices * kValueCols + c] = ym + xm;
-    }
   }
-  for (int i = r; i < m; i += kSlices) {  // Gv = H X - Bm and pi = H 1
-    const float* hr = Hm + (int64_t)i * u.ldE;
-    float acc = 0.0f, ps = 0.0f;
-    for (int k = 0; k < m; ++k) {
-      acc = fmaf(hr[k], X[k * kValueCols + c], acc);
-      ps += hr[k];
-    }
-    Gv[i * kValueCols + c] = acc - Bm[(int64_t)i * D + col0 + c];
-    if (c == 0) pi[i] = ps;
-  }
-  __syncthreads();
-  const float Sc = red[kSlices * kValueCols + c];
-  const int64_t steps = (int64_t)meta.sweeps * m;
-  RowRing ring{rows, Hm, u.ldE, m};
-  for (int p = 0; p < kAhead; ++p) ring.issue(p < steps);
-  int j = 0, cb = 0;  // step st's row and ring buffer
-  for (int64_t st = 0; st < steps; ++st) {
-    ring.issue(st + kAhead < steps);
-    cp_async_wait_group<kAhead>();  // this thread's copies of step st's row are in
-    __syncthreads();
-    const float Hjj = hdiag[j];
-    const float gv = Gv[j * kValueCols + c];
-    const float dl = (Hjj > 0.0f && fabsf(gv) > kAmGuard * pi[j] * Sc) ? -gv / Hjj : 0.0f;
-    __syncthreads();
-    if (dl != 0.0f) {
-      const float* rj = rows + cb * m;
-      for (int i = r; i < m; i += kSlices) Gv[i * kValueCols + c] = fmaf(rj[i], dl, Gv[i * kValueCols + c]);
-      if (r == 0) X[j * kValueCols + c] += dl;
-    }
-    j = (j + 1 == m) ? 0 : j + 1;
-    cb = (cb + 1 == kRing) ? 0 : cb + 1;
-  }
+  stage_tile(tiles, Hm, ld, 0, min(kDb, m), 0, min(kDb, m), threadIdx.x, kAmThreads);  // block 0's diagonal
+  cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
+  const int64_t iters = (int64_t)meta.sweeps * nb;
+  int jp = 0, cntp = 0;  // the previous block
+  for (int64_t it = 0; it < iters; ++it) {
+    const int cur = (int)(it & 1), prev = cur ^ 1;
+    const int j0 = (int)(it % nb) * kDb, cnt = min(kDb, m - j0);
+    const float* dtile = tiles + cur * 2 * kTile;  // diag[t][k] = H[j0 + t][j0 + k]
+    const float* ctile = dtile + kTile;            // cross[t][k] = H[jp + t][j0 + k]
+    float* dxc = dxs + cur * kDb * kVc;
+    const float* dxp = dxs + prev * kDb * kVc;
+    if (warp == 0) {
+      bar_sync_n(1, kAmThreads);  // the block's rows have the previous block's moves
+      const int c = lane & (kVc - 1);
+      const float Sc = S[c];
+      float gv[kDb];
+#pragma unroll
+      for (int t = 0; t < kDb; ++t) gv[t] = t < cnt ? Gs[c * ldv + j0 + t] : 0.0f;
+      bool mv = false;
+#pragma unroll
+      for (int t = 0; t < kDb; ++t) {
+        float dl = 0.0f;
+        if (t < cnt) {
+          const float gt = gv[t];
+          dl = fabsf(gt) > thrb[j0 + t] * Sc ? -gt / hdiag[j0 + t] : 0.0f;
+          if (__any_sync(0xffffffffu, dl != 0.0f)) {
+            mv = true;
+            const float4* t4 = reinterpret_cast<const float4*>(dtile + t * kTileLd);
+#pragma unroll
+            for (int q = 0; q < kDb / 4; ++q) {
+              const float4 h = t4[q];
+              gv[4 * q + 0] = fmaf(h.x, dl, gv[4 * q + 0]);
+              gv[4 * q + 1] = fmaf(h.y, dl, gv[4 * q + 1]);
+              gv[4 * q + 2] = fmaf(h.z, dl, gv[4 * q + 2]);
+              gv[4 * q + 3] = fmaf(h.w, dl, gv[4 * q + 3]);
+            }
+          }
+        }
+        if (lane < kVc) dxc[t * kVc + c] = dl;
+      }
+      if (lane < kVc) {
+#pragma unroll
+        for (int t = 0; t < kDb; ++t)
+          if (t < cnt) Gs[c * ldv + j0 + t] = gv[t];
+      }
+      if (lane == 0) moved[cur] = mv ? 1 : 0;
+    } else {
+      const int tid = threadIdx.x - 32;
+      const bool mvp = moved[prev] != 0;
+      const bool apply = mvp && nb > 1;
+      if (apply && warp <= kVc / 4 && lane < cnt) {  // the block's own rows, four columns per warp
+        const int c0 = (warp - 1) * 4;
+        float acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = Gs[(c0 + q) * ldv + j0 + lane];
+        for (int t = 0; t < cntp; ++t) {
+          const float h = ctile[t * kTileLd + lane];
+          const float4 d = *reinterpret_cast<const float4*>(dxp + t * kVc + c0);
+          acc[0] = fmaf(h, d.x, acc[0]);
+          acc[1] = fmaf(h, d.y, acc[1]);
+          acc[2] = fmaf(h, d.z, acc[2]);
+          acc[3] = fmaf(h, d.w, acc[3]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Gs[(c0 + q) * ldv + j0 + lane] = acc[q];
+      }
+      bar_arrive_n(1, kAmThreads);
+      if (mvp) value_moves(Xg, D, col0, jp, cntp, dxp, tid, kHelpers);
+      if (apply) value_update(Hm, ld, m, ldv, jp, cntp, dxp, Gs, jp, jp + cntp, j0, j0 + cnt, tid, kHelpers);
+      if (it + 1 < iters) {  // the next block's tiles
+        const int jn = (int)((it + 1) % nb) * kDb, cntn = min(kDb, m - jn);
+        float* nt = tiles + prev * 2 * kTile;
+        stage_tile(nt, Hm, ld, jn, cntn, jn, cntn, tid, kHelpers);
+        stage_tile(nt + kTile, Hm, ld, j0, cnt, jn, cntn, tid, kHelpers);
+        cp_async_commit();
+        cp_async_wait_all();
+      }
+    }
+    jp = j0;
+    cntp = cnt;
+    __syncthreads();
+  }
+  if (iters > 0 && moved[(iters - 1) & 1]) value_moves(Xg, D, col0, jp, cntp, dxs + ((iters - 1) & 1) * kDb * kVc,
+                                                        threadIdx.x, kAmThreads);
+  __syncthreads();
   const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
-  for (int j = r; j < m; j += kSlices) {
-    const float x = X[j * kValueCols + c];
+  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
+    const int j = e / kVc, c = e % kVc;
+    const float x = Xg[(int64_t)j * D + col0 + c];
     if (vc != nullptr) vc[(orow + j) * D + col0 + c] = x;
     const int pos = am_kept(meta, u, keep, j, status);
     const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
@@ -896,7 +1084,7 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * ((D + 127) / 128)), kTbThreads, kTbSmem, stream>>>(m, al.ws, 2,
                                                                                               al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_value_kernel<D><<<(unsigned)(m.units * (D / kValueCols)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
+    am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);
     if ((e = check()) != cudaSuccess) return e;
   }

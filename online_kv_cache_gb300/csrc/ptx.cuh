@@ -83,6 +83,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------------------------ named barriers
+// Barrier `id` (1..15) over `n` threads: bar_sync waits for all n, bar_arrive
+// counts the caller and goes on.  Every participant reaches it once per use;
+// the non-aligned forms allow a warp that diverged just before.
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_n(int id, int n) {
+  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ------------------------------------------------------------------ cp.async (4-byte)
 
 // Asynchronous 4-byte global -> shared copy (completion tracked per thread by
@@ -90,6 +101,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
                "l"(reinterpret_cast<uint64_t>(gmem_src))
+               : "memory");
+}
+// Asynchronous 16-byte copy of which only the first `src_bytes` (0..16) are
+// read; the rest of the destination is zero-filled.  Both addresses 16-byte
+// aligned.
+__device__ __forceinline__ void cp_async_16z(void* smem_dst, const void* gmem_src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(src_bytes)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
