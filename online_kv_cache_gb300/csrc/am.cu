@@ -455,20 +455,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // x2 = bf16(x - x0 - x1): 8 + 8 + 8 significant bits, x0 + x1 + x2 = x to the
 // last bit of x's significand), and the six part products whose weight is
 // above 2^-24 are accumulated in fp32 in TMEM: a0b0 + a0b1 + a1b0 + a1b1 +
-// a0b2 + a2b0 (each product of two 8-bit significands is exact).  Block =
-// (unit, 128 p, 128 q), 256 threads: per chunk of 64 rows every thread loads
-// 8 consecutive fp32 values at a time, splits them with the packed fp32->bf16x2
-// conversion and writes the parts into shared memory as MN-major operands
-// (1024-byte atoms of 8 rows x 64 elements along p or q: LBO = 1024 B along
-// p/q, SBO = 2048 B along the rows); thread 0 issues the chunk's 24 MMAs
-// (M = N = 128, K = 16, both operands MN-major).  Two chunk buffers: the
-// conversion of chunk c + 1 overlaps the MMAs of chunk c.
+// a0b2 + a2b0 (each product of two 8-bit significands is exact).
+// Block = (unit, 128 p, 128 q), 256 threads.  G's first m columns and H are
+// symmetric: only tiles with p0 <= q0 run, and each writes its transpose too
+// (a diagonal tile writes its upper triangle and mirrors it), so both
+// triangles hold the same numbers; a diagonal tile stages one strip, which
+// serves as both operands (in mode 0 E's strips are taken over the m + 1
+// columns of [E | s], so that G's column m is in it).  Per chunk of 32 rows the fp32 rows arrive by
+// 16-byte cp.async in a ring of three stages, two chunks ahead; every thread
+// then splits 8 consecutive values at a time with the packed fp32->bf16x2
+// conversion and writes the parts as MN-major operands (1024-byte atoms of 8
+// rows x 64 elements along p or q: LBO = 1024 B along p/q, SBO = 2048 B along
+// the rows); thread 0 issues the chunk's 12 MMAs (M = N = 128, K = 16, both
+// operands MN-major).  Two operand buffers: the split of chunk c + 1 overlaps
+// the MMAs of chunk c.
 constexpr int kTbThreads = 256;
-constexpr int kTbRows = 64;                                // proxy rows per chunk
-constexpr int kTbPart = kTbRows * 128 * 2;                 // one bf16 part of one operand: 16 KB
-constexpr int kTbBuf = 6 * kTbPart;                        // A0 A1 A2 B0 B1 B2
-constexpr int kTbSmem = 1024 + 1024 + 2 * kTbBuf;          // head, alignment slack, two buffers
-static_assert(kTbSmem <= 227 * 1024, "two chunk buffers fit one CTA's shared memory");
+constexpr int kTbRows = 32;                         // proxy rows per chunk
+constexpr int kTbPart = kTbRows * 128 * 2;          // one bf16 part of one operand: 8 KB
+constexpr int kTbBuf = 6 * kTbPart;                 // A0 A1 A2 B0 B1 B2
+constexpr int kTbStageFloats = kTbRows * 256;       // fp32 rows of both strips: A at 0, B at 128
+constexpr int kTbStages = 3;
+constexpr int kTbSmem = 1024 + 1024 + 2 * kTbBuf + kTbStages * kTbStageFloats * 4;  // head, slack, buffers, ring
+static_assert(kTbSmem <= 227 * 1024, "operand buffers and the fp32 ring fit one CTA's shared memory");
 
 __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
   const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(a, b));
@@ -478,16 +486,20 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 __global__ void __launch_bounds__(kTbThreads, 1)
     am_atb_tc_kernel(const AmMeta meta, float* ws, int mode, unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
-  uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [2] a buffer's MMAs are done
+  uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [2] an operand buffer's MMAs are done
   uint64_t* fin = done + 2;                                // every MMA is done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tb_smem + 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* bufs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tb_smem) + 1024 + 1023) &
                                              ~uintptr_t(1023));
+  float* ring = reinterpret_cast<float*>(bufs + 2 * kTbBuf);
   const int mt = (meta.max_m + 127) / 128;
   const int nt = mode == 2 ? (meta.d + 127) / 128 : (meta.max_m + 1 + 127) / 128;
   const int ni = (int)(blockIdx.x % nt);
   const int mi = (int)((blockIdx.x / nt) % mt);
+  const bool sym = mode != 2;
+  if (sym && mi > ni) return;
+  const bool dg = sym && mi == ni;  // diagonal tile: one strip, both operands
   const AmUnit u = am_unit(meta, blockIdx.x / ((int64_t)nt * mt), ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
@@ -500,6 +512,26 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
   const int ldc = mode == 2 ? meta.d : u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nops = dg ? 1 : 2;
+  const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
+  // chunk c's fp32 rows into ring stage c % 3 (zero past R and past the strip's columns)
+  auto load_chunk = [&](int c) {
+    if (c < nchunks) {
+      float* st = ring + (c % kTbStages) * kTbStageFloats;
+      const int i0 = c * kTbRows;
+      for (int e = threadIdx.x; e < nops * kTbRows * 32; e += kTbThreads) {
+        const int op = e >> 10, r = (e >> 5) & (kTbRows - 1), q = e & 31;
+        const float* X = op ? B : A;
+        const int ld = op ? ldb : lda;
+        const int col = (op ? q0 : p0) + 4 * q;
+        const int ncol = op || mode == 0 ? N : M;  // mode 0: A over m + 1 columns too (row m of C is not kept)
+        const int i = i0 + r;
+        const int valid = i < meta.R ? max(0, min(4, ncol - col)) : 0;
+        cp_async_16z(st + r * 256 + op * 128 + 4 * q, valid > 0 ? X + (int64_t)i * ld + col : X, valid * 4);
+      }
+    }
+    cp_async_commit();  // one group per chunk, empty past the end
+  };
   if (threadIdx.x == 0) {
     mbar_init(&done[0], 1);
     mbar_init(&done[1], 1);
@@ -511,40 +543,31 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     __syncwarp();
     tmem_alloc(tmem_slot, 128);
   }
+  load_chunk(0);
+  load_chunk(1);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // both operands MN-major (transpose bits), bf16 x bf16 -> fp32, M = N = 128
   const uint32_t idesc = idesc_bf16_f32(128, 128) | (1u << 15) | (1u << 16);
-  const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
   bool ok = true;
   for (int c = 0; c < nchunks && ok; ++c) {
+    load_chunk(c + 2);
+    cp_async_wait_group<2>();  // this thread's copies of chunk c are in
     uint8_t* buf = bufs + (c & 1) * kTbBuf;
-    if (c >= 2) {  // the MMAs of chunk c - 2 have read this buffer
+    if (c >= 2) {  // the MMAs of chunk c - 2 have read this operand buffer
       ok = mbar_wait(&done[c & 1], ((c >> 1) - 1) & 1, abort_flag, status);
       if (!__syncthreads_and(ok)) { ok = false; break; }
+    } else {
+      __syncthreads();
     }
-    const int i0 = c * kTbRows;
-#pragma unroll 2
-    for (int e = 0; e < 8; ++e) {  // 2 operands x 64 rows x 16 groups of 8 columns, 8 per thread
-      const int w = threadIdx.x + e * kTbThreads;
-      const int op = w >> 10, r = (w >> 4) & 63, g = w & 15;
-      const float* X = op ? B : A;
-      const int ld = op ? ldb : lda;
-      const int ncol = op ? N : M;
-      const int col = (op ? q0 : p0) + g * 8;
-      float x[8];
-      const int i = i0 + r;
-      if (i < meta.R && col + 8 <= ncol) {
-        const float4 v0 = *reinterpret_cast<const float4*>(X + (int64_t)i * ld + col);
-        const float4 v1 = *reinterpret_cast<const float4*>(X + (int64_t)i * ld + col + 4);
-        x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-        x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
-      } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = (i < meta.R && col + t < ncol) ? X[(int64_t)i * ld + col + t] : 0.0f;
-      }
+    const float* st = ring + (c % kTbStages) * kTbStageFloats;
+    for (int e = threadIdx.x; e < nops * kTbRows * 16; e += kTbThreads) {  // 8 values per item
+      const int op = e >> 9, r = (e >> 4) & (kTbRows - 1), g = e & 15;
+      const float4 v0 = *reinterpret_cast<const float4*>(st + r * 256 + op * 128 + g * 8);
+      const float4 v1 = *reinterpret_cast<const float4*>(st + r * 256 + op * 128 + g * 8 + 4);
+      const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       uint32_t h0[4], h1[4], h2[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -565,7 +588,7 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) {
       tc_fence_after_sync();
-      const uint32_t a = smem_u32(buf), b = a + 3 * kTbPart;
+      const uint32_t a = smem_u32(buf), b = dg ? a : a + 3 * kTbPart;
       const int pa[6] = {0, 0, 1, 1, 0, 2}, pb[6] = {0, 1, 0, 1, 2, 0};
 #pragma unroll
       for (int ks = 0; ks < kTbRows / 16; ++ks) {  // 16 rows = two 8-row atom groups
@@ -579,6 +602,7 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       mma_commit(&done[c & 1]);
     }
   }
+  cp_async_wait_all();
   if (threadIdx.x == 0) mma_commit(fin);  // covers every MMA issued (also after an abort)
   const bool fin_ok = mbar_wait(fin, 0, nullptr, status);
   if (ok && fin_ok) {
@@ -590,12 +614,17 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     for (int cc = 0; cc < 64; cc += 32) {
       float y[32];
       tmem_ld32(t_lane + cc, y);
+      const int qb = q0 + half * 64 + cc;
       if (pr < M) {
-        float* dst = C + (int64_t)pr * ldc + q0 + half * 64 + cc;
-        const int qb = q0 + half * 64 + cc;
+        float* dst = C + (int64_t)pr * ldc + qb;
 #pragma unroll
         for (int t = 0; t < 32; ++t)
-          if (qb + t < N) dst[t] = y[t];
+          if (qb + t < N && (!dg || qb + t >= pr)) dst[t] = y[t];
+      }
+      if (sym) {  // the transpose: C[q][p] for q < m (not G's column m), lanes along p coalesced
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (pr < M && qb + t < M && qb + t > pr) C[(int64_t)(qb + t) * ldc + pr] = y[t];
       }
     }
   }
