@@ -456,27 +456,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // last bit of x's significand), and the six part products whose weight is
 // above 2^-24 are accumulated in fp32 in TMEM: a0b0 + a0b1 + a1b0 + a1b1 +
 // a0b2 + a2b0 (each product of two 8-bit significands is exact).
-// Block = (unit, 128 p, 128 q), 256 threads.  G's first m columns and H are
-// symmetric: only tiles with p0 <= q0 run, and each writes its transpose too
+//
+// C is cut into 128 x 128 tiles.  G's first m columns and H are symmetric:
+// only tiles with p0 <= q0 are computed, and each also writes its transpose
 // (a diagonal tile writes its upper triangle and mirrors it), so both
-// triangles hold the same numbers; a diagonal tile stages one strip, which
-// serves as both operands (in mode 0 E's strips are taken over the m + 1
-// columns of [E | s], so that G's column m is in it).  Per chunk of 32 rows the fp32 rows arrive by
-// 16-byte cp.async in a ring of three stages, two chunks ahead; every thread
-// then splits 8 consecutive values at a time with the packed fp32->bf16x2
-// conversion and writes the parts as MN-major operands (1024-byte atoms of 8
-// rows x 64 elements along p or q: LBO = 1024 B along p/q, SBO = 2048 B along
-// the rows); thread 0 issues the chunk's 12 MMAs (M = N = 128, K = 16, both
-// operands MN-major).  Two operand buffers: the split of chunk c + 1 overlaps
-// the MMAs of chunk c.
-constexpr int kTbThreads = 256;
-constexpr int kTbRows = 32;                         // proxy rows per chunk
-constexpr int kTbPart = kTbRows * 128 * 2;          // one bf16 part of one operand: 8 KB
-constexpr int kTbBuf = 6 * kTbPart;                 // A0 A1 A2 B0 B1 B2
-constexpr int kTbStageFloats = kTbRows * 256;       // fp32 rows of both strips: A at 0, B at 128
-constexpr int kTbStages = 3;
+// triangles hold the same numbers.  A block of 512 threads takes up to three
+// consecutive tiles of the unit (row-major over the computed ones), one
+// 128-column TMEM accumulator each, and the distinct 128-column strips they
+// read (at most four: modes 0 and 1 read both operands from the same matrix,
+// E's strips taken over the m + 1 columns of [E | s]), so a strip shared by
+// its tiles is staged and split once.  Per chunk of 16 proxy rows the strips'
+// fp32 rows arrive by 16-byte cp.async (zero past R and past the columns) in
+// a ring of four stages, three chunks ahead; a worker splits 8
+// consecutive values at a time with the packed fp32->bf16x2 conversion and
+// writes the parts as MN-major operands (1024-byte atoms of 8 rows x 64
+// elements along p or q: LBO = 1024 B along p/q, SBO = 2048 B along the
+// rows).  Warps 1-15 stage and split (a named barrier among them per chunk)
+// and signal the operand buffer on an mbarrier; one thread of warp 0 only
+// issues the six MMAs per tile (M = N = 128, K = 16, both operands MN-major)
+// and commits them to the buffer's "done" mbarrier.  Two operand buffers:
+// the split of chunk c + 1 overlaps the MMAs of chunk c.
+constexpr int kTbThreads = 512;
+constexpr int kTbRows = 16;                                 // proxy rows per chunk (one K step)
+constexpr int kTbTiles = 3;                                 // output tiles per block
+constexpr int kTbStrips = 4;                                // distinct strips per block, at most
+constexpr int kTbPart = kTbRows * 128 * 2;                  // one bf16 part of one strip: 4 KB
+constexpr int kTbBuf = kTbStrips * 3 * kTbPart;             // every strip's three parts
+constexpr int kTbStripFloats = kTbRows * 128;               // one strip's fp32 rows of a chunk
+constexpr int kTbStageFloats = kTbStrips * kTbStripFloats;  // one ring stage
+constexpr int kTbStages = 4;
+constexpr int kTbWorkers = kTbThreads - 32;                 // warps 1-15 stage and split; warp 0 issues
+constexpr int kTbSlots = (kTbStageFloats / 4 + kTbWorkers - 1) / kTbWorkers;  // 16-byte copies per worker
+constexpr int kTbItems = (kTbStageFloats / 8 + kTbWorkers - 1) / kTbWorkers;  // 8-value splits per worker
 constexpr int kTbSmem = 1024 + 1024 + 2 * kTbBuf + kTbStages * kTbStageFloats * 4;  // head, slack, buffers, ring
 static_assert(kTbSmem <= 227 * 1024, "operand buffers and the fp32 ring fit one CTA's shared memory");
+constexpr int kAtbTile = 128;  // output tile of the A^T B products
+
+// The computed tiles of one unit: rows mt = ceil(m / 128) of p, nt columns of
+// q; the symmetric modes take mi <= ni only.
+struct TileGrid {
+  int mt, nt;
+  bool sym;
+  __host__ __device__ int count() const { return sym ? mt * nt - mt * (mt - 1) / 2 : mt * nt; }
+  // tile number t (row-major over the computed tiles) -> (mi, ni)
+  __host__ __device__ void tile(int t, int& mi, int& ni) const {
+    for (mi = 0;; ++mi) {
+      const int in_row = sym ? nt - mi : nt;
+      if (t < in_row) break;
+      t -= in_row;
+    }
+    ni = (sym ? mi : 0) + t;
+  }
+};
+__host__ __device__ inline TileGrid tile_grid(int mode, int m, int d) {
+  TileGrid g;
+  g.mt = (m + kAtbTile - 1) / kAtbTile;
+  g.nt = mode == 2 ? (d + kAtbTile - 1) / kAtbTile : (mode == 0 ? m + 1 + kAtbTile - 1 : m + kAtbTile - 1) / kAtbTile;
+  g.sym = mode != 2;
+  return g;
+}
+// blocks per unit for the largest m of a launch
+inline int atb_blocks_per_unit(int mode, int max_m, int d) {
+  return (tile_grid(mode, max_m, d).count() + kTbTiles - 1) / kTbTiles;
+}
 
 __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
   const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(a, b));
@@ -484,50 +526,102 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 }
 
 __global__ void __launch_bounds__(kTbThreads, 1)
-    am_atb_tc_kernel(const AmMeta meta, float* ws, int mode, unsigned* status) {
+    am_atb_tc_kernel(const AmMeta meta, float* ws, int mode, int blocks_per_unit, unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
   uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [2] an operand buffer's MMAs are done
-  uint64_t* fin = done + 2;                                // every MMA is done
+  uint64_t* ready = done + 2;                              // [2] an operand buffer is split
+  uint64_t* fin = ready + 2;                               // every MMA is done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tb_smem + 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* bufs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tb_smem) + 1024 + 1023) &
                                              ~uintptr_t(1023));
   float* ring = reinterpret_cast<float*>(bufs + 2 * kTbBuf);
-  const int mt = (meta.max_m + 127) / 128;
-  const int nt = mode == 2 ? (meta.d + 127) / 128 : (meta.max_m + 1 + 127) / 128;
-  const int ni = (int)(blockIdx.x % nt);
-  const int mi = (int)((blockIdx.x / nt) % mt);
-  const bool sym = mode != 2;
-  if (sym && mi > ni) return;
-  const bool dg = sym && mi == ni;  // diagonal tile: one strip, both operands
-  const AmUnit u = am_unit(meta, blockIdx.x / ((int64_t)nt * mt), ws);
+  const AmUnit u = am_unit(meta, blockIdx.x / blocks_per_unit, ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
-  const int p0 = mi * 128, q0 = ni * 128;
-  if (p0 >= M || q0 >= N) return;
-  const float* A = u.base;
-  const int lda = u.ldE;
-  const float* B = mode == 2 ? u.base + am_off_Y(meta.R, u.m, u.ldE) : u.base;
-  const int ldb = mode == 2 ? meta.d : u.ldE;
+  const TileGrid tg = tile_grid(mode, M, meta.d);
+  const int t0 = (int)(blockIdx.x % blocks_per_unit) * kTbTiles;
+  const int ntiles = min(kTbTiles, tg.count() - t0);
+  if (ntiles <= 0) return;
+  // the block's tiles and strips: strip slot k holds 128 columns from col[k]
+  // of X[k] (row stride ld[k], ncol[k] columns); tile k reads slots sa[k], sb[k]
+  const float* Xm = u.base;  // E or Ph
+  const float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
+  int tmi[kTbTiles], tni[kTbTiles], sa[kTbTiles], sb[kTbTiles];
+  int scol[kTbStrips];
+  int nstr = 0;
+#pragma unroll
+  for (int k = 0; k < kTbTiles; ++k) {
+    tmi[k] = tni[k] = sa[k] = sb[k] = 0;
+    if (k < ntiles) tg.tile(t0 + k, tmi[k], tni[k]);
+  }
+  // strips of the first operand (columns of X)
+  auto find_or_add = [&](int col) {
+    for (int k = 0; k < nstr; ++k)
+      if (scol[k] == col) return k;
+    scol[nstr] = col;
+    return nstr++;
+  };
+#pragma unroll
+  for (int k = 0; k < kTbTiles; ++k)
+    if (k < ntiles) sa[k] = find_or_add(tmi[k] * 128);
+  int ybase = nstr;  // mode 2: the second operand's strips come from Y
+#pragma unroll
+  for (int k = 0; k < kTbTiles; ++k) {
+    if (k >= ntiles) continue;
+    if (mode == 2) {
+      const int col = tni[k] * 128;
+      int found = -1;
+      for (int s = ybase; s < nstr; ++s)
+        if (scol[s] == col) found = s;
+      if (found < 0) {
+        scol[nstr] = col;
+        found = nstr++;
+      }
+      sb[k] = found;
+    } else {
+      sb[k] = find_or_add(tni[k] * 128);
+    }
+  }
+  const int ncolX = mode == 0 ? N : M;  // mode 0: E over the m + 1 columns of [E | s] (row m of C is not kept)
   float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
   const int ldc = mode == 2 ? meta.d : u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nops = dg ? 1 : 2;
   const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
-  // chunk c's fp32 rows into ring stage c % 3 (zero past R and past the strip's columns)
+  const int wt = threadIdx.x - 32;  // worker thread number (warps 1-15)
+  // Each worker's share of a chunk's 16-byte copies (slot k: float4 number
+  // wt + k * kTbWorkers of [strip][row][32]) is the same in every chunk; only
+  // the rows move.  Per slot: the ring offset, the source of row r of the
+  // first chunk, the bytes inside the strip's columns, the row stride.
+  int soff[kTbSlots], vb[kTbSlots], srow[kTbSlots];
+  const float* src[kTbSlots];
+  int64_t step[kTbSlots];
+#pragma unroll
+  for (int k = 0; k < kTbSlots; ++k) {
+    const int e = wt + k * kTbWorkers;
+    const int st = e >> 9, r = (e >> 5) & (kTbRows - 1), q = e & 31;
+    const bool used = wt >= 0 && st < nstr;
+    const bool fromY = mode == 2 && st >= ybase;
+    const float* X = fromY ? Y : Xm;
+    const int ld = fromY ? meta.d : u.ldE;
+    const int ncol = fromY ? meta.d : ncolX;
+    const int col = (used ? scol[st] : 0) + 4 * q;
+    soff[k] = st * kTbStripFloats + r * 128 + 4 * q;
+    srow[k] = r;
+    vb[k] = used ? max(0, min(4, ncol - col)) * 4 : -1;  // -1: slot unused
+    src[k] = vb[k] > 0 ? X + (int64_t)r * ld + col : Xm;
+    step[k] = vb[k] > 0 ? (int64_t)kTbRows * ld : 0;
+  }
+  // chunk c's fp32 rows into ring stage c % kTbStages (workers)
   auto load_chunk = [&](int c) {
     if (c < nchunks) {
-      float* st = ring + (c % kTbStages) * kTbStageFloats;
+      float* stg = ring + (c % kTbStages) * kTbStageFloats;
       const int i0 = c * kTbRows;
-      for (int e = threadIdx.x; e < nops * kTbRows * 32; e += kTbThreads) {
-        const int op = e >> 10, r = (e >> 5) & (kTbRows - 1), q = e & 31;
-        const float* X = op ? B : A;
-        const int ld = op ? ldb : lda;
-        const int col = (op ? q0 : p0) + 4 * q;
-        const int ncol = op || mode == 0 ? N : M;  // mode 0: A over m + 1 columns too (row m of C is not kept)
-        const int i = i0 + r;
-        const int valid = i < meta.R ? max(0, min(4, ncol - col)) : 0;
-        cp_async_16z(st + r * 256 + op * 128 + 4 * q, valid > 0 ? X + (int64_t)i * ld + col : X, valid * 4);
+#pragma unroll
+      for (int k = 0; k < kTbSlots; ++k) {
+        if (vb[k] < 0) continue;
+        const bool in = i0 + srow[k] < meta.R && vb[k] > 0;
+        cp_async_16z(stg + soff[k], in ? src[k] + c * step[k] : Xm, in ? vb[k] : 0);
       }
     }
     cp_async_commit();  // one group per chunk, empty past the end
@@ -535,93 +629,112 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&done[0], 1);
     mbar_init(&done[1], 1);
+    mbar_init(&ready[0], kTbWorkers);
+    mbar_init(&ready[1], kTbWorkers);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
     __syncwarp();
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 512);
   }
-  load_chunk(0);
-  load_chunk(1);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // both operands MN-major (transpose bits), bf16 x bf16 -> fp32, M = N = 128
-  const uint32_t idesc = idesc_bf16_f32(128, 128) | (1u << 15) | (1u << 16);
   bool ok = true;
-  for (int c = 0; c < nchunks && ok; ++c) {
-    load_chunk(c + 2);
-    cp_async_wait_group<2>();  // this thread's copies of chunk c are in
-    uint8_t* buf = bufs + (c & 1) * kTbBuf;
-    if (c >= 2) {  // the MMAs of chunk c - 2 have read this operand buffer
-      ok = mbar_wait(&done[c & 1], ((c >> 1) - 1) & 1, abort_flag, status);
-      if (!__syncthreads_and(ok)) { ok = false; break; }
-    } else {
-      __syncthreads();
-    }
-    const float* st = ring + (c % kTbStages) * kTbStageFloats;
-    for (int e = threadIdx.x; e < nops * kTbRows * 16; e += kTbThreads) {  // 8 values per item
-      const int op = e >> 9, r = (e >> 4) & (kTbRows - 1), g = e & 15;
-      const float4 v0 = *reinterpret_cast<const float4*>(st + r * 256 + op * 128 + g * 8);
-      const float4 v1 = *reinterpret_cast<const float4*>(st + r * 256 + op * 128 + g * 8 + 4);
-      const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      uint32_t h0[4], h1[4], h2[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = x[2 * t], b = x[2 * t + 1];
-        h0[t] = bf2_bits(a, b);
-        const float ra = a - __uint_as_float(h0[t] << 16), rb = b - __uint_as_float(h0[t] & 0xFFFF0000u);
-        h1[t] = bf2_bits(ra, rb);
-        h2[t] = bf2_bits(ra - __uint_as_float(h1[t] << 16), rb - __uint_as_float(h1[t] & 0xFFFF0000u));
-      }
-      // MN-major atom layout: row r, 8 elements at g * 8 along p / q
-      const int off = (r >> 3) * 2048 + (g >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
-      uint8_t* base = buf + op * 3 * kTbPart + off;
-      *reinterpret_cast<uint4*>(base) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-      *reinterpret_cast<uint4*>(base + kTbPart) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-      *reinterpret_cast<uint4*>(base + 2 * kTbPart) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the parts, for the tensor cores
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after_sync();
-      const uint32_t a = smem_u32(buf), b = dg ? a : a + 3 * kTbPart;
+  if (warp == 0) {
+    if (lane == 0) {  // the MMA issuer: one chunk's MMAs once its operands are split
+      // both operands MN-major (transpose bits), bf16 x bf16 -> fp32, M = N = 128
+      const uint32_t idesc = idesc_bf16_f32(128, 128) | (1u << 15) | (1u << 16);
+      const uint64_t dbase = sdesc_mn_sw128(smem_u32(bufs), 1024, 2048);  // + (byte offset >> 4)
       const int pa[6] = {0, 0, 1, 1, 0, 2}, pb[6] = {0, 1, 0, 1, 2, 0};
-#pragma unroll
-      for (int ks = 0; ks < kTbRows / 16; ++ks) {  // 16 rows = two 8-row atom groups
-#pragma unroll
-        for (int pr = 0; pr < 6; ++pr) {
-          const uint64_t da = sdesc_mn_sw128(a + pa[pr] * kTbPart + ks * 2 * 2048, 1024, 2048);
-          const uint64_t db = sdesc_mn_sw128(b + pb[pr] * kTbPart + ks * 2 * 2048, 1024, 2048);
-          mma_bf16(tmem, da, db, idesc, (c > 0 || ks > 0 || pr > 0) ? 1u : 0u);
+      for (int c = 0; c < nchunks; ++c) {
+        if (!mbar_wait(&ready[c & 1], (uint32_t)(c >> 1) & 1u, abort_flag, status)) {
+          ok = false;
+          break;
         }
+        tc_fence_after_sync();
+        const uint32_t boff = (uint32_t)(c & 1) * kTbBuf;
+#pragma unroll
+        for (int k = 0; k < kTbTiles; ++k) {
+          if (k >= ntiles) break;
+          const uint32_t a = boff + sa[k] * 3 * kTbPart, b = boff + sb[k] * 3 * kTbPart;
+#pragma unroll
+          for (int pr = 0; pr < 6; ++pr)
+            mma_bf16(tmem + k * 128, dbase + ((a + pa[pr] * kTbPart) >> 4), dbase + ((b + pb[pr] * kTbPart) >> 4),
+                     idesc, (c > 0 || pr > 0) ? 1u : 0u);
+        }
+        mma_commit(&done[c & 1]);
       }
-      mma_commit(&done[c & 1]);
     }
+    __syncwarp();
+  } else {  // workers: stage, split, hand the operand buffer over
+    for (int c = 0; c < kTbStages - 1; ++c) load_chunk(c);
+    for (int c = 0; c < nchunks; ++c) {
+      cp_async_wait_group<kTbStages - 2>();  // this thread's copies of chunk c are in
+      bool w_ok = true;
+      if (c >= 2)  // the MMAs of chunk c - 2 have read this operand buffer
+        w_ok = mbar_wait(&done[c & 1], ((c >> 1) - 1) & 1, abort_flag, status);
+      // every worker's copies of chunk c are in, and every worker is done with chunk c - 1
+      if (!bar_red_and_n(1, kTbWorkers, w_ok)) {
+        ok = false;
+        break;
+      }
+      load_chunk(c + kTbStages - 1);  // into the stage of chunk c - 1
+      uint8_t* buf = bufs + (c & 1) * kTbBuf;
+      const float* stg = ring + (c % kTbStages) * kTbStageFloats;
+#pragma unroll
+      for (int k = 0; k < kTbItems; ++k) {  // 8 values per item
+        const int e = wt + k * kTbWorkers;
+        const int st = e >> 8, r = (e >> 4) & (kTbRows - 1), g = e & 15;
+        if (st >= nstr) continue;
+        const float* sp = stg + st * kTbStripFloats + r * 128 + g * 8;
+        const float4 v0 = *reinterpret_cast<const float4*>(sp);
+        const float4 v1 = *reinterpret_cast<const float4*>(sp + 4);
+        const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t h0[4], h1[4], h2[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = x[2 * t], b = x[2 * t + 1];
+          h0[t] = bf2_bits(a, b);
+          const float ra = a - __uint_as_float(h0[t] << 16), rb = b - __uint_as_float(h0[t] & 0xFFFF0000u);
+          h1[t] = bf2_bits(ra, rb);
+          h2[t] = bf2_bits(ra - __uint_as_float(h1[t] << 16), rb - __uint_as_float(h1[t] & 0xFFFF0000u));
+        }
+        // MN-major atom layout: row r, 8 elements at g * 8 along p / q
+        const int off = (r >> 3) * 2048 + (g >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
+        uint8_t* base = buf + st * 3 * kTbPart + off;
+        *reinterpret_cast<uint4*>(base) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+        *reinterpret_cast<uint4*>(base + kTbPart) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+        *reinterpret_cast<uint4*>(base + 2 * kTbPart) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the parts, for the tensor cores
+      mbar_arrive(&ready[c & 1]);
+    }
+    cp_async_wait_all();
   }
-  cp_async_wait_all();
+  if (!ok) *abort_flag = 1;
   if (threadIdx.x == 0) mma_commit(fin);  // covers every MMA issued (also after an abort)
   const bool fin_ok = mbar_wait(fin, 0, nullptr, status);
-  if (ok && fin_ok) {
+  if (__syncthreads_and(ok && fin_ok && !*abort_flag)) {
     tc_fence_after_sync();
-    const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; columns [64 half, 64 half + 64)
-    const int pr = p0 + q4 * 32 + lane;
-    const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(half * 64);
-#pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
+    const int q4 = warp & 3, cq = warp >> 2;  // TMEM lane quarter; columns [32 cq, 32 cq + 32) of a tile
+#pragma unroll 1
+    for (int k = 0; k < ntiles; ++k) {
+      const bool dg = tg.sym && tmi[k] == tni[k];
+      const int pr = tmi[k] * 128 + q4 * 32 + lane;
       float y[32];
-      tmem_ld32(t_lane + cc, y);
-      const int qb = q0 + half * 64 + cc;
+      tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(k * 128 + cq * 32), y);
+      const int qb = tni[k] * 128 + cq * 32;
       if (pr < M) {
         float* dst = C + (int64_t)pr * ldc + qb;
 #pragma unroll
         for (int t = 0; t < 32; ++t)
           if (qb + t < N && (!dg || qb + t >= pr)) dst[t] = y[t];
       }
-      if (sym) {  // the transpose: C[q][p] for q < m (not G's column m), lanes along p coalesced
+      if (tg.sym) {  // the transpose: C[q][p] for q < m (not G's column m), lanes along p coalesced
 #pragma unroll
         for (int t = 0; t < 32; ++t)
           if (pr < M && qb + t < M && qb + t > pr) C[(int64_t)(qb + t) * ldc + pr] = y[t];
@@ -633,11 +746,10 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   tc_fence_after_sync();
   if (warp == 0) {
     __syncwarp();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-constexpr int kAtbTile = 128;  // output tile of the A^T B products (grid sizing)
 
 // ------------------------------------------------------------------ blocked descents
 // Both fits are cyclic coordinate descents on normal equations: a step on
@@ -1099,19 +1211,18 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     am_targets_tc_kernel<D><<<(unsigned)(m.units * rbt), kTcThreads, tc_smem_bytes<D>(), stream>>>(
         *al.tmK, *al.tmV, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    const int mt128 = (m.max_m + kAtbTile - 1) / kAtbTile;
-    const int nt0 = (m.max_m + 1 + kAtbTile - 1) / kAtbTile;
-    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * nt0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 0, al.status);
+    const int g0 = atb_blocks_per_unit(0, m.max_m, D);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 0, g0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * nt0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 1, al.status);
+    const int g1 = atb_blocks_per_unit(1, m.max_m, D), g2 = atb_blocks_per_unit(2, m.max_m, D);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(m, al.ws, 1, g1, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * mt128 * ((D + 127) / 128)), kTbThreads, kTbSmem, stream>>>(m, al.ws, 2,
-                                                                                              al.status);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(m, al.ws, 2, g2, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);
