@@ -289,21 +289,25 @@ def profile_traffic(kernel: str, workload: str):
 
 def am_flops(sp, n, m, sweeps: int):
     """Algorithmic flops of one Attention Matching fit (2 per multiply-add), summed over the units,
-    as (tensor-core part, fp32 part).  Tensor cores: the full-attention targets, Q K^T and P V over
-    all n keys (the kept keys' exponentials reuse those logits).  fp32 CUDA cores: the Gram
-    products E^T [E | s], Ph^T Ph and Ph^T Y, the compact probabilities, and the two descents
-    (m-long updates of the mass gradient, m x d-long updates of the value gradient, per step;
-    their initial gradients)."""
+    as (targets, Gram products, fp32 rest).  Targets: Q K^T and P V over all n keys (the kept keys'
+    exponentials reuse those logits), bf16 operands on the tensor cores.  Gram products: E^T [E | s],
+    Ph^T Ph and Ph^T Y, fp32-accurate (on the tensor cores as split-bf16 products).  fp32 rest, on
+    the CUDA cores: the compact probabilities and the two descents (m-long updates of the mass
+    gradient, m x d-long updates of the value gradient, per step; their initial gradients)."""
     R, d = sp.R, sp.d
-    ft = ff = 0.0
+    ft = fg = ff = 0.0
     for nb, mb in zip(n, m):
         mb = min(mb, nb)
         if mb <= 0:
             continue
-        ft += sp.L * sp.H * 4.0 * R * nb * d
-        ff += sp.L * sp.H * (2.0 * R * mb * (mb + 1) + 2.0 * R * mb * mb + 2.0 * R * mb * d + 2.0 * R * mb
-                             + 2.0 * mb * mb * (d + 1) + sweeps * (2.0 * mb * mb + 2.0 * mb * mb * d))
-    return ft, ff
+        units = sp.L * sp.H
+        ft += units * 4.0 * R * nb * d
+        fg += units * (2.0 * R * mb * (mb + 1) + 2.0 * R * mb * mb + 2.0 * R * mb * d)
+        ff += units * (2.0 * R * mb + 2.0 * mb * mb * (d + 1) + sweeps * (2.0 * mb * mb + 2.0 * mb * mb * d))
+    return ft, fg, ff
+
+
+SPLIT_PRODUCTS = 6  # bf16 products per fp32-accurate product (three-part split, terms above 2^-24)
 
 
 def fp32_peak_tflops() -> float:
@@ -533,22 +537,27 @@ def our_arm(args):
     roofline.update({"traffic": profile_traffic(dom_kernel, sp.name), "peak_source": pk["source"],
                      "algorithmic_flops_per_launch": F_alg, "algorithmic_bytes_per_launch": B_pass})
     if args.am_sweeps > 0:
-        # Attention Matching dominates the step, timed as one stage: its targets run on the
-        # tensor cores, its Gram products and descents on the fp32 CUDA cores.  The stage's
-        # roofline time is the sum of each part at its own peak; "achieved" is the fp32-equivalent
-        # rate (tensor work weighted by fp32 peak / bf16 peak), so frac = t_roof / t_stage.
-        F_tc, F_fp = am_flops(sp, n, m, args.am_sweeps)
+        # Attention Matching dominates the step, timed as one stage.  Its roofline time is the
+        # sum of each part at the rate it can run on this GPU: the targets at the bf16 tensor
+        # peak; the fp32-accurate Gram products as SPLIT_PRODUCTS bf16 products each at the same
+        # peak (three tf32 products at half the rate cost the same); the descents and compact
+        # probabilities at the fp32 FMA peak of the CUDA cores.  "achieved" is the bf16-equivalent
+        # rate, so frac = t_roof / t_stage.
+        F_tc, F_gram, F_fp = am_flops(sp, n, m, args.am_sweeps)
         t_am = per_stage["am_fit"] * 1e-3
-        peak = fp32_peak_tflops()
-        t_roof = F_tc / (pk["bf16_tflops"] * 1e12) + F_fp / (peak * 1e12)
-        roofline = {"bound": "alu", "kernel": "kvc_am_fit (one stage: tensor-core targets, fp32 Gram "
-                                              "products and descents)",
-                    "achieved": t_roof * peak / t_am, "peak": peak, "unit": "TFLOP/s",
-                    "frac": t_roof / t_am, "traffic": None,
-                    "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x 2070 MHz; tensor part "
-                                   "against the measured bf16 peak",
-                    "algorithmic_flops_per_launch": F_tc + F_fp, "tensor_flops": F_tc, "fp32_flops": F_fp,
-                    "t_roof_ms": t_roof * 1e3}
+        bf = pk["bf16_tflops"] * 1e12
+        fp_peak = fp32_peak_tflops()
+        t_am_roof = (F_tc + SPLIT_PRODUCTS * F_gram) / bf + F_fp / (fp_peak * 1e12)
+        t_roof += t_am_roof  # the step: the token-eviction chain's bound plus the fit's
+        roofline = {"bound": "tensor", "kernel": "kvc_am_fit (one stage: tensor-core targets and Gram "
+                                                 "products, fp32 descents)",
+                    "achieved": t_am_roof * pk["bf16_tflops"] / t_am, "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": t_am_roof / t_am, "traffic": None,
+                    "peak_source": pk["source"] + "; Gram products counted as %d bf16 products; fp32 "
+                                   "part against the derived 152 SMs x 128 FMA/clk x 2 x 2070 MHz = "
+                                   "%.1f TFLOP/s" % (SPLIT_PRODUCTS, fp_peak),
+                    "algorithmic_flops_per_launch": F_tc + F_gram + F_fp, "targets_flops": F_tc,
+                    "gram_flops": F_gram, "fp32_flops": F_fp, "t_roof_ms": t_am_roof * 1e3}
     if args.variant == "sentinel":  # evicted rows written: K and V rows (2d bytes each) and a tag
         compact_bytes = (entries - sp.L * sp.H * Mtot) * (4.0 * d + 4.0)
     else:
