@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
       const bool v = lane < cnt;
       const int j = j0 + lane;
       float gk = v ? g[j] : 0.0f;
-      const float w0 = v ? w[j] : 0.0f, tk = v ? thr[j] : INFINITY, dk = v ? diag[j] : 1.0f;
+      const float w0 = v ? w[j] : 0.0f, tk = v ? thr[j] : INFINITY, dk = v ? 1.0f / diag[j] : 1.0f;
       float wk = w0, dwk = 0.0f;
 #pragma unroll
       for (int t = 0; t < kDb; ++t) {
@@ -853,8 +853,8 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
         const float gt = __shfl_sync(0xffffffffu, gk, t);
         const float wt = __shfl_sync(0xffffffffu, w0, t);  // w of coordinate t before its own step
         const float tt = __shfl_sync(0xffffffffu, tk, t);
-        const float dt = __shfl_sync(0xffffffffu, dk, t);
-        const float nw = fabsf(gt) > tt ? fmaxf(0.0f, wt - gt / dt) : wt;
+        const float dt = __shfl_sync(0xffffffffu, dk, t);  // 1 / G_tt
+        const float nw = fabsf(gt) > tt ? fmaxf(0.0f, wt - gt * dt) : wt;
         const float dl = nw - wt;
         if (dl != 0.0f) {
           gk = fmaf(dl, dtile[t * kTileLd + lane], gk);
@@ -1017,7 +1017,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   float* Sx = S + kVc;                                     // [kVc] max |X0| (bits)
   int* moved = reinterpret_cast<int*>(Sx + kVc);           // [2] did that block move
   float* Gs = am_smem + kValueHead;                        // [kVc][ldv] gradient, column-major
-  float* hdiag = Gs + kVc * ldv;                           // [m] H_jj
+  float* hdiag = Gs + kVc * ldv;                           // [m] 1 / H_jj (0 where H_jj <= 0)
   float* thrb = hdiag + m;                                 // [m] 2^-17 pi_j; +inf where H_jj <= 0
   const float* Hm = u.base + am_off_G(meta.R, u.ldE);
   const int64_t ld = u.ldE;
@@ -1031,7 +1031,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
     for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
     if (lane == 0) {
       const float d = hr[i];
-      hdiag[i] = d;
+      hdiag[i] = d > 0.0f ? 1.0f / d : 0.0f;
       thrb[i] = d > 0.0f ? kAmGuard * ps : INFINITY;
     }
   }
@@ -1106,7 +1106,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
         float dl = 0.0f;
         if (t < cnt) {
           const float gt = gv[t];
-          dl = fabsf(gt) > thrb[j0 + t] * Sc ? -gt / hdiag[j0 + t] : 0.0f;
+          dl = fabsf(gt) > thrb[j0 + t] * Sc ? -gt * hdiag[j0 + t] : 0.0f;
           if (__any_sync(0xffffffffu, dl != 0.0f)) {
             mv = true;
             const float4* t4 = reinterpret_cast<const float4*>(dtile + t * kTileLd);
