@@ -847,9 +847,13 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
       float gk = v ? g[j] : 0.0f;
       const float w0 = v ? w[j] : 0.0f, tk = v ? thr[j] : INFINITY, dk = v ? 1.0f / diag[j] : 1.0f;
       float wk = w0, dwk = 0.0f;
+      // If no coordinate of the block would move on the gradient as it stands,
+      // none moves at all (a step that does not move changes nothing): skip.
+      const bool would = v && (fabsf(gk) > tk ? fmaxf(0.0f, w0 - gk * dk) : w0) != w0;
+      const bool steps = __any_sync(0xffffffffu, would);
 #pragma unroll
       for (int t = 0; t < kDb; ++t) {
-        if (t >= cnt) break;
+        if (t >= cnt || !steps) break;
         const float gt = __shfl_sync(0xffffffffu, gk, t);
         const float wt = __shfl_sync(0xffffffffu, w0, t);  // w of coordinate t before its own step
         const float tt = __shfl_sync(0xffffffffu, tk, t);
@@ -864,7 +868,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
           }
         }
       }
-      if (v) {
+      if (v && steps) {
         g[j] = gk;
         w[j] = wk;
       }
@@ -1100,9 +1104,17 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
       float gv[kDb];
 #pragma unroll
       for (int t = 0; t < kDb; ++t) gv[t] = t < cnt ? Gs[c * ldv + j0 + t] : 0.0f;
+      // If no step of the block would move any column on the gradient as it
+      // stands, none moves at all (a step that does not move changes nothing).
+      bool would = false;
+#pragma unroll
+      for (int t = 0; t < kDb; ++t)
+        if (t < cnt) would |= fabsf(gv[t]) > thrb[j0 + t] * Sc && -gv[t] * hdiag[j0 + t] != 0.0f;
+      const bool steps = __any_sync(0xffffffffu, would);
       bool mv = false;
 #pragma unroll
       for (int t = 0; t < kDb; ++t) {
+        if (!steps) break;
         float dl = 0.0f;
         if (t < cnt) {
           const float gt = gv[t];
@@ -1122,7 +1134,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
         }
         if (lane < kVc) dxc[t * kVc + c] = dl;
       }
-      if (lane < kVc) {
+      if (lane < kVc && steps) {
 #pragma unroll
         for (int t = 0; t < kDb; ++t)
           if (t < cnt) Gs[c * ldv + j0 + t] = gv[t];
