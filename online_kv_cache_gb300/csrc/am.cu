@@ -94,7 +94,7 @@ __device__ __forceinline__ AmUnit am_unit(const AmMeta& meta, int64_t unit, floa
   u.m = q.m;
   u.ldE = q.ldE;
   u.moff = q.moff;
-  u.base = ws + q.ws + (int64_t)r * q.unit_floats;
+  u.base = ws + q.ws + (int64_t)r * q.unit_floats;  // regions laid out for the launch's largest m
   return u;
 }
 
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (ok) {
       tc_fence_after_sync();
-      float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
+      float* Y = u.base + am_off_Y(meta.R, meta.max_m, u.ldE);
 #pragma unroll
       for (int col = 0; col < D; col += 32) {
         float y[32];
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (i < meta.R) {
-        u.base[am_off_lse(meta.R, u.m, u.ldE, D) + i] = lse;
+        u.base[am_off_lse(meta.R, meta.max_m, u.ldE, D) + i] = lse;
         Erow[u.m] = exp2f((lse - c) * kLog2e);
       }
     }
@@ -476,19 +476,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // issues the six MMAs per tile (M = N = 128, K = 16, both operands MN-major)
 // and commits them to the buffer's "done" mbarrier.  Two operand buffers:
 // the split of chunk c + 1 overlaps the MMAs of chunk c.
-constexpr int kTbThreads = 512;
+constexpr int kTbThreads = 544;                             // warp 0 issues, warps 1-15 split, warp 16 loads
 constexpr int kTbRows = 16;                                 // proxy rows per chunk (one K step)
 constexpr int kTbTiles = 3;                                 // output tiles per block
 constexpr int kTbStrips = 4;                                // distinct strips per block, at most
 constexpr int kTbPart = kTbRows * 128 * 2;                  // one bf16 part of one strip: 4 KB
 constexpr int kTbBuf = kTbStrips * 3 * kTbPart;             // every strip's three parts
-constexpr int kTbStripFloats = kTbRows * 128;               // one strip's fp32 rows of a chunk
+constexpr int kTbStripFloats = kTbRows * 128;               // one strip's fp32 rows of a chunk (one box)
 constexpr int kTbStageFloats = kTbStrips * kTbStripFloats;  // one ring stage
-constexpr int kTbStages = 4;
-constexpr int kTbWorkers = kTbThreads - 32;                 // warps 1-15 stage and split; warp 0 issues
-constexpr int kTbSlots = (kTbStageFloats / 4 + kTbWorkers - 1) / kTbWorkers;  // 16-byte copies per worker
+constexpr int kTbStages = 2;
+constexpr int kTbBufs = 3;                                  // operand buffers: the split runs up to two chunks ahead
+constexpr int kTbWorkers = 15 * 32;                         // the splitting warps
 constexpr int kTbItems = (kTbStageFloats / 8 + kTbWorkers - 1) / kTbWorkers;  // 8-value splits per worker
-constexpr int kTbSmem = 1024 + 1024 + 2 * kTbBuf + kTbStages * kTbStageFloats * 4;  // head, slack, buffers, ring
+constexpr int kTbSmem = 1024 + 1024 + kTbBufs * kTbBuf + kTbStages * kTbStageFloats * 4;  // head, slack, buffers, ring
 static_assert(kTbSmem <= 227 * 1024, "operand buffers and the fp32 ring fit one CTA's shared memory");
 constexpr int kAtbTile = 128;  // output tile of the A^T B products
 
@@ -526,27 +526,30 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 }
 
 __global__ void __launch_bounds__(kTbThreads, 1)
-    am_atb_tc_kernel(const AmMeta meta, float* ws, int mode, int blocks_per_unit, unsigned* status) {
+    am_atb_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                     const AmMeta meta, float* ws, int mode, int blocks_per_unit, unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
-  uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [2] an operand buffer's MMAs are done
-  uint64_t* ready = done + 2;                              // [2] an operand buffer is split
-  uint64_t* fin = ready + 2;                               // every MMA is done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tb_smem + 64);
+  uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [kTbBufs] an operand buffer's MMAs are done
+  uint64_t* ready = done + kTbBufs;                        // [kTbBufs] an operand buffer is split
+  uint64_t* full = ready + kTbBufs;                              // [kTbStages] a ring stage's rows are in
+  uint64_t* empty = full + kTbStages;                      // [kTbStages] a ring stage is split
+  uint64_t* fin = empty + kTbStages;                       // every MMA is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tb_smem + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* bufs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tb_smem) + 1024 + 1023) &
                                              ~uintptr_t(1023));
-  float* ring = reinterpret_cast<float*>(bufs + 2 * kTbBuf);
-  const AmUnit u = am_unit(meta, blockIdx.x / blocks_per_unit, ws);
+  float* ring = reinterpret_cast<float*>(bufs + kTbBufs * kTbBuf);
+  const int64_t unit = blockIdx.x / blocks_per_unit;
+  const AmUnit u = am_unit(meta, unit, ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
   const TileGrid tg = tile_grid(mode, M, meta.d);
   const int t0 = (int)(blockIdx.x % blocks_per_unit) * kTbTiles;
   const int ntiles = min(kTbTiles, tg.count() - t0);
   if (ntiles <= 0) return;
-  // the block's tiles and strips: strip slot k holds 128 columns from col[k]
-  // of X[k] (row stride ld[k], ncol[k] columns); tile k reads slots sa[k], sb[k]
-  const float* Xm = u.base;  // E or Ph
-  const float* Y = u.base + am_off_Y(meta.R, u.m, u.ldE);
+  // the block's tiles and strips: strip slot k holds the 128 columns from
+  // scol[k] of E / Ph, or (mode 2, slots from ybase on) of Y; tile k reads
+  // slots sa[k] and sb[k]
   int tmi[kTbTiles], tni[kTbTiles], sa[kTbTiles], sb[kTbTiles];
   int scol[kTbStrips];
   int nstr = 0;
@@ -555,7 +558,6 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     tmi[k] = tni[k] = sa[k] = sb[k] = 0;
     if (k < ntiles) tg.tile(t0 + k, tmi[k], tni[k]);
   }
-  // strips of the first operand (columns of X)
   auto find_or_add = [&](int col) {
     for (int k = 0; k < nstr; ++k)
       if (scol[k] == col) return k;
@@ -565,15 +567,15 @@ __global__ void __launch_bounds__(kTbThreads, 1)
 #pragma unroll
   for (int k = 0; k < kTbTiles; ++k)
     if (k < ntiles) sa[k] = find_or_add(tmi[k] * 128);
-  int ybase = nstr;  // mode 2: the second operand's strips come from Y
+  const int ybase = nstr;
 #pragma unroll
   for (int k = 0; k < kTbTiles; ++k) {
     if (k >= ntiles) continue;
     if (mode == 2) {
       const int col = tni[k] * 128;
       int found = -1;
-      for (int s = ybase; s < nstr; ++s)
-        if (scol[s] == col) found = s;
+      for (int st = ybase; st < nstr; ++st)
+        if (scol[st] == col) found = st;
       if (found < 0) {
         scol[nstr] = col;
         found = nstr++;
@@ -583,54 +585,23 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       sb[k] = find_or_add(tni[k] * 128);
     }
   }
-  const int ncolX = mode == 0 ? N : M;  // mode 0: E over the m + 1 columns of [E | s] (row m of C is not kept)
-  float* C = mode == 2 ? u.base + am_off_Bm(meta.R, u.m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
+  // columns of a strip inside the unit's matrix (the maps run to the launch's
+  // row stride): mode 0 takes E over the m + 1 columns of [E | s] (row m of C
+  // is not kept), so that one strip serves both operands of a diagonal tile
+  const int ncolX = mode == 0 ? N : M;
+  float* C = mode == 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
   const int ldc = mode == 2 ? meta.d : u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
-  const int wt = threadIdx.x - 32;  // worker thread number (warps 1-15)
-  // Each worker's share of a chunk's 16-byte copies (slot k: float4 number
-  // wt + k * kTbWorkers of [strip][row][32]) is the same in every chunk; only
-  // the rows move.  Per slot: the ring offset, the source of row r of the
-  // first chunk, the bytes inside the strip's columns, the row stride.
-  int soff[kTbSlots], vb[kTbSlots], srow[kTbSlots];
-  const float* src[kTbSlots];
-  int64_t step[kTbSlots];
-#pragma unroll
-  for (int k = 0; k < kTbSlots; ++k) {
-    const int e = wt + k * kTbWorkers;
-    const int st = e >> 9, r = (e >> 5) & (kTbRows - 1), q = e & 31;
-    const bool used = wt >= 0 && st < nstr;
-    const bool fromY = mode == 2 && st >= ybase;
-    const float* X = fromY ? Y : Xm;
-    const int ld = fromY ? meta.d : u.ldE;
-    const int ncol = fromY ? meta.d : ncolX;
-    const int col = (used ? scol[st] : 0) + 4 * q;
-    soff[k] = st * kTbStripFloats + r * 128 + 4 * q;
-    srow[k] = r;
-    vb[k] = used ? max(0, min(4, ncol - col)) * 4 : -1;  // -1: slot unused
-    src[k] = vb[k] > 0 ? X + (int64_t)r * ld + col : Xm;
-    step[k] = vb[k] > 0 ? (int64_t)kTbRows * ld : 0;
-  }
-  // chunk c's fp32 rows into ring stage c % kTbStages (workers)
-  auto load_chunk = [&](int c) {
-    if (c < nchunks) {
-      float* stg = ring + (c % kTbStages) * kTbStageFloats;
-      const int i0 = c * kTbRows;
-#pragma unroll
-      for (int k = 0; k < kTbSlots; ++k) {
-        if (vb[k] < 0) continue;
-        const bool in = i0 + srow[k] < meta.R && vb[k] > 0;
-        cp_async_16z(stg + soff[k], in ? src[k] + c * step[k] : Xm, in ? vb[k] : 0);
-      }
-    }
-    cp_async_commit();  // one group per chunk, empty past the end
-  };
   if (threadIdx.x == 0) {
-    mbar_init(&done[0], 1);
-    mbar_init(&done[1], 1);
-    mbar_init(&ready[0], kTbWorkers);
-    mbar_init(&ready[1], kTbWorkers);
+    for (int b = 0; b < kTbBufs; ++b) {
+      mbar_init(&done[b], 1);
+      mbar_init(&ready[b], kTbWorkers);
+    }
+    for (int st = 0; st < kTbStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kTbWorkers);
+    }
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -651,12 +622,12 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       const uint64_t dbase = sdesc_mn_sw128(smem_u32(bufs), 1024, 2048);  // + (byte offset >> 4)
       const int pa[6] = {0, 0, 1, 1, 0, 2}, pb[6] = {0, 1, 0, 1, 2, 0};
       for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait(&ready[c & 1], (uint32_t)(c >> 1) & 1u, abort_flag, status)) {
+        if (!mbar_wait(&ready[c % kTbBufs], (uint32_t)(c / kTbBufs) & 1u, abort_flag, status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t boff = (uint32_t)(c & 1) * kTbBuf;
+        const uint32_t boff = (uint32_t)(c % kTbBufs) * kTbBuf;
 #pragma unroll
         for (int k = 0; k < kTbTiles; ++k) {
           if (k >= ntiles) break;
@@ -666,25 +637,46 @@ __global__ void __launch_bounds__(kTbThreads, 1)
             mma_bf16(tmem + k * 128, dbase + ((a + pa[pr] * kTbPart) >> 4), dbase + ((b + pb[pr] * kTbPart) >> 4),
                      idesc, (c > 0 || pr > 0) ? 1u : 0u);
         }
-        mma_commit(&done[c & 1]);
+        mma_commit(&done[c % kTbBufs]);
       }
     }
     __syncwarp();
-  } else {  // workers: stage, split, hand the operand buffer over
-    for (int c = 0; c < kTbStages - 1; ++c) load_chunk(c);
+  } else if (warp == kTbThreads / 32 - 1) {  // the producer: one box per strip and chunk
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kTbStages;
+        if (c >= kTbStages &&  // the workers have split the stage's previous chunk
+            !mbar_wait(&empty[st], (uint32_t)(c / kTbStages - 1) & 1u, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nstr * kTbStripFloats * 4);
+        float* stg = ring + st * kTbStageFloats;
+        for (int k = 0; k < nstr; ++k) {
+          const bool fromY = mode == 2 && k >= ybase;
+          tma_load_3d(stg + k * kTbStripFloats, fromY ? &tmY : &tmX, &full[st], scol[k], c * kTbRows, (int)unit);
+        }
+        issued = c + 1;
+      }
+      // the copies in flight land before the block leaves (bounded waits)
+      for (int c = max(0, issued - kTbStages); c < issued; ++c)
+        mbar_wait(&full[c % kTbStages], (uint32_t)(c / kTbStages) & 1u, nullptr, status);
+    }
+    __syncwarp();
+  } else {  // workers: split the staged rows, hand the operand buffer over
+    const int wt = threadIdx.x - 32;
     for (int c = 0; c < nchunks; ++c) {
-      cp_async_wait_group<kTbStages - 2>();  // this thread's copies of chunk c are in
-      bool w_ok = true;
-      if (c >= 2)  // the MMAs of chunk c - 2 have read this operand buffer
-        w_ok = mbar_wait(&done[c & 1], ((c >> 1) - 1) & 1, abort_flag, status);
-      // every worker's copies of chunk c are in, and every worker is done with chunk c - 1
-      if (!bar_red_and_n(1, kTbWorkers, w_ok)) {
+      const int st0 = c % kTbStages;
+      bool w_ok = mbar_wait(&full[st0], (uint32_t)(c / kTbStages) & 1u, abort_flag, status);
+      if (w_ok && c >= kTbBufs)  // the MMAs of chunk c - kTbBufs have read this operand buffer
+        w_ok = mbar_wait(&done[c % kTbBufs], (uint32_t)(c / kTbBufs - 1) & 1u, abort_flag, status);
+      if (!w_ok) {
         ok = false;
         break;
       }
-      load_chunk(c + kTbStages - 1);  // into the stage of chunk c - 1
-      uint8_t* buf = bufs + (c & 1) * kTbBuf;
-      const float* stg = ring + (c % kTbStages) * kTbStageFloats;
+      uint8_t* buf = bufs + (c % kTbBufs) * kTbBuf;
+      const float* stg = ring + st0 * kTbStageFloats;
 #pragma unroll
       for (int k = 0; k < kTbItems; ++k) {  // 8 values per item
         const int e = wt + k * kTbWorkers;
@@ -693,7 +685,15 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         const float* sp = stg + st * kTbStripFloats + r * 128 + g * 8;
         const float4 v0 = *reinterpret_cast<const float4*>(sp);
         const float4 v1 = *reinterpret_cast<const float4*>(sp + 4);
-        const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        if (!(mode == 2 && st >= ybase)) {  // E / Ph: columns past this unit's are not its own
+          const int nv = ncolX - scol[st] - g * 8;
+          if (nv < 8) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (t >= nv) x[t] = 0.0f;
+          }
+        }
         uint32_t h0[4], h1[4], h2[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -711,18 +711,18 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         *reinterpret_cast<uint4*>(base + 2 * kTbPart) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the parts, for the tensor cores
-      mbar_arrive(&ready[c & 1]);
+      mbar_arrive(&ready[c % kTbBufs]);
+      mbar_arrive(&empty[st0]);
     }
-    cp_async_wait_all();
   }
   if (!ok) *abort_flag = 1;
   if (threadIdx.x == 0) mma_commit(fin);  // covers every MMA issued (also after an abort)
   const bool fin_ok = mbar_wait(fin, 0, nullptr, status);
   if (__syncthreads_and(ok && fin_ok && !*abort_flag)) {
     tc_fence_after_sync();
-    const int q4 = warp & 3, cq = warp >> 2;  // TMEM lane quarter; columns [32 cq, 32 cq + 32) of a tile
+    const int q4 = warp & 3, cq = (warp >> 2) & 3;  // TMEM lane quarter; columns [32 cq, 32 cq + 32) of a tile
 #pragma unroll 1
-    for (int k = 0; k < ntiles; ++k) {
+    for (int k = 0; k < ntiles && warp < 16; ++k) {
       const bool dg = tg.sym && tmi[k] == tni[k];
       const int pr = tmi[k] * 128 + q4 * 32 + lane;
       float y[32];
@@ -749,7 +749,6 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
-
 
 // ------------------------------------------------------------------ blocked descents
 // Both fits are cyclic coordinate descents on normal equations: a step on
@@ -911,7 +910,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
     cntp = cnt;
     __syncthreads();
   }
-  float* wout = u.base + am_off_w(meta.R, m, u.ldE, meta.d);
+  float* wout = u.base + am_off_w(meta.R, meta.max_m, u.ldE, meta.d);
   const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
   for (int j = threadIdx.x; j < m; j += kAmThreads) {
     const float wj = w[j];
@@ -936,7 +935,7 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
   const int lane = threadIdx.x & 31;
   if (i >= meta.R) return;
   float* E = u.base + (int64_t)i * u.ldE;
-  const float* w = u.base + am_off_w(meta.R, u.m, u.ldE, meta.d);
+  const float* w = u.base + am_off_w(meta.R, meta.max_m, u.ldE, meta.d);
   float z = 0.0f;
   for (int j = lane; j < u.m; j += 32) z = fmaf(E[j], w[j], z);
 #pragma unroll
@@ -1025,7 +1024,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   float* thrb = hdiag + m;                                 // [m] 2^-17 pi_j; +inf where H_jj <= 0
   const float* Hm = u.base + am_off_G(meta.R, u.ldE);
   const int64_t ld = u.ldE;
-  float* Xg = u.base + am_off_Bm(meta.R, m, u.ldE, D);    // Bm, then X (row stride D)
+  float* Xg = u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, D);    // Bm, then X (row stride D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < m; i += kAmThreads / 32) {  // H_jj and pi_j, one warp per row
     const float* hr = Hm + (int64_t)i * ld;
@@ -1048,7 +1047,7 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   __syncthreads();
   {
     const int c = threadIdx.x % kVc;
-    const float* Y = u.base + am_off_Y(meta.R, m, u.ldE);
+    const float* Y = u.base + am_off_Y(meta.R, meta.max_m, u.ldE);
     float ym = 0.0f;
     for (int i = threadIdx.x / kVc; i < meta.R; i += kAmThreads / kVc)
       ym = fmaxf(ym, fabsf(Y[(int64_t)i * D + col0 + c]));
@@ -1224,7 +1223,8 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
         *al.tmK, *al.tmV, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
     const int g0 = atb_blocks_per_unit(0, m.max_m, D);
-    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(m, al.ws, 0, g0, al.status);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
+                                                                                0, g0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
@@ -1232,9 +1232,11 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
     const int g1 = atb_blocks_per_unit(1, m.max_m, D), g2 = atb_blocks_per_unit(2, m.max_m, D);
-    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(m, al.ws, 1, g1, al.status);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
+                                                                                1, g1, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(m, al.ws, 2, g2, al.status);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
+                                                                                2, g2, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);

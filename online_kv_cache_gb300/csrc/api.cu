@@ -414,6 +414,25 @@ kvc_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int d, in
   return KVC_OK;
 }
 
+// A launch's per-unit fp32 matrices as a 3-D tensor [unit][row][column]
+// (row stride ld floats, unit stride unit_floats floats) with a {128, 16, 1}
+// box and no swizzle: one box is 16 rows of a 128-column strip, dense in
+// shared memory; rows past `rows` and columns past `cols` read as zeros.
+kvc_status make_amap(CUtensorMap* map, const float* base, int64_t cols, int64_t rows, int64_t units, int64_t ld,
+                     int64_t unit_floats) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)units};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)unit_floats * 4};
+  const cuuint32_t box[3] = {128, 16, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled (AM operands) failed (%d)", (int)r);
+  return KVC_OK;
+}
+
 // The K pool as a 4-D tensor [row group][k-block][row in group][64 elements]
 // (k-blocks of 64 head-dim elements = 128 B, groups of 8 rows): one box of
 // {64, 8, d/64, P/8} fetches a whole page of one head in one copy and lands in
@@ -1187,6 +1206,11 @@ void build_am_plan(const kvc_cache* c, const Plan& p, int R, float scale, int sw
     am.Mtot = p.Mtot;
     const size_t a1 = std::min(act.size(), a0 + (size_t)kMaxSeqPerLaunch);
     am.nseq = (int)(a1 - a0);
+    for (size_t k = a0; k < a1; ++k) am.max_m = std::max(am.max_m, p.seqs[act[k]].m);
+    // every unit of the launch is laid out for its largest m (one row stride,
+    // one unit stride), so that one tensor map per operand covers the launch
+    const int ldE = (am.max_m + 1 + 3) & ~3;
+    const int64_t unit_floats = am_unit_floats(R, am.max_m, ldE, c->head_dim);
     int64_t units = 0;
     for (size_t k = a0; k < a1; ++k) {
       const size_t i = act[k];
@@ -1196,14 +1220,13 @@ void build_am_plan(const kvc_cache* c, const Plan& p, int R, float scale, int sw
       s.s0 = q.s0;
       s.n = q.n;
       s.m = q.m;
-      s.ldE = (q.m + 1 + 3) & ~3;
+      s.ldE = ldE;
       s.moff = p.moff[i];
       s.unit0 = units;
       s.ws = wsf;
-      s.unit_floats = am_unit_floats(R, q.m, s.ldE, c->head_dim);
+      s.unit_floats = unit_floats;
       units += LH;
       wsf += LH * s.unit_floats;
-      am.max_m = std::max(am.max_m, q.m);
     }
     am.units = units;
     out->metas.push_back(am);
@@ -1290,12 +1313,26 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   if ((st = make_kmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
   if ((st = make_kmap(&tmV, cache->v_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
   if ((st = make_tmap(&tmQ, q, qrows, cache->head_dim, kScoreTile)) != KVC_OK) return st;
+  // per launch chunk: the units' E / Ph and Y for the Gram products
+  std::vector<CUtensorMap> tmX(ap.metas.size()), tmY(ap.metas.size());
+  for (size_t ci = 0; ci < ap.metas.size(); ++ci) {
+    const AmMeta& am = ap.metas[ci];
+    const float* base = static_cast<const float*>(ws) + am.seq[0].ws;
+    const int ldE = am.seq[0].ldE;
+    const int64_t uf = am.seq[0].unit_floats;
+    if ((st = make_amap(&tmX[ci], base, ldE, R, am.units, ldE, uf)) != KVC_OK) return st;
+    if ((st = make_amap(&tmY[ci], base + am_off_Y(R, am.max_m, ldE), cache->head_dim, R, am.units,
+                        cache->head_dim, uf)) != KVC_OK)
+      return st;
+  }
   AmLaunch al;
   al.chunks = ap.metas.size();
   al.meta = ap.metas.data();
   al.tmK = &tmK;
   al.tmV = &tmV;
   al.tmQ = &tmQ;
+  al.tmX = tmX.data();
+  al.tmY = tmY.data();
   al.lse_rows = lse_rows;
   al.block_table = cache->block_table;
   al.k_pool = cache->k_pool;

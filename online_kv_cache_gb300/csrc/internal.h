@@ -158,12 +158,12 @@ constexpr int kLrfuMaxSegment = 1 << 20;
 //   w   [m4]       fitted exp(beta)
 struct AmSeq {
   int32_t b, s0, n, m;
-  int32_t ldE;          // row stride of E and G: m + 1 rounded up to a multiple of 4
+  int32_t ldE;          // row stride of E and G: the launch's largest m + 1, rounded up to a multiple of 4
   int32_t pad;
   int64_t moff;         // offset of the sequence in [L][H][Mtot]
   int64_t unit0;        // first unit of the sequence in this launch
   int64_t ws;           // float offset of the sequence's first unit in the workspace
-  int64_t unit_floats;  // workspace floats per unit
+  int64_t unit_floats;  // workspace floats per unit (every unit of a launch laid out for its largest m)
 };
 
 struct AmMeta {
@@ -202,6 +202,8 @@ struct AmLaunch {
   const CUtensorMap* tmK = nullptr;  // K pool, one page per box (as the scoring passes)
   const CUtensorMap* tmV = nullptr;  // V pool, same geometry
   const CUtensorMap* tmQ = nullptr;  // Q, box {64, 128}
+  const CUtensorMap* tmX = nullptr;  // [chunks] the units' E / Ph (fp32 [unit][R][ldE]), box {128, 16, 1}
+  const CUtensorMap* tmY = nullptr;  // [chunks] the units' Y (fp32 [unit][R][d]), box {128, 16, 1}
   const float* lse_rows = nullptr;   // [B][L][H][R] natural-log LSE of every proxy row
   const int32_t* block_table = nullptr;
   const void* k_pool = nullptr;
