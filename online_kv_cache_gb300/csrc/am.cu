@@ -460,22 +460,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // C is cut into 128 x 128 tiles.  G's first m columns and H are symmetric:
 // only tiles with p0 <= q0 are computed, and each also writes its transpose
 // (a diagonal tile writes its upper triangle and mirrors it), so both
-// triangles hold the same numbers.  A block of 512 threads takes up to three
-// consecutive tiles of the unit (row-major over the computed ones), one
-// 128-column TMEM accumulator each, and the distinct 128-column strips they
-// read (at most four: modes 0 and 1 read both operands from the same matrix,
-// E's strips taken over the m + 1 columns of [E | s]), so a strip shared by
-// its tiles is staged and split once.  Per chunk of 16 proxy rows the strips'
-// fp32 rows arrive by 16-byte cp.async (zero past R and past the columns) in
-// a ring of four stages, three chunks ahead; a worker splits 8
-// consecutive values at a time with the packed fp32->bf16x2 conversion and
-// writes the parts as MN-major operands (1024-byte atoms of 8 rows x 64
-// elements along p or q: LBO = 1024 B along p/q, SBO = 2048 B along the
-// rows).  Warps 1-15 stage and split (a named barrier among them per chunk)
-// and signal the operand buffer on an mbarrier; one thread of warp 0 only
-// issues the six MMAs per tile (M = N = 128, K = 16, both operands MN-major)
-// and commits them to the buffer's "done" mbarrier.  Two operand buffers:
-// the split of chunk c + 1 overlaps the MMAs of chunk c.
+// triangles hold the same numbers.  A block takes up to three consecutive
+// tiles of the unit (row-major over the computed ones), one 128-column TMEM
+// accumulator each, and the distinct 128-column strips they read (at most
+// four: modes 0 and 1 read both operands from the same matrix, E's strips
+// taken over the m + 1 columns of [E | s]), so a strip shared by its tiles is
+// loaded and split once.  Per chunk of 16 proxy rows, warp 16 loads each strip
+// as one TMA box of the launch's 3-D tensor map (every unit of a launch is laid
+// out for the launch's largest m: rows past R and columns past the map read as
+// zeros) into a ring of two stages (full / empty mbarriers); warps 1-15 split
+// 8 consecutive values at a time with the packed fp32->bf16x2 conversion
+// (values past the unit's own columns become zeros) and write the parts as
+// MN-major operands (1024-byte atoms of 8 rows x 64 elements along p or q:
+// LBO = 1024 B along p/q, SBO = 2048 B along the rows) into one of three
+// operand buffers, then arrive on its "ready" mbarrier; one thread of warp 0
+// only issues the six MMAs per tile (M = N = 128, K = 16, both operands
+// MN-major) and commits them to the buffer's "done" mbarrier.
 constexpr int kTbThreads = 544;                             // warp 0 issues, warps 1-15 split, warp 16 loads
 constexpr int kTbRows = 16;                                 // proxy rows per chunk (one K step)
 constexpr int kTbTiles = 3;                                 // output tiles per block
