@@ -28,6 +28,8 @@
 //   am_mass_kernel     w by projected coordinate descent; beta = ln w
 //   am_probs_kernel    Ph = rows of E diag(w), normalised (in place)
 //   am_atb_tc_kernel   H = Ph^T Ph, Bm = Ph^T Y     (modes 1, 2)
+//   am_x0_kernel       X0 = the kept values (fp32)
+//   am_atb_tc_kernel   H X0 - Bm, the value fit's starting gradient (mode 3)
 //   am_value_kernel    V_C by coordinate descent; written to the pool (bf16)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,17 +58,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kAmGuard = 7.62939453125e-06f;  // 2^-17
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
-
-__device__ __forceinline__ void unpack8(const uint4 v, float* out) {
-  out[0] = bf16_bits_to_float(v.x & 0xffffu);
-  out[1] = bf16_bits_to_float(v.x >> 16);
-  out[2] = bf16_bits_to_float(v.y & 0xffffu);
-  out[3] = bf16_bits_to_float(v.y >> 16);
-  out[4] = bf16_bits_to_float(v.z & 0xffffu);
-  out[5] = bf16_bits_to_float(v.z >> 16);
-  out[6] = bf16_bits_to_float(v.w & 0xffffu);
-  out[7] = bf16_bits_to_float(v.w >> 16);
-}
 
 struct AmUnit {
   int k;        // sequence index within the launch
@@ -450,6 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //   mode 0: A = E (m columns), B = [E | s] (m + 1), C = G        (stride ldE)
 //   mode 1: A = B = Ph (m columns),                 C = H in G's place
 //   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d)
+//   mode 3: A = H (m rows), B = X0 (the kept values), C = H X0 - Bm in Bm's
+//           place (the value fit's starting gradient; H is symmetric)
 // on tcgen05 with fp32-level accuracy: every fp32 value
 // x is split into three bf16 parts (x0 = bf16(x), x1 = bf16(x - x0),
 // x2 = bf16(x - x0 - x1): 8 + 8 + 8 significant bits, x0 + x1 + x2 = x to the
@@ -475,7 +468,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // LBO = 1024 B along p/q, SBO = 2048 B along the rows) into one of three
 // operand buffers, then arrive on its "ready" mbarrier; one thread of warp 0
 // only issues the six MMAs per tile (M = N = 128, K = 16, both operands
-// MN-major) and commits them to the buffer's "done" mbarrier.
+// MN-major) and commits them to the buffer's "done" mbarrier.  The epilogue
+// turns each warp's 32 x 32 block of C around in shared memory so that its
+// stores run along rows.
 constexpr int kTbThreads = 544;                             // warp 0 issues, warps 1-15 split, warp 16 loads
 constexpr int kTbRows = 16;                                 // proxy rows per chunk (one K step)
 constexpr int kTbTiles = 3;                                 // output tiles per block
@@ -511,8 +506,8 @@ struct TileGrid {
 __host__ __device__ inline TileGrid tile_grid(int mode, int m, int d) {
   TileGrid g;
   g.mt = (m + kAtbTile - 1) / kAtbTile;
-  g.nt = mode == 2 ? (d + kAtbTile - 1) / kAtbTile : (mode == 0 ? m + 1 + kAtbTile - 1 : m + kAtbTile - 1) / kAtbTile;
-  g.sym = mode != 2;
+  g.nt = mode >= 2 ? (d + kAtbTile - 1) / kAtbTile : (mode == 0 ? m + 1 + kAtbTile - 1 : m + kAtbTile - 1) / kAtbTile;
+  g.sym = mode < 2;
   return g;
 }
 // blocks per unit for the largest m of a launch
@@ -526,7 +521,7 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 }
 
 __global__ void __launch_bounds__(kTbThreads, 1)
-    am_atb_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+    am_atb_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const AmMeta meta, float* ws, int mode, int blocks_per_unit, unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
   uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [kTbBufs] an operand buffer's MMAs are done
@@ -543,12 +538,13 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   const AmUnit u = am_unit(meta, unit, ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
+  const int K = mode == 3 ? u.m : meta.R;  // the rows summed over
   const TileGrid tg = tile_grid(mode, M, meta.d);
   const int t0 = (int)(blockIdx.x % blocks_per_unit) * kTbTiles;
   const int ntiles = min(kTbTiles, tg.count() - t0);
   if (ntiles <= 0) return;
   // the block's tiles and strips: strip slot k holds the 128 columns from
-  // scol[k] of E / Ph, or (mode 2, slots from ybase on) of Y; tile k reads
+  // scol[k] of A, or (modes 2 and 3, slots from ybase on) of B; tile k reads
   // slots sa[k] and sb[k]
   int tmi[kTbTiles], tni[kTbTiles], sa[kTbTiles], sb[kTbTiles];
   int scol[kTbStrips];
@@ -571,7 +567,7 @@ __global__ void __launch_bounds__(kTbThreads, 1)
 #pragma unroll
   for (int k = 0; k < kTbTiles; ++k) {
     if (k >= ntiles) continue;
-    if (mode == 2) {
+    if (mode >= 2) {
       const int col = tni[k] * 128;
       int found = -1;
       for (int st = ybase; st < nstr; ++st)
@@ -585,14 +581,15 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       sb[k] = find_or_add(tni[k] * 128);
     }
   }
-  // columns of a strip inside the unit's matrix (the maps run to the launch's
-  // row stride): mode 0 takes E over the m + 1 columns of [E | s] (row m of C
-  // is not kept), so that one strip serves both operands of a diagonal tile
+  // columns of an A strip inside the unit's matrix (the maps run to the
+  // launch's row stride): mode 0 takes E over the m + 1 columns of [E | s]
+  // (row m of C is not kept), so that one strip serves both operands of a
+  // diagonal tile; B's maps (Y, X0) end at d
   const int ncolX = mode == 0 ? N : M;
-  float* C = mode == 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
-  const int ldc = mode == 2 ? meta.d : u.ldE;
+  float* C = mode >= 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
+  const int ldc = mode >= 2 ? meta.d : u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchunks = (meta.R + kTbRows - 1) / kTbRows;
+  const int nchunks = (K + kTbRows - 1) / kTbRows;
   if (threadIdx.x == 0) {
     for (int b = 0; b < kTbBufs; ++b) {
       mbar_init(&done[b], 1);
@@ -654,8 +651,8 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         mbar_arrive_expect_tx(&full[st], (uint32_t)nstr * kTbStripFloats * 4);
         float* stg = ring + st * kTbStageFloats;
         for (int k = 0; k < nstr; ++k) {
-          const bool fromY = mode == 2 && k >= ybase;
-          tma_load_3d(stg + k * kTbStripFloats, fromY ? &tmY : &tmX, &full[st], scol[k], c * kTbRows, (int)unit);
+          const bool fromB = mode >= 2 && k >= ybase;
+          tma_load_3d(stg + k * kTbStripFloats, fromB ? &tmB : &tmA, &full[st], scol[k], c * kTbRows, (int)unit);
         }
         issued = c + 1;
       }
@@ -686,13 +683,13 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         const float4 v0 = *reinterpret_cast<const float4*>(sp);
         const float4 v1 = *reinterpret_cast<const float4*>(sp + 4);
         float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        if (!(mode == 2 && st >= ybase)) {  // E / Ph: columns past this unit's are not its own
-          const int nv = ncolX - scol[st] - g * 8;
-          if (nv < 8) {
+        // A's columns past this unit's, and (mode 3: the maps run to the launch's
+        // largest m) rows past it, are not its own
+        const int nv = c * kTbRows + r >= K ? 0 : (mode >= 2 && st >= ybase ? 8 : ncolX - scol[st] - g * 8);
+        if (nv < 8) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-              if (t >= nv) x[t] = 0.0f;
-          }
+          for (int t = 0; t < 8; ++t)
+            if (t >= nv) x[t] = 0.0f;
         }
         uint32_t h0[4], h1[4], h2[4];
 #pragma unroll
@@ -721,24 +718,43 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   if (__syncthreads_and(ok && fin_ok && !*abort_flag)) {
     tc_fence_after_sync();
     const int q4 = warp & 3, cq = (warp >> 2) & 3;  // TMEM lane quarter; columns [32 cq, 32 cq + 32) of a tile
+    // The operand buffers are free now: each warp turns its 32 x 32 block
+    // around in shared memory, so that a store (and mode 3's load) covers 32
+    // consecutive columns of one row.
+    float* tr = reinterpret_cast<float*>(bufs) + warp * 32 * 33;
 #pragma unroll 1
     for (int k = 0; k < ntiles && warp < 16; ++k) {
       const bool dg = tg.sym && tmi[k] == tni[k];
-      const int pr = tmi[k] * 128 + q4 * 32 + lane;
+      const int p0w = tmi[k] * 128 + q4 * 32, pr = p0w + lane;
       float y[32];
       tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(k * 128 + cq * 32), y);
       const int qb = tni[k] * 128 + cq * 32;
-      if (pr < M) {
-        float* dst = C + (int64_t)pr * ldc + qb;
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (qb + t < N && (!dg || qb + t >= pr)) dst[t] = y[t];
-      }
       if (tg.sym) {  // the transpose: C[q][p] for q < m (not G's column m), lanes along p coalesced
 #pragma unroll
         for (int t = 0; t < 32; ++t)
           if (pr < M && qb + t < M && qb + t > pr) C[(int64_t)(qb + t) * ldc + pr] = y[t];
       }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) tr[lane * 33 + t] = y[t];
+      __syncwarp();
+      const int q = qb + lane;  // this lane's column; rows p0w .. p0w + 31
+      if (mode == 3) {  // C = H X0 - Bm, 16 rows at a time: their Bm values first
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 16) {
+          float bm[16];
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            bm[r] = (p0w + r0 + r < M && q < N) ? C[(int64_t)(p0w + r0 + r) * ldc + q] : 0.0f;
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (p0w + r0 + r < M && q < N) C[(int64_t)(p0w + r0 + r) * ldc + q] = tr[(r0 + r) * 33 + lane] - bm[r];
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (p0w + r < M && q < N && (!dg || q >= p0w + r)) C[(int64_t)(p0w + r) * ldc + q] = tr[r * 33 + lane];
+      }
+      __syncwarp();
     }
   }
   tc_fence_before_sync();
@@ -944,6 +960,37 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
   for (int j = lane; j < u.m; j += 32) E[j] = E[j] * w[j] * inv;
 }
 
+// ------------------------------------------------------------------ kept values
+// Block = (unit, 8 kept entries), one warp per entry: X0[j] = the kept entry's
+// V row (bf16 -> fp32) into the unit's X region (zero for a bad page or
+// position, which is reported).
+template <int D>
+__global__ void __launch_bounds__(kAmThreads) am_x0_kernel(const AmMeta meta, const int32_t* __restrict__ bt,
+                                                           const int32_t* __restrict__ keep,
+                                                           const uint16_t* __restrict__ vp, float* ws,
+                                                           unsigned* status) {
+  const int jb = (meta.max_m + 7) / 8;
+  const AmUnit u = am_unit(meta, blockIdx.x / jb, ws);
+  const int j = (int)(blockIdx.x % jb) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= u.m) return;
+  int64_t row = -1;
+  if (lane == 0) {
+    const int pos = am_kept(meta, u, keep, j, status);
+    row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
+  }
+  row = __shfl_sync(0xffffffffu, row, 0);
+  float* X = u.base + am_off_X(meta.R, meta.max_m, u.ldE, D) + (int64_t)j * D;
+  for (int e = lane * 2; e < D; e += 64) {
+    float2 v = make_float2(0.0f, 0.0f);
+    if (row >= 0) {
+      const uint32_t b2 = *reinterpret_cast<const uint32_t*>(vp + row * D + e);
+      v = make_float2(bf16_bits_to_float(b2 & 0xffffu), bf16_bits_to_float(b2 >> 16));
+    }
+    *reinterpret_cast<float2*>(X + e) = v;
+  }
+}
+
 // ------------------------------------------------------------------ value fit
 // Block = (unit, 16 of the d value columns).  The columns are independent
 // least-squares problems sharing H = Ph^T Ph: cyclic coordinate descent from
@@ -952,9 +999,10 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
 // pi_j S_c (pi_j = sum_k H_jk, S_c = max_i |Y_ic| + max_k |X0_kc|: the scale
 // of the gradient's terms in column c).  In a block's steps lane c of warp 0
 // holds column c of the block's 32 gradient rows; the diagonal tile's row t
-// is read as a broadcast.  X lives in the workspace in Bm's place (Bm is read
-// once into the gradient).  At the end V_C is written to `vc` (fp32) and over
-// the kept entries' V rows (bf16, round to nearest even).
+// is read as a broadcast.  The starting gradient H X0 - Bm comes from the
+// tensor-core Gram kernel (mode 3, in Bm's place) and X0 from am_x0_kernel;
+// X lives in its own workspace region.  At the end V_C is written to `vc`
+// (fp32) and over the kept entries' V rows (bf16, round to nearest even).
 constexpr int kVc = 16;  // value columns per block
 __host__ __device__ constexpr int value_ld(int m) { return m | 1; }
 constexpr int kValueHead = 2 * kDb * kVc + 4 * kTile + 2 * kVc + 4;  // moves, tiles, scales, flags
@@ -1024,7 +1072,8 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   float* thrb = hdiag + m;                                 // [m] 2^-17 pi_j; +inf where H_jj <= 0
   const float* Hm = u.base + am_off_G(meta.R, u.ldE);
   const int64_t ld = u.ldE;
-  float* Xg = u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, D);    // Bm, then X (row stride D)
+  const float* G0 = u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, D);  // H X0 - Bm (row stride D)
+  float* Xg = u.base + am_off_X(meta.R, meta.max_m, u.ldE, D);           // X, from X0 (row stride D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < m; i += kAmThreads / 32) {  // H_jj and pi_j, one warp per row
     const float* hr = Hm + (int64_t)i * ld;
@@ -1038,9 +1087,9 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
       thrb[i] = d > 0.0f ? kAmGuard * ps : INFINITY;
     }
   }
-  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {  // Gv = -Bm to start
+  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {  // the starting gradient H X0 - Bm (Bm's place)
     const int i = e / kVc, c = e % kVc;
-    Gs[c * ldv + i] = -Xg[(int64_t)i * D + col0 + c];
+    Gs[c * ldv + i] = G0[(int64_t)i * D + col0 + c];
   }
   if (threadIdx.x < 2 * kVc) S[threadIdx.x] = 0.0f;  // S: max |Y| bits, Sx: max |X0| bits
   if (threadIdx.x < 2) moved[threadIdx.x] = 0;
@@ -1048,41 +1097,17 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   {
     const int c = threadIdx.x % kVc;
     const float* Y = u.base + am_off_Y(meta.R, meta.max_m, u.ldE);
-    float ym = 0.0f;
+    float ym = 0.0f, xm = 0.0f;
     for (int i = threadIdx.x / kVc; i < meta.R; i += kAmThreads / kVc)
       ym = fmaxf(ym, fabsf(Y[(int64_t)i * D + col0 + c]));
+    for (int j = threadIdx.x / kVc; j < m; j += kAmThreads / kVc)
+      xm = fmaxf(xm, fabsf(Xg[(int64_t)j * D + col0 + c]));
     atomicMax(reinterpret_cast<int*>(S) + c, __float_as_int(ym));  // non-negative floats order as ints
-  }
-  for (int j = threadIdx.x; j < m; j += kAmThreads) {  // X = the kept entries' values
-    const int pos = am_kept(meta, u, keep, j, status);
-    const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
-    float v[kVc];
-    if (row >= 0) {
-      unpack8(*reinterpret_cast<const uint4*>(vp + row * D + col0), v);
-      unpack8(*reinterpret_cast<const uint4*>(vp + row * D + col0 + 8), v + 8);
-    } else {
-#pragma unroll
-      for (int e = 0; e < kVc; ++e) v[e] = 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < kVc; ++e) {
-      Xg[(int64_t)j * D + col0 + e] = v[e];
-      atomicMax(reinterpret_cast<int*>(Sx) + e, __float_as_int(fabsf(v[e])));
-    }
+    atomicMax(reinterpret_cast<int*>(Sx) + c, __float_as_int(xm));
   }
   __syncthreads();
   if (threadIdx.x < kVc) S[threadIdx.x] += Sx[threadIdx.x];
   const int nb = (m + kDb - 1) / kDb;
-  for (int b = 0; b < nb; ++b) {  // Gv += H X0, 32 coordinates at a time
-    const int j0 = b * kDb, cnt = min(kDb, m - j0);
-    for (int e = threadIdx.x; e < kDb * kVc; e += kAmThreads) {
-      const int t = e / kVc, c = e % kVc;
-      dxs[e] = t < cnt ? Xg[(int64_t)(j0 + t) * D + col0 + c] : 0.0f;
-    }
-    __syncthreads();
-    value_update(Hm, ld, m, ldv, j0, cnt, dxs, Gs, 0, 0, 0, 0, threadIdx.x, kAmThreads);
-    __syncthreads();
-  }
   stage_tile(tiles, Hm, ld, 0, min(kDb, m), 0, min(kDb, m), threadIdx.x, kAmThreads);  // block 0's diagonal
   cp_async_commit();
   cp_async_wait_all();
@@ -1220,10 +1245,14 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if (m.units <= 0) continue;
     const int rbt = (m.R + kTcRows - 1) / kTcRows;
     am_targets_tc_kernel<D><<<(unsigned)(m.units * rbt), kTcThreads, tc_smem_bytes<D>(), stream>>>(
-        *al.tmK, *al.tmV, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
+        *al.tmK, *al.tmVp, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    const int g0 = atb_blocks_per_unit(0, m.max_m, D);
-    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
+    am_x0_kernel<D><<<(unsigned)(m.units * ((m.max_m + 7) / 8)), kAmThreads, 0, stream>>>(
+        m, al.block_table, al.keep, vp, al.ws, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+    const int g0 = atb_blocks_per_unit(0, m.max_m, D), g1 = atb_blocks_per_unit(1, m.max_m, D);
+    const int g2 = atb_blocks_per_unit(2, m.max_m, D), g3 = atb_blocks_per_unit(3, m.max_m, D);
+    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws,
                                                                                 0, g0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
@@ -1231,12 +1260,14 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if ((e = check()) != cudaSuccess) return e;
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
-    const int g1 = atb_blocks_per_unit(1, m.max_m, D), g2 = atb_blocks_per_unit(2, m.max_m, D);
-    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
+    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws,
                                                                                 1, g1, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
                                                                                 2, g2, al.status);
+    if ((e = check()) != cudaSuccess) return e;
+    am_atb_tc_kernel<<<(unsigned)(m.units * g3), kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmV[ci], m, al.ws,
+                                                                                3, g3, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);

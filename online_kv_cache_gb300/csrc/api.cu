@@ -1314,25 +1314,29 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   if ((st = make_kmap(&tmV, cache->v_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;
   if ((st = make_tmap(&tmQ, q, qrows, cache->head_dim, kScoreTile)) != KVC_OK) return st;
   // per launch chunk: the units' E / Ph and Y for the Gram products
-  std::vector<CUtensorMap> tmX(ap.metas.size()), tmY(ap.metas.size());
-  for (size_t ci = 0; ci < ap.metas.size(); ++ci) {
+  const size_t nc = ap.metas.size();
+  std::vector<CUtensorMap> tmX(nc), tmY(nc), tmH(nc), tmX0(nc);
+  for (size_t ci = 0; ci < nc; ++ci) {
     const AmMeta& am = ap.metas[ci];
     const float* base = static_cast<const float*>(ws) + am.seq[0].ws;
-    const int ldE = am.seq[0].ldE;
+    const int ldE = am.seq[0].ldE, d = cache->head_dim;
     const int64_t uf = am.seq[0].unit_floats;
-    if ((st = make_amap(&tmX[ci], base, ldE, R, am.units, ldE, uf)) != KVC_OK) return st;
-    if ((st = make_amap(&tmY[ci], base + am_off_Y(R, am.max_m, ldE), cache->head_dim, R, am.units,
-                        cache->head_dim, uf)) != KVC_OK)
+    if ((st = make_amap(&tmX[ci], base, ldE, R, am.units, ldE, uf)) != KVC_OK ||
+        (st = make_amap(&tmY[ci], base + am_off_Y(R, am.max_m, ldE), d, R, am.units, d, uf)) != KVC_OK ||
+        (st = make_amap(&tmH[ci], base + am_off_G(R, ldE), ldE, am.max_m, am.units, ldE, uf)) != KVC_OK ||
+        (st = make_amap(&tmX0[ci], base + am_off_X(R, am.max_m, ldE, d), d, am.max_m, am.units, d, uf)) != KVC_OK)
       return st;
   }
   AmLaunch al;
   al.chunks = ap.metas.size();
   al.meta = ap.metas.data();
   al.tmK = &tmK;
-  al.tmV = &tmV;
+  al.tmVp = &tmV;
   al.tmQ = &tmQ;
   al.tmX = tmX.data();
   al.tmY = tmY.data();
+  al.tmH = tmH.data();
+  al.tmV = tmX0.data();
   al.lse_rows = lse_rows;
   al.block_table = cache->block_table;
   al.k_pool = cache->k_pool;

@@ -187,8 +187,12 @@ __host__ __device__ inline int64_t am_off_Bm(int R, int m, int ldE, int d) { ret
 __host__ __device__ inline int64_t am_off_w(int R, int m, int ldE, int d) {
   return am_off_Bm(R, m, ldE, d) + (int64_t)m * d;
 }
+// X: the value fit's unknowns [m][d] (16-byte aligned: a tensor map reads it)
+__host__ __device__ inline int64_t am_off_X(int R, int m, int ldE, int d) {
+  return (am_off_w(R, m, ldE, d) + ((m + 3) & ~3) + 3) & ~int64_t(3);
+}
 __host__ __device__ inline int64_t am_unit_floats(int R, int m, int ldE, int d) {
-  const int64_t x = am_off_w(R, m, ldE, d) + ((m + 3) & ~3);
+  const int64_t x = am_off_X(R, m, ldE, d) + (int64_t)m * d;
   return (x + 63) & ~int64_t(63);  // 256-byte aligned units
 }
 
@@ -200,10 +204,13 @@ struct AmLaunch {
   size_t chunks = 0;
   const AmMeta* meta = nullptr;  // [chunks]
   const CUtensorMap* tmK = nullptr;  // K pool, one page per box (as the scoring passes)
-  const CUtensorMap* tmV = nullptr;  // V pool, same geometry
+  const CUtensorMap* tmVp = nullptr;  // V pool, same geometry
   const CUtensorMap* tmQ = nullptr;  // Q, box {64, 128}
-  const CUtensorMap* tmX = nullptr;  // [chunks] the units' E / Ph (fp32 [unit][R][ldE]), box {128, 16, 1}
-  const CUtensorMap* tmY = nullptr;  // [chunks] the units' Y (fp32 [unit][R][d]), box {128, 16, 1}
+  // [chunks] fp32 operands of the Gram products, [unit][row][column] with a {128, 16, 1} box
+  const CUtensorMap* tmX = nullptr;  // E / Ph: [unit][R][ldE]
+  const CUtensorMap* tmY = nullptr;  // Y: [unit][R][d]
+  const CUtensorMap* tmH = nullptr;  // H (in G's place): [unit][largest m][ldE]
+  const CUtensorMap* tmV = nullptr;  // X0: [unit][largest m][d]
   const float* lse_rows = nullptr;   // [B][L][H][R] natural-log LSE of every proxy row
   const int32_t* block_table = nullptr;
   const void* k_pool = nullptr;
