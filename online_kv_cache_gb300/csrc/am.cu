@@ -141,8 +141,8 @@ constexpr int kTcHead = 1024;  // barriers, TMEM address, abort flag
 template <int D>
 constexpr int tc_tile_bytes() { return kTcKeys * D * 2; }
 template <int D>
-constexpr int tc_smem_bytes() {  // head, alignment slack, Q rows, kTcStages x (K tile, V tile), keep list
-  return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4;
+constexpr int tc_smem_bytes() {  // head, slack, Q rows, kTcStages x (K tile, V tile), keep list, 4 x 32 x 33 turn-around
+  return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4 + 4 * 32 * 33 * 4;
 }
 static_assert(tc_smem_bytes<128>() <= 227 * 1024, "targets working set fits one CTA's shared memory");
 
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            ~uintptr_t(1023));
   uint8_t* sKV = sQ + kTcRows * D * 2;            // stage s: K at s * 2 * kTile, V at + kTile
   int32_t* sKeep = reinterpret_cast<int32_t*>(sKV + kTcStages * 2 * kTile);  // the unit's kept positions
+  float* sTr = reinterpret_cast<float*>(sKeep + kAmMaxM);  // [4 epilogue warps][32][33] turn-around
   float* red = reinterpret_cast<float*>(tc_smem + 576);  // [6] warp maxima of the rows' LSE
 
   const int rb = (meta.R + kTcRows - 1) / kTcRows;
@@ -335,6 +336,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int w = 1; w < kTcThreads / 32; ++w) c = fmaxf(c, red[w]);
     const float cc = c * kLog2e;
     float* Erow = u.base + (int64_t)i * u.ldE;  // E[i][k] = exp(L_i,keep[k] - c), column m = s_i
+    // stores of E and Y go through the warp's 32 x 33 turn-around, so that each
+    // runs along one row (lane = column) instead of down 32 rows (lane = row)
+    float* tr = sTr + (warp - 2) * 32 * 33;
+    const int iw = r0 + q4 * 32;                // the warp's first proxy row
+    float* Ew = u.base + (int64_t)iw * u.ldE;
     int kk = 0;                                 // first kept position not yet passed
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
@@ -347,20 +353,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
          // eight columns per load-and-wait
         int k_end = kk;
         while (k_end < u.m && sKeep[k_end] < (t + 1) * kTcKeys) ++k_end;
-        for (int k0 = kk; k0 < k_end; k0 += 8) {
-          uint32_t a[8];
+        for (int kc = kk; kc < k_end; kc += 32) {  // 32 kept columns at a time
+          const int nk = min(32, k_end - kc);
+          for (int k0 = kc; k0 < kc + nk; k0 += 8) {
+            uint32_t a[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = min(k0 + e, k_end - 1);
-            a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
-          }
-          float ev[8];
-          tmem_ld1x8(a, ev);
-          if (i < meta.R) {
+            for (int e = 0; e < 8; ++e) {
+              const int k = min(k0 + e, k_end - 1);
+              a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
+            }
+            float ev[8];
+            tmem_ld1x8(a, ev);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              if (k0 + e < k_end) Erow[k0 + e] = exp2f(fmaf(ev[e], c2, -cc));
+              if (k0 + e < kc + nk) tr[lane * 33 + (k0 - kc) + e] = exp2f(fmaf(ev[e], c2, -cc));
           }
+          __syncwarp();
+          if (lane < nk) {
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr)
+              if (iw + rr < meta.R) Ew[(int64_t)rr * u.ldE + kc + lane] = tr[rr * 33 + lane];
+          }
+          __syncwarp();
         }
         kk = k_end;
       }
@@ -408,16 +422,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (ok) {
       tc_fence_after_sync();
-      float* Y = u.base + am_off_Y(meta.R, meta.max_m, u.ldE);
-#pragma unroll
+      float* Yw = u.base + am_off_Y(meta.R, meta.max_m, u.ldE) + (int64_t)iw * D;
+#pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         float y[32];
         tmem_ld32(t_lane + kColY + col, y);
-        if (i < meta.R) {
-          float4* dst = reinterpret_cast<float4*>(Y + (int64_t)i * D + col);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dst[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
-        }
+        for (int e = 0; e < 32; ++e) tr[lane * 33 + e] = y[e];
+        __syncwarp();
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr)
+          if (iw + rr < meta.R) Yw[(int64_t)rr * D + col + lane] = tr[rr * 33 + lane];
+        __syncwarp();
       }
       if (i < meta.R) {
         u.base[am_off_lse(meta.R, meta.max_m, u.ldE, D) + i] = lse;
