@@ -1130,11 +1130,23 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   __syncthreads();
   const int64_t iters = (int64_t)meta.sweeps * nb;
   int jp = 0, cntp = 0;  // the previous block
-  for (int64_t it = 0; it < iters; ++it) {
+  int64_t it = 0;
+  for (; it < iters; ++it) {
     const int cur = (int)(it & 1), prev = cur ^ 1;
     const int j0 = (int)(it % nb) * kDb, cnt = min(kDb, m - j0);
     const float* dtile = tiles + cur * 2 * kTile;  // diag[t][k] = H[j0 + t][j0 + k]
     const float* ctile = dtile + kTile;            // cross[t][k] = H[jp + t][j0 + k]
+    if (j0 == 0 && moved[prev] == 0) {
+      // A sweep starts with every gradient entry current.  If no coordinate
+      // would move in any column, none ever will: the fixed point is reached.
+      bool would = false;
+      for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
+        const int i = e % m, c = e / m;
+        const float gi = Gs[c * ldv + i];
+        would |= fabsf(gi) > thrb[i] * S[c] && -gi * hdiag[i] != 0.0f;
+      }
+      if (!__syncthreads_or(would)) break;
+    }
     float* dxc = dxs + cur * kDb * kVc;
     const float* dxp = dxs + prev * kDb * kVc;
     if (warp == 0) {
@@ -1216,8 +1228,8 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
     cntp = cnt;
     __syncthreads();
   }
-  if (iters > 0 && moved[(iters - 1) & 1]) value_moves(Xg, D, col0, jp, cntp, dxs + ((iters - 1) & 1) * kDb * kVc,
-                                                        threadIdx.x, kAmThreads);
+  if (it > 0 && moved[(it - 1) & 1])  // the last block's moves into X
+    value_moves(Xg, D, col0, jp, cntp, dxs + ((it - 1) & 1) * kDb * kVc, threadIdx.x, kAmThreads);
   __syncthreads();
   const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
   for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
