@@ -836,7 +836,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
   if (m <= 0) return;
   float* dws = am_smem;                                       // [2][32] moves of the last two blocks
   float* tiles = dws + 2 * kDb;                               // [2][2][kTile]
-  int* moved = reinterpret_cast<int*>(tiles + 4 * kTile);     // [2] did that block move
+  int* moved = reinterpret_cast<int*>(tiles + 4 * kTile);     // [2] did that block move; [2] did this sweep
   float* g = am_smem + kMassHead;                             // [m] gradient G w - b
   float* w = g + m;                                           // [m]
   float* thr = w + m;                                         // [m] 2^-17 b_j; +inf where G_jj <= 0
@@ -858,7 +858,7 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
       diag[i] = d;
     }
   }
-  if (threadIdx.x < 2) moved[threadIdx.x] = 0;
+  if (threadIdx.x < 3) moved[threadIdx.x] = 0;
   const int nb = (m + kDb - 1) / kDb;
   stage_tile(tiles, G, ld, 0, min(kDb, m), 0, min(kDb, m), threadIdx.x, kAmThreads);  // block 0's diagonal
   cp_async_commit();
@@ -871,6 +871,9 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
     const int j0 = (int)(it % nb) * kDb, cnt = min(kDb, m - j0);
     const float* dtile = tiles + cur * 2 * kTile;  // diag[t][k] = G[j0 + t][j0 + k]
     const float* ctile = dtile + kTile;            // cross[t][k] = G[jp + t][j0 + k]
+    // A sweep in which no coordinate moved left g and w as they were, so the
+    // next one would repeat it: the descent has reached its fixed point.
+    if (j0 == 0 && it > 0 && moved[2] == 0) break;
     if (warp == 0) {
       bar_sync_n(1, kAmThreads);  // the block's rows have the previous block's moves
       const bool v = lane < cnt;
@@ -905,7 +908,10 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
       }
       dws[cur * kDb + lane] = dwk;
       const bool any = __any_sync(0xffffffffu, dwk != 0.0f);
-      if (lane == 0) moved[cur] = any ? 1 : 0;
+      if (lane == 0) {
+        moved[cur] = any ? 1 : 0;
+        moved[2] = (j0 == 0 ? 0 : moved[2]) | (any ? 1 : 0);  // read by every thread before bar_sync
+      }
     } else {
       const int tid = threadIdx.x - 32;
       const float* dwp = dws + prev * kDb;
