@@ -120,7 +120,8 @@ __device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, cons
 //               head-dim elements), through a ring of kTcStages; the block-table
 //               entries of the next tile are loaded while this tile is issued
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 2..5  epilogue, one TMEM lane quarter (32 rows) each
+//   warps 2..9  epilogue, two per TMEM lane quarter (32 rows), each with 64 of a
+//               tile's 128 columns
 // Per key tile t the issuer forms S = Q K_t^T (bf16 operands, fp32 in TMEM; two
 // S buffers, so tile t+1's logits form while tile t's probabilities are made).
 // The epilogue turns row i of S into p_ij = 2^(c L_ij - lse2_i) with the row's
@@ -132,7 +133,8 @@ __device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, cons
 // end Y = softmax(L) V and the LSE rows go to the unit's workspace.
 // TMEM columns: S0 [0, 128), S1 [128, 256), P_hi [256, 320), P_lo [320, 384),
 // Y [384, 384 + D).
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
+constexpr int kTcEpi = 8;      // epilogue warps
 constexpr int kTcStages = 2;
 constexpr int kTcRows = 128;   // proxy rows per block = MMA M
 constexpr int kTcKeys = 128;   // keys per tile
@@ -141,8 +143,8 @@ constexpr int kTcHead = 1024;  // barriers, TMEM address, abort flag
 template <int D>
 constexpr int tc_tile_bytes() { return kTcKeys * D * 2; }
 template <int D>
-constexpr int tc_smem_bytes() {  // head, slack, Q rows, kTcStages x (K tile, V tile), keep list, 4 x 32 x 33 turn-around
-  return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4 + 4 * 32 * 33 * 4;
+constexpr int tc_smem_bytes() {  // head, slack, Q rows, kTcStages x (K tile, V tile), keep list, turn-arounds
+  return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4 + kTcEpi * 32 * 33 * 4;
 }
 static_assert(tc_smem_bytes<128>() <= 227 * 1024, "targets working set fits one CTA's shared memory");
 
@@ -162,8 +164,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* st_full = bars + 1;                   // [kTcStages] K and V of a tile landed
   uint64_t* st_empty = st_full + kTcStages;       // [kTcStages] the tile's MMAs are done
   uint64_t* s_full = st_empty + kTcStages;        // [2] S buffer formed
-  uint64_t* s_empty = s_full + 2;                 // [2] S buffer read (4 epilogue warps)
-  uint64_t* p_full = s_empty + 2;                 // P stored (4 epilogue warps)
+  uint64_t* s_empty = s_full + 2;                 // [2] S buffer read (every epilogue warp)
+  uint64_t* p_full = s_empty + 2;                 // P stored (every epilogue warp)
   uint64_t* p_empty = p_full + 1;                 // P read by the output MMAs
   uint64_t* y_full = p_empty + 1;                 // all output MMAs done
   uint64_t* drain = y_full + 1;                   // abort: every MMA issued is done
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            ~uintptr_t(1023));
   uint8_t* sKV = sQ + kTcRows * D * 2;            // stage s: K at s * 2 * kTile, V at + kTile
   int32_t* sKeep = reinterpret_cast<int32_t*>(sKV + kTcStages * 2 * kTile);  // the unit's kept positions
-  float* sTr = reinterpret_cast<float*>(sKeep + kAmMaxM);  // [4 epilogue warps][32][33] turn-around
+  float* sTr = reinterpret_cast<float*>(sKeep + kAmMaxM);  // [kTcEpi][32][33] turn-around
   float* red = reinterpret_cast<float*>(tc_smem + 576);  // [6] warp maxima of the rows' LSE
 
   const int rb = (meta.R + kTcRows - 1) / kTcRows;
@@ -203,8 +205,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kTcStages; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4); }
-    mbar_init(p_full, 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], kTcEpi); }
+    mbar_init(p_full, kTcEpi);
     mbar_init(p_empty, 1);
     mbar_init(y_full, 1);
     mbar_init(drain, 1);
@@ -325,6 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int hf = (warp - 2) >> 2;        // which 64 of a tile's 128 columns
     const int r = q4 * 32 + lane;          // row within the tile
     const int i = r0 + r;                  // proxy row
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -335,12 +338,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int w = 1; w < kTcThreads / 32; ++w) c = fmaxf(c, red[w]);
     const float cc = c * kLog2e;
-    float* Erow = u.base + (int64_t)i * u.ldE;  // E[i][k] = exp(L_i,keep[k] - c), column m = s_i
     // stores of E and Y go through the warp's 32 x 33 turn-around, so that each
     // runs along one row (lane = column) instead of down 32 rows (lane = row)
     float* tr = sTr + (warp - 2) * 32 * 33;
     const int iw = r0 + q4 * 32;                // the warp's first proxy row
-    float* Ew = u.base + (int64_t)iw * u.ldE;
+    float* Ew = u.base + (int64_t)iw * u.ldE;   // E[i][k] = exp(L_i,keep[k] - c), column m = s_i
     int kk = 0;                                 // first kept position not yet passed
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
@@ -348,18 +350,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after_sync();
       const uint32_t s_col = t_lane + (uint32_t)(t & 1) * 128u;
-      {  // E over the kept keys of this tile, from the same logits as the LSE pass: a kept
-         // key's column is the same for the whole warp, so it is read straight from TMEM,
-         // eight columns per load-and-wait
-        int k_end = kk;
+      {  // E over the kept keys of this warp's 64 columns of the tile, from the same logits as
+         // the LSE pass: a kept key's column is the same for the whole warp, so it is read
+         // straight from TMEM, eight columns per load-and-wait
+        int k_mid = kk, k_end = kk;
+        while (k_mid < u.m && sKeep[k_mid] < t * kTcKeys + 64) ++k_mid;
+        k_end = k_mid;
         while (k_end < u.m && sKeep[k_end] < (t + 1) * kTcKeys) ++k_end;
-        for (int kc = kk; kc < k_end; kc += 32) {  // 32 kept columns at a time
-          const int nk = min(32, k_end - kc);
+        const int ka = hf ? k_mid : kk, kb = hf ? k_end : k_mid;
+        for (int kc = ka; kc < kb; kc += 32) {  // 32 kept columns at a time
+          const int nk = min(32, kb - kc);
           for (int k0 = kc; k0 < kc + nk; k0 += 8) {
             uint32_t a[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int k = min(k0 + e, k_end - 1);
+              const int k = min(k0 + e, kb - 1);
               a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
             }
             float ev[8];
@@ -378,38 +383,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         kk = k_end;
       }
-      float v[128];
-      tmem_ld128(s_col, v);
+      float v0[32], v1[32];  // this warp's 64 logits of the row
+      tmem_ld32(s_col + 64 * hf, v0);
+      tmem_ld32(s_col + 64 * hf + 32, v1);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[t & 1]);
-      const int nvalid = u.n - t * kTcKeys;
-      if (nvalid < kTcKeys) {  // keys past the segment: p = 0
+      const int nvalid = u.n - t * kTcKeys - 64 * hf;
+      if (nvalid < 64) {  // keys past the segment: p = 0
 #pragma unroll
-        for (int jj = 0; jj < kTcKeys; ++jj)
-          if (jj >= nvalid) v[jj] = -INFINITY;
+        for (int jj = 0; jj < 32; ++jj) {
+          if (jj >= nvalid) v0[jj] = -INFINITY;
+          if (jj + 32 >= nvalid) v1[jj] = -INFINITY;
+        }
+      }
+      // the probabilities first (while the previous tile's output MMAs still read P),
+      // then the wait for P's buffer, then the stores
+      const float2 cc2 = make_float2(c2, c2), nl2 = make_float2(-lse2, -lse2), neg = make_float2(-1.0f, -1.0f);
+      uint32_t hi[2][16], lo[2][16];  // 32 keys per chunk: 16 packed pairs into each of P_hi and P_lo
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const float* vv = ch ? v1 : v0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 x = __ffma2_rn(make_float2(vv[2 * e], vv[2 * e + 1]), cc2, nl2);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          const __nv_bfloat162 h = __float22bfloat162_rn(p);  // .x (the low half) is the even key
+          const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+          const float2 hfl = make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
+          const __nv_bfloat162 l = __float22bfloat162_rn(__ffma2_rn(hfl, neg, p));  // p - hi, rounded
+          hi[ch][e] = hb;
+          lo[ch][e] = *reinterpret_cast<const uint32_t*>(&l);
+        }
       }
       ok = mbar_wait(p_empty, (t & 1) ^ 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after_sync();
-      const float2 cc2 = make_float2(c2, c2), nl2 = make_float2(-lse2, -lse2), neg = make_float2(-1.0f, -1.0f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 keys: 16 packed pairs into each of P_hi and P_lo
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j0 = c * 32 + 2 * e;
-          const float2 x = __ffma2_rn(make_float2(v[j0], v[j0 + 1]), cc2, nl2);
-          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          const __nv_bfloat162 h = __float22bfloat162_rn(p);  // .x (the low half) is the even key
-          const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
-          const float2 hf = make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
-          const __nv_bfloat162 l = __float22bfloat162_rn(__ffma2_rn(hf, neg, p));  // p - hi, rounded
-          hi[e] = hb;
-          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
-        }
-        tmem_st16(t_lane + kColP + c * 16, hi);
-        tmem_st16(t_lane + kColPlo + c * 16, lo);
+      for (int ch = 0; ch < 2; ++ch) {
+        const int cg = 2 * hf + ch;  // keys 32 cg .. 32 cg + 31 of the tile
+        tmem_st16(t_lane + kColP + cg * 16, hi[ch]);
+        tmem_st16(t_lane + kColPlo + cg * 16, lo[ch]);
       }
       tmem_wait_st();
       tc_fence_before_sync();
@@ -424,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after_sync();
       float* Yw = u.base + am_off_Y(meta.R, meta.max_m, u.ldE) + (int64_t)iw * D;
 #pragma unroll 1
-      for (int col = 0; col < D; col += 32) {
+      for (int col = 64 * hf; col < min(D, 64 * hf + 64); col += 32) {  // this warp's half of Y's columns
         float y[32];
         tmem_ld32(t_lane + kColY + col, y);
 #pragma unroll
@@ -435,9 +449,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (iw + rr < meta.R) Yw[(int64_t)rr * D + col + lane] = tr[rr * 33 + lane];
         __syncwarp();
       }
-      if (i < meta.R) {
+      if (hf == 0 && i < meta.R) {
         u.base[am_off_lse(meta.R, meta.max_m, u.ldE, D) + i] = lse;
-        Erow[u.m] = exp2f((lse - c) * kLog2e);
+        u.base[(int64_t)i * u.ldE + u.m] = exp2f((lse - c) * kLog2e);
       }
     }
   }
