@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "internal.h"
@@ -353,10 +354,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       {  // E over the kept keys of this warp's 64 columns of the tile, from the same logits as
          // the LSE pass: a kept key's column is the same for the whole warp, so it is read
          // straight from TMEM, eight columns per load-and-wait
-        int k_mid = kk, k_end = kk;
-        while (k_mid < u.m && sKeep[k_mid] < t * kTcKeys + 64) ++k_mid;
-        k_end = k_mid;
-        while (k_end < u.m && sKeep[k_end] < (t + 1) * kTcKeys) ++k_end;
+        // the kept keys of the tile's two halves: positions ascend, so 32 of them
+        // at a time and two ballots count them (one round unless more than 32
+        // keys of the tile are kept)
+        int n_lo = 0, n_all = 0;
+        for (int base = kk;; base += 32) {
+          const int pos = base + lane < u.m ? sKeep[base + lane] : INT_MAX;
+          const unsigned lo = __ballot_sync(0xffffffffu, pos < t * kTcKeys + 64);
+          const unsigned all = __ballot_sync(0xffffffffu, pos < (t + 1) * kTcKeys);
+          n_lo += __popc(lo);
+          n_all += __popc(all);
+          if (all != 0xffffffffu) break;
+        }
+        const int k_mid = kk + n_lo, k_end = kk + n_all;
         const int ka = hf ? k_mid : kk, kb = hf ? k_end : k_mid;
         for (int kc = ka; kc < kb; kc += 32) {  // 32 kept columns at a time
           const int nk = min(32, kb - kc);
