@@ -183,6 +183,10 @@ def check_writes(case, m, keep_np, beta, vc, before_v, before_k, before_aux, aux
     (64, 32, 2, 40, (200, 65, 1), 0.2, 8, "normal", True),   # R = 80 > m, a one-key unit: w, V_C compared
     (64, 16, 4, 32, (160, 97), 0.2, 8, "normal", True),      # R = 128 > m, two sequences
     (128, 16, 8, 16, (700,), 0.1, 3, "aligned", False),      # Q-aligned heavy hitters, two key tiles of rows
+    # m = 640 and 300 in one launch (laid out for the larger): five row tiles of the Gram products,
+    # blocks whose three tiles span two tile rows and read four strips, G's column m alone in a
+    # sixth column tile
+    (64, 16, 2, 48, (3200, 1500), 0.2, 8, "normal", False),
 ])
 def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist, elementwise):
     sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, shuffle_pages=True,
