@@ -839,6 +839,24 @@ __device__ __forceinline__ void stage_tile(float* tile, const float* M, int64_t 
   }
 }
 
+// Sums of rows i0 .. i0 + 3 of M over its first m columns, in every lane of
+// the warp (lanes take every 32nd column; four rows at a time keep four loads
+// in flight per column step).  Rows at or past m get 0.
+__device__ __forceinline__ void row_sums4(const float* __restrict__ M, int64_t ld, int m, int i0, float (&sum)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) sum[r] = 0.0f;
+  for (int k = lane; k < m; k += 32) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (i0 + r < m) sum[r] += M[(int64_t)(i0 + r) * ld + k];
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
+}
+
 // ------------------------------------------------------------------ mass fit
 // Block = unit.  Projected cyclic coordinate descent on min_{w >= 0} ||E w - s||^2
 // from w = 1: with g = G w - b, coordinate j moves to max(0, w_j - g_j / G_jj)
@@ -868,15 +886,15 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
   const float* G = u.base + am_off_G(meta.R, u.ldE);
   const int64_t ld = u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < m; i += kAmThreads / 32) {  // g = G 1 - b, one warp per row
-    const float* gr = G + (int64_t)i * ld;
-    float acc = 0.0f;
-    for (int k = lane; k < m; k += 32) acc += gr[k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
+  for (int i0 = warp * 4; i0 < m; i0 += kAmThreads / 8) {  // g = G 1 - b, four rows per warp at a time
+    float acc[4];
+    row_sums4(G, ld, m, i0, acc);
+    if (lane < 4 && i0 + lane < m) {
+      const int i = i0 + lane;
+      const float* gr = G + (int64_t)i * ld;
       const float b = gr[m], d = gr[i];
-      g[i] = acc - b;
+      const float a = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+      g[i] = a - b;
       w[i] = 1.0f;
       thr[i] = d > 0.0f ? kAmGuard * b : INFINITY;
       diag[i] = d;
@@ -1121,16 +1139,15 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   const float* G0 = u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, D);  // H X0 - Bm (row stride D)
   float* Xg = u.base + am_off_X(meta.R, meta.max_m, u.ldE, D);           // X, from X0 (row stride D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < m; i += kAmThreads / 32) {  // H_jj and pi_j, one warp per row
-    const float* hr = Hm + (int64_t)i * ld;
-    float ps = 0.0f;
-    for (int k = lane; k < m; k += 32) ps += hr[k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    if (lane == 0) {
-      const float d = hr[i];
+  for (int i0 = warp * 4; i0 < m; i0 += kAmThreads / 8) {  // H_jj and pi_j, four rows per warp at a time
+    float ps[4];
+    row_sums4(Hm, ld, m, i0, ps);
+    if (lane < 4 && i0 + lane < m) {
+      const int i = i0 + lane;
+      const float d = Hm[(int64_t)i * ld + i];
+      const float p = lane == 0 ? ps[0] : lane == 1 ? ps[1] : lane == 2 ? ps[2] : ps[3];
       hdiag[i] = d > 0.0f ? 1.0f / d : 0.0f;
-      thrb[i] = d > 0.0f ? kAmGuard * ps : INFINITY;
+      thrb[i] = d > 0.0f ? kAmGuard * p : INFINITY;
     }
   }
   for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {  // the starting gradient H X0 - Bm (Bm's place)
