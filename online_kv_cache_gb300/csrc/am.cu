@@ -1007,7 +1007,8 @@ __global__ void __launch_bounds__(kAmThreads) am_mass_kernel(const AmMeta meta, 
 
 // ------------------------------------------------------------------ compact probabilities
 // Block = (unit, 8 proxy rows), one warp per row: z_i = sum_j E_ij w_j, then
-// Ph_ij = E_ij w_j / z_i in place (a row without mass stays zero).
+// Ph_ij = E_ij w_j / z_i in place (a row without mass stays zero); the first
+// 512 products stay in registers between the two, so E is read once.
 __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta, float* ws) {
   const int rb = (meta.R + 7) / 8;
   const AmUnit u = am_unit(meta, blockIdx.x / rb, ws);
@@ -1016,12 +1017,26 @@ __global__ void __launch_bounds__(kAmThreads) am_probs_kernel(const AmMeta meta,
   if (i >= meta.R) return;
   float* E = u.base + (int64_t)i * u.ldE;
   const float* w = u.base + am_off_w(meta.R, meta.max_m, u.ldE, meta.d);
+  constexpr int kHeld = 16;  // E_ij w_j held in registers for the first 32 x kHeld columns
+  float ew[kHeld];
   float z = 0.0f;
-  for (int j = lane; j < u.m; j += 32) z = fmaf(E[j], w[j], z);
+#pragma unroll
+  for (int t = 0; t < kHeld; ++t) {
+    const int j = lane + 32 * t;
+    ew[t] = j < u.m ? E[j] * w[j] : 0.0f;
+  }
+#pragma unroll
+  for (int t = 0; t < kHeld; ++t) z += ew[t];
+  for (int j = lane + 32 * kHeld; j < u.m; j += 32) z += E[j] * w[j];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   const float inv = z > 0.0f ? 1.0f / z : 0.0f;
-  for (int j = lane; j < u.m; j += 32) E[j] = E[j] * w[j] * inv;
+#pragma unroll
+  for (int t = 0; t < kHeld; ++t) {
+    const int j = lane + 32 * t;
+    if (j < u.m) E[j] = ew[t] * inv;
+  }
+  for (int j = lane + 32 * kHeld; j < u.m; j += 32) E[j] = E[j] * w[j] * inv;
 }
 
 // ------------------------------------------------------------------ kept values
