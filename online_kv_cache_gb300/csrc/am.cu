@@ -1335,7 +1335,7 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if (m.units <= 0) continue;
     const int rbt = (m.R + kTcRows - 1) / kTcRows;
     am_targets_tc_kernel<D><<<(unsigned)(m.units * rbt), kTcThreads, tc_smem_bytes<D>(), stream>>>(
-        *al.tmK, *al.tmVp, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
+        *al.tmK, *al.tmVpool, *al.tmQ, m, al.block_table, al.keep, al.lse_rows, al.ws, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_x0_kernel<D><<<(unsigned)(m.units * ((m.max_m + 7) / 8)), kAmThreads, 0, stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.status);
@@ -1356,7 +1356,7 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
                                                                                 2, g2, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * g3), kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmV[ci], m, al.ws,
+    am_atb_tc_kernel<<<(unsigned)(m.units * g3), kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmX0[ci], m, al.ws,
                                                                                 3, g3, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(

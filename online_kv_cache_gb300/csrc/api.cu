@@ -1331,12 +1331,12 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   al.chunks = ap.metas.size();
   al.meta = ap.metas.data();
   al.tmK = &tmK;
-  al.tmVp = &tmV;
+  al.tmVpool = &tmV;
   al.tmQ = &tmQ;
   al.tmX = tmX.data();
   al.tmY = tmY.data();
   al.tmH = tmH.data();
-  al.tmV = tmX0.data();
+  al.tmX0 = tmX0.data();
   al.lse_rows = lse_rows;
   al.block_table = cache->block_table;
   al.k_pool = cache->k_pool;

@@ -204,13 +204,13 @@ struct AmLaunch {
   size_t chunks = 0;
   const AmMeta* meta = nullptr;  // [chunks]
   const CUtensorMap* tmK = nullptr;  // K pool, one page per box (as the scoring passes)
-  const CUtensorMap* tmVp = nullptr;  // V pool, same geometry
+  const CUtensorMap* tmVpool = nullptr;  // V pool, same geometry
   const CUtensorMap* tmQ = nullptr;  // Q, box {64, 128}
   // [chunks] fp32 operands of the Gram products, [unit][row][column] with a {128, 16, 1} box
   const CUtensorMap* tmX = nullptr;  // E / Ph: [unit][R][ldE]
   const CUtensorMap* tmY = nullptr;  // Y: [unit][R][d]
   const CUtensorMap* tmH = nullptr;  // H (in G's place): [unit][largest m][ldE]
-  const CUtensorMap* tmV = nullptr;  // X0: [unit][largest m][d]
+  const CUtensorMap* tmX0 = nullptr;  // X0: [unit][largest m][d]
   const float* lse_rows = nullptr;   // [B][L][H][R] natural-log LSE of every proxy row
   const int32_t* block_table = nullptr;
   const void* k_pool = nullptr;
