@@ -1294,15 +1294,32 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
     value_moves(Xg, D, col0, jp, cntp, dxs + ((it - 1) & 1) * kDb * kVc, threadIdx.x, kAmThreads);
   __syncthreads();
   const int64_t orow = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
-  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
-    const int j = e / kVc, c = e % kVc;
-    const float x = Xg[(int64_t)j * D + col0 + c];
-    if (vc != nullptr) vc[(orow + j) * D + col0 + c] = x;
+  for (int j = threadIdx.x; j < m; j += kAmThreads) {  // one kept entry (its 16 columns) per thread
     const int pos = am_kept(meta, u, keep, j, status);
     const int64_t row = pos < 0 ? -1 : am_row(meta, u, bt, pos, status);
-    if (row >= 0) {
-      const __nv_bfloat16 hb = __float2bfloat16_rn(x);
-      vp[row * D + col0 + c] = *reinterpret_cast<const uint16_t*>(&hb);
+    float x[kVc];
+#pragma unroll
+    for (int q = 0; q < kVc / 4; ++q) {  // X rows are 16-byte aligned (region and stride)
+      const float4 v = *reinterpret_cast<const float4*>(Xg + (int64_t)j * D + col0 + 4 * q);
+      x[4 * q] = v.x;
+      x[4 * q + 1] = v.y;
+      x[4 * q + 2] = v.z;
+      x[4 * q + 3] = v.w;
+    }
+    if (vc != nullptr) {
+#pragma unroll
+      for (int c = 0; c < kVc; ++c) vc[(orow + j) * D + col0 + c] = x[c];
+    }
+    if (row >= 0) {  // bf16, round to nearest even; 32 bytes at a 32-byte boundary of the V row
+      uint32_t b[kVc / 2];
+#pragma unroll
+      for (int c = 0; c < kVc / 2; ++c) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
+        b[c] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(vp + row * D + col0);
+      dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+      dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
     }
   }
 }
