@@ -376,9 +376,12 @@ kvc_status kvc_commit_fresh(const kvc_cache *cache, const kvc_segments *segs, co
 /* ------------------------------------------------------ Attention Matching */
 
 /* Bytes of workspace kvc_am_fit needs: per (layer, head, sequence with m > 0)
- * about 4 * ((R + m) * (m + 4) + R * (d + 1) + m * (d + 1)) bytes, plus the
- * workspace of the LSE pass (kvc_score_workspace_size) and 4 * B * L * H * R
- * bytes of row LSE; 0 when no sequence keeps an entry. */
+ * about 4 * ((R + M) * (M + 4) + R * (d + 1) + 2 * M * (d + 1)) bytes, M the
+ * largest m among the (up to 128) sequences launched together, since their
+ * fits share one layout (E [R][M+1], G [M][M+1], Y [R][d], LSE [R],
+ * B [M][d], w [M], X [M][d], rows padded to 4 floats, units to 256 bytes);
+ * plus the workspace of the LSE pass (kvc_score_workspace_size) and
+ * 4 * B * L * H * R bytes of row LSE; 0 when no sequence keeps an entry. */
 kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
                                  int32_t R, size_t *bytes);
 
@@ -396,7 +399,9 @@ kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *seg
  * [0, 1000]; 0 leaves token eviction's answer.  The full-attention targets
  * (LSE and softmax(Q K^T) V over all n keys) run on the tensor cores (bf16
  * Q, K and V as stored, fp32 accumulation, the probabilities in two bf16
- * parts); the Gram products and descents in fp32 on the CUDA cores.
+ * parts); so do the Gram products of the normal equations, fp32-accurate
+ * (each fp32 operand split into three bf16 parts, six partial products);
+ * the coordinate descents run in fp32 on the CUDA cores.
  * Effects: every kept entry's V row becomes its V_C row (bf16, round to
  * nearest even) and, when cache->aux is not NULL, its per-slot state becomes
  * beta (-inf where w = 0: the key is masked); kvc_compact then moves both with
