@@ -20,9 +20,10 @@
 // A work item is (unit, row group, key range).  Each K tile yields one MMA job
 // per 128-row tile (pass 1) or per W-row chunk (pass 2) of the group.
 //
-// Pass 1 (lse pass):   D[128 rows x 128 keys] = Q_tile K_tile^T; online (max,
-//                      sum) per row in the log2 domain; each warpgroup writes
-//                      one partial per (item, row).
+// Pass 1 (lse pass):   D[128 rows x 128 keys] = Q_tile K_tile^T; per row a
+//                      running (offset, sum) in the log2 domain, the offset
+//                      raised only when a tile would overflow the sum; each
+//                      warpgroup writes one partial per (item, row).
 // Combine:             merges the partials of a row into the pass-2 offset
 //                      nob_i = kBias - pw log2 sum_j 2^(c q_i.k_j)  (c = scale log2 e).
 // Pass 2 (alpha pass): D[128 keys x W rows] = K_tile Q_chunk^T; every TMEM lane
@@ -516,14 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int jj = 0; jj < kTile; ++jj)
                 if (jj >= valid) v[jj] = -INFINITY;
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-            for (int jj = 0; jj < kTile; jj += 8) {
-              mx0 = max3f(mx0, v[jj + 0], v[jj + 1]);
-              mx1 = max3f(mx1, v[jj + 2], v[jj + 3]);
-              mx2 = max3f(mx2, v[jj + 4], v[jj + 5]);
-              mx3 = max3f(mx3, v[jj + 6], v[jj + 7]);
-            }
             float mprev = m_run[0], sprev = s_run[0];
 #pragma unroll
             for (int q = 1; q < 4; ++q)
@@ -531,9 +524,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mprev = m_run[q];
                 sprev = s_run[q];
               }
-            const float mnew = fmaxf(mprev, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
-            const float tile_sum = tile_exp2_sum(v, c, mnew);
-            const float snew = fmaf(sprev, ex2_approx(mprev - mnew), tile_sum);
+            // The row's offset need not be its running maximum: any finite offset
+            // m gives the same sum * 2^m as long as no term overflows.  The first
+            // tile of the item takes its first key's logit (never masked); a tile
+            // whose sum stays at or below 2^64 (every logit at most ~64 above the
+            // offset, ~500 q.k units at scale 1/sqrt(128)) adds to the row as it
+            // stands, and only a tile above that (or inf/NaN) takes its exact
+            // maximum and rescales.  The row's sum then stays below 2^77 over
+            // 2^20 keys, and (offset, sum) merge like any pair in the combine.
+            if (mprev == -INFINITY) mprev = v[0] * c;
+            float mnew = mprev, snew;
+            const float tile_sum = tile_exp2_sum(v, c, mprev);
+            if (tile_sum <= 0x1p64f) {
+              snew = sprev + tile_sum;
+            } else {
+              float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+              for (int jj = 0; jj < kTile; jj += 8) {
+                mx0 = max3f(mx0, v[jj + 0], v[jj + 1]);
+                mx1 = max3f(mx1, v[jj + 2], v[jj + 3]);
+                mx2 = max3f(mx2, v[jj + 4], v[jj + 5]);
+                mx3 = max3f(mx3, v[jj + 6], v[jj + 7]);
+              }
+              mnew = fmaxf(mprev, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+              snew = fmaf(sprev, ex2_approx(mprev - mnew), tile_exp2_sum(v, c, mnew));
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               if (j == q) {
