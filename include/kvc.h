@@ -196,7 +196,7 @@ kvc_status kvc_score_workspace_size(const kvc_cache *cache, const kvc_segments *
  * lse    out fp32 [B][L][H][R] (natural log) or NULL.
  * ws     device workspace of kvc_score_workspace_size bytes.
  * Two tensor-core passes (bf16 operands, fp32 accumulation): the first
- * builds LSE with an online max/sum, the second recomputes the logits and
+ * builds LSE from a running (offset, sum) per row, the second recomputes the logits and
  * accumulates alpha^2.  Keys are used as stored (no positional rotation).
  * scale must be finite and > 0. */
 kvc_status kvc_score(const kvc_cache *cache, const kvc_segments *segs, const uint16_t *q,
