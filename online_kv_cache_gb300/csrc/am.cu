@@ -351,54 +351,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after_sync();
       const uint32_t s_col = t_lane + (uint32_t)(t & 1) * 128u;
-      {  // E over the kept keys of this warp's 64 columns of the tile, from the same logits as
-         // the LSE pass: a kept key's column is the same for the whole warp, so it is read
-         // straight from TMEM, eight columns per load-and-wait
-        // the kept keys of the tile's two halves: positions ascend, so 32 of them
-        // at a time and two ballots count them (one round unless more than 32
-        // keys of the tile are kept)
-        int n_lo = 0, n_all = 0;
-        for (int base = kk;; base += 32) {
-          const int pos = base + lane < u.m ? sKeep[base + lane] : INT_MAX;
-          const unsigned lo = __ballot_sync(0xffffffffu, pos < t * kTcKeys + 64);
-          const unsigned all = __ballot_sync(0xffffffffu, pos < (t + 1) * kTcKeys);
-          n_lo += __popc(lo);
-          n_all += __popc(all);
-          if (all != 0xffffffffu) break;
-        }
-        const int k_mid = kk + n_lo, k_end = kk + n_all;
-        const int ka = hf ? k_mid : kk, kb = hf ? k_end : k_mid;
-        for (int kc = ka; kc < kb; kc += 32) {  // 32 kept columns at a time
-          const int nk = min(32, kb - kc);
-          for (int k0 = kc; k0 < kc + nk; k0 += 8) {
-            uint32_t a[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int k = min(k0 + e, kb - 1);
-              a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
-            }
-            float ev[8];
-            tmem_ld1x8(a, ev);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (k0 + e < kc + nk) tr[lane * 33 + (k0 - kc) + e] = exp2f(fmaf(ev[e], c2, -cc));
-          }
-          __syncwarp();
-          if (lane < nk) {
-#pragma unroll 4
-            for (int rr = 0; rr < 32; ++rr)
-              if (iw + rr < meta.R) Ew[(int64_t)rr * u.ldE + kc + lane] = tr[rr * 33 + lane];
-          }
-          __syncwarp();
-        }
-        kk = k_end;
-      }
       float v0[32], v1[32];  // this warp's 64 logits of the row
       tmem_ld32(s_col + 64 * hf, v0);
       tmem_ld32(s_col + 64 * hf + 32, v1);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[t & 1]);
       const int nvalid = u.n - t * kTcKeys - 64 * hf;
       if (nvalid < 64) {  // keys past the segment: p = 0
 #pragma unroll
@@ -439,6 +394,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      // E after the hand-off of P, so that its loads and stores overlap the output
+      // MMAs instead of delaying them; S's buffer is released once E is read
+      {  // E over the kept keys of this warp's 64 columns of the tile, from the same logits as
+         // the LSE pass: a kept key's column is the same for the whole warp, so it is read
+         // straight from TMEM, eight columns per load-and-wait
+        // the kept keys of the tile's two halves: positions ascend, so 32 of them
+        // at a time and two ballots count them (one round unless more than 32
+        // keys of the tile are kept)
+        int n_lo = 0, n_all = 0;
+        for (int base = kk;; base += 32) {
+          const int pos = base + lane < u.m ? sKeep[base + lane] : INT_MAX;
+          const unsigned in_lo = __ballot_sync(0xffffffffu, pos < t * kTcKeys + 64);
+          const unsigned in_all = __ballot_sync(0xffffffffu, pos < (t + 1) * kTcKeys);
+          n_lo += __popc(in_lo);
+          n_all += __popc(in_all);
+          if (in_all != 0xffffffffu) break;
+        }
+        const int k_mid = kk + n_lo, k_end = kk + n_all;
+        const int ka = hf ? k_mid : kk, kb = hf ? k_end : k_mid;
+        for (int kc = ka; kc < kb; kc += 32) {  // 32 kept columns at a time
+          const int nk = min(32, kb - kc);
+          for (int k0 = kc; k0 < kc + nk; k0 += 8) {
+            uint32_t a[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int k = min(k0 + e, kb - 1);
+              a[e] = s_col + (uint32_t)max(0, sKeep[k] - t * kTcKeys);
+            }
+            float ev[8];
+            tmem_ld1x8(a, ev);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (k0 + e < kc + nk) tr[lane * 33 + (k0 - kc) + e] = exp2f(fmaf(ev[e], c2, -cc));
+          }
+          __syncwarp();
+          if (lane < nk) {
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr)
+              if (iw + rr < meta.R) Ew[(int64_t)rr * u.ldE + kc + lane] = tr[rr * 33 + lane];
+          }
+          __syncwarp();
+        }
+        kk = k_end;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[t & 1]);
     }
     if (ok) {
       ok = mbar_wait(y_full, 0, abort_flag, status);
