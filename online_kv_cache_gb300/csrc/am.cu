@@ -114,12 +114,15 @@ __device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, cons
 }
 
 // ------------------------------------------------------------------ targets (tensor cores)
-// Block = (unit, 128 proxy rows), 192 threads:
+// Block = (unit, 128 proxy rows), 352 threads:
 //   warp 0      producer: the block's Q rows (two-dimensional TMA, once), then
-//               the K and V tiles of 128 keys, page by page (four-dimensional
-//               TMA: one copy per page lands as 1024-byte atoms of 8 keys x 64
-//               head-dim elements), through a ring of kTcStages; the block-table
-//               entries of the next tile are loaded while this tile is issued
+//               the K tiles of 128 keys, page by page (four-dimensional TMA: one
+//               copy per page lands as 1024-byte atoms of 8 keys x 64 head-dim
+//               elements), through a ring of kTcStages whose stages free up as
+//               soon as a tile's logits are formed; the block-table entries of
+//               the next tile are loaded while this tile is issued
+//   warp 10     producer of the V tiles the same way, through a second ring
+//               whose stages free up when a tile's output MMAs are done
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..9  epilogue, two per TMEM lane quarter (32 rows), each with 64 of a
 //               tile's 128 columns
@@ -131,10 +134,13 @@ __device__ __forceinline__ int am_kept(const AmMeta& meta, const AmUnit& u, cons
 // the bf16 of the remainder (16 bits of mantissa together) and stores both into
 // TMEM.  The issuer then accumulates Y += P_hi V_t + P_lo V_t with A read from
 // TMEM and V_t as an MN-major B operand (the pool stores V key by key).  At the
-// end Y = softmax(L) V and the LSE rows go to the unit's workspace.
+// end Y = softmax(L) V and the LSE rows go to the unit's workspace.  E over the
+// kept keys is formed from the same logits after P's hand-off, read back from the
+// S buffer column by column (a kept key's column is the same for the whole warp).
 // TMEM columns: S0 [0, 128), S1 [128, 256), P_hi [256, 320), P_lo [320, 384),
 // Y [384, 384 + D).
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;
+constexpr int kTcWarpV = 10;   // the V producer
 constexpr int kTcEpi = 8;      // epilogue warps
 constexpr int kTcStages = 2;
 constexpr int kTcRows = 128;   // proxy rows per block = MMA M
@@ -144,7 +150,7 @@ constexpr int kTcHead = 1024;  // barriers, TMEM address, abort flag
 template <int D>
 constexpr int tc_tile_bytes() { return kTcKeys * D * 2; }
 template <int D>
-constexpr int tc_smem_bytes() {  // head, slack, Q rows, kTcStages x (K tile, V tile), keep list, turn-arounds
+constexpr int tc_smem_bytes() {  // head, slack, Q rows, the K and V rings, keep list, turn-arounds
   return kTcHead + 1024 + kTcRows * D * 2 + kTcStages * 2 * tc_tile_bytes<D>() + kAmMaxM * 4 + kTcEpi * 32 * 33 * 4;
 }
 static_assert(tc_smem_bytes<128>() <= 227 * 1024, "targets working set fits one CTA's shared memory");
@@ -162,9 +168,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ __align__(16) uint8_t tc_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem);
   uint64_t* q_full = bars;                        // [1]
-  uint64_t* st_full = bars + 1;                   // [kTcStages] K and V of a tile landed
-  uint64_t* st_empty = st_full + kTcStages;       // [kTcStages] the tile's MMAs are done
-  uint64_t* s_full = st_empty + kTcStages;        // [2] S buffer formed
+  uint64_t* k_full = bars + 1;                    // [kTcStages] K tile landed
+  uint64_t* k_empty = k_full + kTcStages;         // [kTcStages] its logits are formed
+  uint64_t* v_full = k_empty + kTcStages;         // [kTcStages] V tile landed
+  uint64_t* v_empty = v_full + kTcStages;         // [kTcStages] its output MMAs are done
+  uint64_t* s_full = v_empty + kTcStages;         // [2] S buffer formed
   uint64_t* s_empty = s_full + 2;                 // [2] S buffer read (every epilogue warp)
   uint64_t* p_full = s_empty + 2;                 // P stored (every epilogue warp)
   uint64_t* p_empty = p_full + 1;                 // P read by the output MMAs
@@ -174,10 +182,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem) + kTcHead + 1023) &
                                            ~uintptr_t(1023));
-  uint8_t* sKV = sQ + kTcRows * D * 2;            // stage s: K at s * 2 * kTile, V at + kTile
-  int32_t* sKeep = reinterpret_cast<int32_t*>(sKV + kTcStages * 2 * kTile);  // the unit's kept positions
+  uint8_t* sK = sQ + kTcRows * D * 2;             // K ring: stage s at s * kTile
+  uint8_t* sV = sK + kTcStages * kTile;           // V ring
+  int32_t* sKeep = reinterpret_cast<int32_t*>(sV + kTcStages * kTile);  // the unit's kept positions
   float* sTr = reinterpret_cast<float*>(sKeep + kAmMaxM);  // [kTcEpi][32][33] turn-around
-  float* red = reinterpret_cast<float*>(tc_smem + 576);  // [6] warp maxima of the rows' LSE
+  float* red = reinterpret_cast<float*>(tc_smem + 576);  // [one per warp] maxima of the rows' LSE
 
   const int rb = (meta.R + kTcRows - 1) / kTcRows;
   const AmUnit u = am_unit(meta, blockIdx.x / rb, ws);
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // zero the K/V ring: rows of pages past the segment are never loaded and
   // must hold finite values (their probabilities are 0)
   for (int i = threadIdx.x; i < kTcStages * 2 * kTile / 16; i += kTcThreads)
-    reinterpret_cast<uint4*>(sKV)[i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sK)[i] = make_uint4(0u, 0u, 0u, 0u);
   // the unit's kept positions (ascending) and the shift c = max_i LSE_i of its rows
   const int64_t krow0 = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
   for (int k = threadIdx.x; k < u.m; k += kTcThreads) {
@@ -205,7 +214,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cmax;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kTcStages; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_empty[i], 1); }
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], kTcEpi); }
     mbar_init(p_full, kTcEpi);
     mbar_init(p_empty, 1);
@@ -227,14 +241,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
+  if (warp == 0 || warp == kTcWarpV) {
+    // ---------------------------------------------------------- producers
+    // warp 0: the Q rows (once) and the K tiles; warp kTcWarpV: the V tiles.  A K
+    // stage is free again once its logits are formed, a V stage once its output
+    // MMAs are done, so K runs a tile further ahead than a shared ring allows.
+    const bool is_k = warp == 0;
+    uint8_t* ring = is_k ? sK : sV;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
     bool ok = true;
     uint32_t issued = 0;  // tiles whose copies were issued
-    const int64_t qrow = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R + r0;
-    if (lane == 0) mbar_arrive_expect_tx(q_full, KB * kTcRows * 128);
-    __syncwarp();
-    if (lane < KB) tma_load_2d(sQ + lane * kTcRows * 128, &tmQ, q_full, lane * 64, (int32_t)qrow);
+    if (is_k) {
+      const int64_t qrow = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R + r0;
+      if (lane == 0) mbar_arrive_expect_tx(q_full, KB * kTcRows * 128);
+      __syncwarp();
+      if (lane < KB) tma_load_2d(sQ + lane * kTcRows * 128, &tmQ, q_full, lane * 64, (int32_t)qrow);
+    }
     const int ppt = kTcKeys / meta.P;  // pages per tile (<= 16)
     const int32_t* bt_row = bt + (int64_t)u.b * meta.max_blocks;
     auto page_of = [&](int t) -> int32_t {
@@ -242,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane >= ppt || slot >= u.n) return -1;
       const int32_t pg = __ldg(bt_row + (u.s0 + slot) / meta.P);
       if (pg < 0 || pg >= meta.num_pages) {
-        atomicOr(status, KVC_DEV_BAD_PAGE);  // outside the pool: reported, not read
+        if (is_k) atomicOr(status, KVC_DEV_BAD_PAGE);  // outside the pool: reported (once), not read
         return -1;
       }
       return pg;
@@ -252,25 +275,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t pg = pg_next;
       if (t + 1 < T) pg_next = page_of(t + 1);
       const int st = t % kTcStages;
-      if (lane == 0) ok = mbar_wait(&st_empty[st], ((t / kTcStages) & 1) ^ 1, abort_flag, status);
+      if (lane == 0) ok = mbar_wait(&empty[st], ((t / kTcStages) & 1) ^ 1, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
-      if (lane == 0) mbar_arrive_expect_tx(&st_full[st], __popc(valid) * 2u * KB * meta.P * 128u);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], __popc(valid) * KB * meta.P * 128u);
       __syncwarp();
       if (pg >= 0) {
         const int32_t prow = (int32_t)((((int64_t)u.l * meta.num_pages + pg) * meta.H + u.h) * meta.P);
-        uint8_t* dk = sKV + st * 2 * kTile + lane * meta.P * D * 2;
-        tma_load_4d(dk, &tmK, &st_full[st], 0, 0, 0, prow >> 3);
-        tma_load_4d(dk + kTile, &tmV, &st_full[st], 0, 0, 0, prow >> 3);
+        uint8_t* dst = ring + st * kTile + lane * meta.P * D * 2;
+        if (is_k)
+          tma_load_4d(dst, &tmK, &full[st], 0, 0, 0, prow >> 3);
+        else
+          tma_load_4d(dst, &tmV, &full[st], 0, 0, 0, prow >> 3);
       }
       ++issued;
     }
     // let the copies issued land before the CTA exits, whichever role gave up
     if (lane == 0) {
-      mbar_wait(q_full, 0, nullptr, status);
+      if (is_k) mbar_wait(q_full, 0, nullptr, status);
       for (uint32_t t = issued > (uint32_t)kTcStages ? issued - kTcStages : 0; t < issued; ++t)
-        mbar_wait(&st_full[t % kTcStages], (t / kTcStages) & 1, nullptr, status);
+        mbar_wait(&full[t % kTcStages], (t / kTcStages) & 1, nullptr, status);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -282,19 +307,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ));
       auto issue_s = [&](int t) {  // S[t & 1] = Q K_t^T
         const int st = t % kTcStages;
-        const uint64_t k_desc = sdesc_k_sw128(smem_u32(sKV + st * 2 * kTile), KB * 1024);
+        const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + st * kTile), KB * 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + (uint32_t)(t & 1) * 128u,
                    q_desc + ((uint64_t)((k >> 2) * (kTcRows * 128) + (k & 3) * 32) >> 4),
                    k_desc + ((uint64_t)((k >> 2) * 1024 + (k & 3) * 32) >> 4), idesc_s, k > 0);
         mma_commit(&s_full[t & 1]);
+        mma_commit(&k_empty[st]);  // the K stage is free once the logits are formed
         issued = true;
       };
       for (int t = 0; t <= T && ok; ++t) {
         // S of tile t (ahead of tile t - 1's output MMAs)
         if (t < T) {
-          if (!(ok = mbar_wait(&st_full[t % kTcStages], (t / kTcStages) & 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait(&k_full[t % kTcStages], (t / kTcStages) & 1, abort_flag, status))) break;
           if (!(ok = mbar_wait(&s_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, status))) break;
           tc_fence_after_sync();
           issue_s(t);
@@ -303,8 +329,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // output of tile t - 1: Y += P_hi V + P_lo V
         const int tp = t - 1;
         if (!(ok = mbar_wait(p_full, tp & 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait(&v_full[tp % kTcStages], (tp / kTcStages) & 1, abort_flag, status))) break;
         tc_fence_after_sync();
-        const uint32_t v_base = smem_u32(sKV + (tp % kTcStages) * 2 * kTile + kTile);
+        const uint32_t v_base = smem_u32(sV + (tp % kTcStages) * kTile);
 #pragma unroll
         for (int k = 0; k < kTcKeys / 16; ++k) {  // 16 keys = two 8-key atoms per step
           const uint64_t v_desc = sdesc_mn_sw128(v_base + k * 2 * KB * 1024, 1024, KB * 1024);
@@ -316,7 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_bf16_tmem_a(tmem + kColY, tmem + kColPlo + 8 * k, v_desc, idesc_y, 1u);
         }
         mma_commit(p_empty);
-        mma_commit(&st_empty[tp % kTcStages]);
+        mma_commit(&v_empty[tp % kTcStages]);
       }
       if (ok) {
         mma_commit(y_full);
