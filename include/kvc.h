@@ -376,10 +376,11 @@ kvc_status kvc_commit_fresh(const kvc_cache *cache, const kvc_segments *segs, co
 /* ------------------------------------------------------ Attention Matching */
 
 /* Bytes of workspace kvc_am_fit needs: per (layer, head, sequence with m > 0)
- * about 4 * ((R + M) * (M + 4) + R * (d + 1) + 2 * M * (d + 1)) bytes, M the
+ * about 4 * ((R + M) * (M + 4) + R * (d + 1) + M * (5 * d + 1)) bytes, M the
  * largest m among the (up to 128) sequences launched together, since their
  * fits share one layout (E [R][M+1], G [M][M+1], Y [R][d], LSE [R],
- * B [M][d], w [M], X [M][d], rows padded to 4 floats, units to 256 bytes);
+ * B [M][d], w [M], X [M][d], and B's sums over three more ranges of the R
+ * rows [3][M][d]; rows padded to 4 floats, units to 256 bytes);
  * plus the workspace of the LSE pass (kvc_score_workspace_size) and
  * 4 * B * L * H * R bytes of row LSE; 0 when no sequence keeps an entry. */
 kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,

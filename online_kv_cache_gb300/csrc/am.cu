@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -509,9 +510,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // products of the fits:
 //   mode 0: A = E (m columns), B = [E | s] (m + 1), C = G        (stride ldE)
 //   mode 1: A = B = Ph (m columns),                 C = H in G's place
-//   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d)
+//   mode 2: A = Ph, B = Y (d columns, stride d),    C = Bm       (stride d),
+//           summed over up to kAmBmParts ranges of the rows by separate blocks
+//           (range p > 0 into Bp part p - 1); it runs in the same launch as
+//           mode 1, whose blocks come first and never read B
 //   mode 3: A = H (m rows), B = X0 (the kept values), C = H X0 - Bm in Bm's
-//           place (the value fit's starting gradient; H is symmetric)
+//           place, Bm's row ranges added in order (the value fit's starting
+//           gradient; H is symmetric)
 // on tcgen05 with fp32-level accuracy: every fp32 value
 // x is split into three bf16 parts (x0 = bf16(x), x1 = bf16(x - x0),
 // x2 = bf16(x - x0 - x1): 8 + 8 + 8 significant bits, x0 + x1 + x2 = x to the
@@ -591,7 +596,8 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 
 __global__ void __launch_bounds__(kTbThreads, 1)
     am_atb_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const AmMeta meta, float* ws, int mode, int blocks_per_unit, unsigned* status) {
+                     const AmMeta meta, float* ws, int mode_lo, int bpu_lo, int64_t blocks_lo, int bpu2,
+                     int parts2, unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
   uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [kTbBufs] an operand buffer's MMAs are done
   uint64_t* ready = done + kTbBufs;                        // [kTbBufs] an operand buffer is split
@@ -603,13 +609,25 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   uint8_t* bufs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tb_smem) + 1024 + 1023) &
                                              ~uintptr_t(1023));
   float* ring = reinterpret_cast<float*>(bufs + kTbBufs * kTbBuf);
-  const int64_t unit = blockIdx.x / blocks_per_unit;
+  // blocks [0, blocks_lo) run mode_lo over all K rows; the others (modes 1 and 2
+  // in one launch) run mode 2 over one of parts2 ranges of the rows
+  int mode = mode_lo, blocks_per_unit = bpu_lo, part = 0, nparts = 1;
+  int64_t lb = blockIdx.x;
+  if (lb >= blocks_lo) {
+    lb -= blocks_lo;
+    mode = 2;
+    blocks_per_unit = bpu2;
+    nparts = parts2;
+    part = (int)(lb % parts2);
+    lb /= parts2;
+  }
+  const int64_t unit = lb / blocks_per_unit;
   const AmUnit u = am_unit(meta, unit, ws);
   const int M = u.m;
   const int N = mode == 0 ? u.m + 1 : (mode == 1 ? u.m : meta.d);
   const int K = mode == 3 ? u.m : meta.R;  // the rows summed over
   const TileGrid tg = tile_grid(mode, M, meta.d);
-  const int t0 = (int)(blockIdx.x % blocks_per_unit) * kTbTiles;
+  const int t0 = (int)(lb % blocks_per_unit) * kTbTiles;
   const int ntiles = min(kTbTiles, tg.count() - t0);
   if (ntiles <= 0) return;
   // the block's tiles and strips: strip slot k holds the 128 columns from
@@ -655,10 +673,11 @@ __global__ void __launch_bounds__(kTbThreads, 1)
   // (row m of C is not kept), so that one strip serves both operands of a
   // diagonal tile; B's maps (Y, X0) end at d
   const int ncolX = mode == 0 ? N : M;
-  float* C = mode >= 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
-  const int ldc = mode >= 2 ? meta.d : u.ldE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchunks = (K + kTbRows - 1) / kTbRows;
+  // this block's chunks of kTbRows rows: [c_lo, c_lo + nchunks)
+  const int nchunks_all = (K + kTbRows - 1) / kTbRows;
+  const int c_lo = (int)((int64_t)part * nchunks_all / nparts);
+  const int nchunks = (int)((int64_t)(part + 1) * nchunks_all / nparts) - c_lo;
   if (threadIdx.x == 0) {
     for (int b = 0; b < kTbBufs; ++b) {
       mbar_init(&done[b], 1);
@@ -721,7 +740,8 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         float* stg = ring + st * kTbStageFloats;
         for (int k = 0; k < nstr; ++k) {
           const bool fromB = mode >= 2 && k >= ybase;
-          tma_load_3d(stg + k * kTbStripFloats, fromB ? &tmB : &tmA, &full[st], scol[k], c * kTbRows, (int)unit);
+          tma_load_3d(stg + k * kTbStripFloats, fromB ? &tmB : &tmA, &full[st], scol[k], (c_lo + c) * kTbRows,
+                      (int)unit);
         }
         issued = c + 1;
       }
@@ -754,7 +774,7 @@ __global__ void __launch_bounds__(kTbThreads, 1)
         float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         // A's columns past this unit's, and (mode 3: the maps run to the launch's
         // largest m) rows past it, are not its own
-        const int nv = c * kTbRows + r >= K ? 0 : (mode >= 2 && st >= ybase ? 8 : ncolX - scol[st] - g * 8);
+        const int nv = (c_lo + c) * kTbRows + r >= K ? 0 : (mode >= 2 && st >= ybase ? 8 : ncolX - scol[st] - g * 8);
         if (nv < 8) {
 #pragma unroll
           for (int t = 0; t < 8; ++t)
@@ -791,12 +811,23 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     // around in shared memory, so that a store (and mode 3's load) covers 32
     // consecutive columns of one row.
     float* tr = reinterpret_cast<float*>(bufs) + warp * 32 * 33;
+    // C: G or H (stride ldE), Bm (stride d), or (mode 2, row range p > 0) Bp part p - 1
+    const float* Bp = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, meta.d);
+    const int64_t bp_stride = (int64_t)meta.max_m * meta.d;
+    float* C = mode >= 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
+    if (mode == 2 && part > 0) C = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, meta.d) + (part - 1) * bp_stride;
+    const int ldc = mode >= 2 ? meta.d : u.ldE;
 #pragma unroll 1
     for (int k = 0; k < ntiles && warp < 16; ++k) {
       const bool dg = tg.sym && tmi[k] == tni[k];
       const int p0w = tmi[k] * 128 + q4 * 32, pr = p0w + lane;
       float y[32];
-      tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(k * 128 + cq * 32), y);
+      if (nchunks > 0) {
+        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(k * 128 + cq * 32), y);
+      } else {  // a row range without rows adds nothing
+#pragma unroll
+        for (int t = 0; t < 32; ++t) y[t] = 0.0f;
+      }
       const int qb = tni[k] * 128 + cq * 32;
       if (tg.sym) {  // the transpose: C[q][p] for q < m (not G's column m), lanes along p coalesced
 #pragma unroll
@@ -807,15 +838,24 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       for (int t = 0; t < 32; ++t) tr[lane * 33 + t] = y[t];
       __syncwarp();
       const int q = qb + lane;  // this lane's column; rows p0w .. p0w + 31
-      if (mode == 3) {  // C = H X0 - Bm, 16 rows at a time: their Bm values first
+      if (mode == 3) {  // C = H X0 - Bm, 8 rows at a time: their Bm values first (its row ranges in order)
+        static_assert(kAmBmParts == 4, "the row ranges of Bm are added below one by one");
 #pragma unroll
-        for (int r0 = 0; r0 < 32; r0 += 16) {
-          float bm[16];
+        for (int r0 = 0; r0 < 32; r0 += 8) {
+          float bm[8];
 #pragma unroll
-          for (int r = 0; r < 16; ++r)
-            bm[r] = (p0w + r0 + r < M && q < N) ? C[(int64_t)(p0w + r0 + r) * ldc + q] : 0.0f;
+          for (int r = 0; r < 8; ++r) {
+            const int64_t o = (int64_t)(p0w + r0 + r) * ldc + q;
+            bm[r] = 0.0f;
+            if (p0w + r0 + r < M && q < N) {
+              bm[r] = C[o];
+              if (parts2 > 1) bm[r] += Bp[o];
+              if (parts2 > 2) bm[r] += Bp[bp_stride + o];
+              if (parts2 > 3) bm[r] += Bp[2 * bp_stride + o];
+            }
+          }
 #pragma unroll
-          for (int r = 0; r < 16; ++r)
+          for (int r = 0; r < 8; ++r)
             if (p0w + r0 + r < M && q < N) C[(int64_t)(p0w + r0 + r) * ldc + q] = tr[(r0 + r) * 33 + lane] - bm[r];
         }
       } else {
@@ -1388,22 +1428,24 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if ((e = check()) != cudaSuccess) return e;
     const int g0 = atb_blocks_per_unit(0, m.max_m, D), g1 = atb_blocks_per_unit(1, m.max_m, D);
     const int g2 = atb_blocks_per_unit(2, m.max_m, D), g3 = atb_blocks_per_unit(3, m.max_m, D);
-    am_atb_tc_kernel<<<(unsigned)(m.units * g0), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws,
-                                                                                0, g0, al.status);
+    // Bm's row ranges: as many as there are 16-row chunks, at most kAmBmParts
+    const int parts = std::min(kAmBmParts, (m.R + kTbRows - 1) / kTbRows);
+    const int64_t nb0 = m.units * g0, nb1 = m.units * g1, nb2 = m.units * g2 * parts, nb3 = m.units * g3;
+    am_atb_tc_kernel<<<(unsigned)nb0, kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws, 0, g0, nb0,
+                                                                     0, 1, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_probs_kernel<<<(unsigned)(m.units * ((m.R + 7) / 8)), kAmThreads, 0, stream>>>(m, al.ws);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * g1), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws,
-                                                                                1, g1, al.status);
+    // H = Ph^T Ph and Bm = Ph^T Y in one launch (mode 1 never reads B): Bm's
+    // row-range blocks fill the SMs the blocks of H leave idle
+    am_atb_tc_kernel<<<(unsigned)(nb1 + nb2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws, 1,
+                                                                             g1, nb1, g2, parts, al.status);
     if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * g2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws,
-                                                                                2, g2, al.status);
-    if ((e = check()) != cudaSuccess) return e;
-    am_atb_tc_kernel<<<(unsigned)(m.units * g3), kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmX0[ci], m, al.ws,
-                                                                                3, g3, al.status);
+    am_atb_tc_kernel<<<(unsigned)nb3, kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmX0[ci], m, al.ws, 3, g3, nb3,
+                                                                     0, parts, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);

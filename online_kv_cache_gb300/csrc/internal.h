@@ -154,8 +154,11 @@ constexpr int kLrfuMaxSegment = 1 << 20;
 //                  overwritten by H = Ph^T Ph for the value fit
 //   Y   [R][d]     full attention output softmax(L) V
 //   lse [R]        natural-log row mass of the full attention
-//   Bm  [m][d]     Ph^T Y
+//   Bm  [m][d]     Ph^T Y over the first of its row ranges (the value fit's
+//                  starting gradient H X0 - Bm replaces it)
 //   w   [m4]       fitted exp(beta)
+//   X   [m][d]     the value fit's unknowns (from the kept values X0)
+//   Bp  [kAmBmParts - 1][m][d]  Ph^T Y over the other row ranges
 struct AmSeq {
   int32_t b, s0, n, m;
   int32_t ldE;          // row stride of E and G: the launch's largest m + 1, rounded up to a multiple of 4
@@ -191,8 +194,15 @@ __host__ __device__ inline int64_t am_off_w(int R, int m, int ldE, int d) {
 __host__ __device__ inline int64_t am_off_X(int R, int m, int ldE, int d) {
   return (am_off_w(R, m, ldE, d) + ((m + 3) & ~3) + 3) & ~int64_t(3);
 }
+// Bm = Ph^T Y is summed over up to kAmBmParts row ranges by separate blocks
+// (they fill the SMs the blocks of H = Ph^T Ph leave idle); range p > 0 lands
+// in Bp part p - 1 and the starting-gradient product adds them to Bm in order.
+constexpr int kAmBmParts = 4;
+__host__ __device__ inline int64_t am_off_Bp(int R, int m, int ldE, int d) {
+  return am_off_X(R, m, ldE, d) + (int64_t)m * d;
+}
 __host__ __device__ inline int64_t am_unit_floats(int R, int m, int ldE, int d) {
-  const int64_t x = am_off_X(R, m, ldE, d) + (int64_t)m * d;
+  const int64_t x = am_off_Bp(R, m, ldE, d) + (int64_t)(kAmBmParts - 1) * m * d;
   return (x + 63) & ~int64_t(63);  // 256-byte aligned units
 }
 

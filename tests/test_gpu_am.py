@@ -187,6 +187,9 @@ def check_writes(case, m, keep_np, beta, vc, before_v, before_k, before_aux, aux
     # blocks whose three tiles span two tile rows and read four strips, G's column m alone in a
     # sixth column tile
     (64, 16, 2, 48, (3200, 1500), 0.2, 8, "normal", False),
+    # R = 8: one 16-row chunk, so Ph^T Y is summed over one row range (R = 32, 80, 96 and 128
+    # above give two, four uneven and four even ranges)
+    (64, 16, 2, 4, (120, 40), 0.2, 8, "normal", False),
 ])
 def test_am_matches_oracle(d, P, G, q, lengths, ratio, sweeps, qdist, elementwise):
     sp = workloads.custom(L=2, H=2, G=G, d=d, P=P, q=q, lengths=lengths, shuffle_pages=True,
