@@ -403,14 +403,15 @@ def our_arm(args):
             ev[1].record(stream)
             cp.lrfu(0.9, 0.5)
         else:
-            cp.score_lse(case.q, sp.scale)
+            cp.score_lse(case.q, sp.scale, want_lse=args.am_sweeps > 0)
             ev[1].record(stream)
             cp.score_alpha(case.q, sp.scale)
         ev[2].record(stream)
         cp.select()
         ev[3].record(stream)
         if args.am_sweeps > 0:
-            cp.am_fit(case.q, sp.scale, args.am_sweeps)
+            # the scoring LSE pass's rows are the fit's (the action scorer writes none)
+            cp.am_fit(case.q, sp.scale, args.am_sweeps, lse=None if args.scorer == "actkv" else cp.lse)
         ev[4].record(stream)
         if args.variant == "inplace":
             cp.plan_compact()

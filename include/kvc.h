@@ -409,6 +409,10 @@ kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *seg
  * the entry.  K rows and tags are untouched.
  *   m     host [batch] budgets (clamped to n_b); every m_b <= 2048
  *   q     bf16 [B][L][H][R][d], R <= 4096, as for kvc_score
+ *   lse   fp32 [B][L][H][R] natural-log LSE of the proxy rows over their
+ *         segments, as kvc_score / kvc_score_lse write it for the same q, R and
+ *         scale (the fit then runs no LSE pass of its own), or NULL: the fit
+ *         runs the scoring LSE pass itself (same numbers)
  *   keep  int32 [L][H][Mtot] ascending segment positions (kvc_select_topm)
  *   beta  out fp32 [L][H][Mtot] or NULL
  *   vc    out fp32 [L][H][Mtot][d] (V_C before rounding) or NULL
@@ -417,8 +421,9 @@ kvc_status kvc_am_workspace_size(const kvc_cache *cache, const kvc_segments *seg
  * KVC_DEV_BAD_KEEP, a block-table entry outside the pool KVC_DEV_BAD_PAGE
  * (that entry is skipped). */
 kvc_status kvc_am_fit(const kvc_cache *cache, const kvc_segments *segs, const int32_t *m,
-                      const uint16_t *q, int32_t R, float scale, const int32_t *keep, int32_t sweeps,
-                      float *beta, float *vc, void *ws, size_t ws_bytes, kvc_stream_t stream);
+                      const uint16_t *q, int32_t R, float scale, const float *lse, const int32_t *keep,
+                      int32_t sweeps, float *beta, float *vc, void *ws, size_t ws_bytes,
+                      kvc_stream_t stream);
 
 /* -------------------------------------------------------------- helpers */
 

@@ -143,7 +143,7 @@ def lib():
             "kvc_score_action": (I32, [C, SG, P, I32, F, P, P, P, S, P]),
             "kvc_lrfu_update": (I32, [C, SG, P, F, F, P, P, P]),
             "kvc_am_workspace_size": (I32, [C, SG, P, I32, ctypes.POINTER(S)]),
-            "kvc_am_fit": (I32, [C, SG, P, P, I32, F, P, I32, P, P, P, S, P]),
+            "kvc_am_fit": (I32, [C, SG, P, P, I32, F, P, P, I32, P, P, P, S, P]),
             "kvc_debug_stall_scoring": (I32, [I64]),
         }
         for name, (res, args) in sig.items():
@@ -421,10 +421,11 @@ def kvc_am_workspace_size(cache: Cache, segs: Segments, m, R: int) -> int:
 
 def kvc_am_fit(cache: Cache, segs: Segments, m, q: torch.Tensor, R: int, scale: float,
                keep: torch.Tensor, sweeps: int, beta: Optional[torch.Tensor], vc: Optional[torch.Tensor],
-               ws: torch.Tensor, stream=None):
+               ws: torch.Tensor, stream=None, lse: Optional[torch.Tensor] = None):
     mm = _host_i32(m)
     _check(lib().kvc_am_fit(cache.ref, segs.ref, mm.ctypes.data, _dev_ptr(q, "q", torch.bfloat16), int(R),
-                            float(scale), _dev_ptr(keep, "keep", torch.int32), int(sweeps),
+                            float(scale), _dev_ptr(lse, "lse", torch.float32),
+                            _dev_ptr(keep, "keep", torch.int32), int(sweeps),
                             _dev_ptr(beta, "beta", torch.float32), _dev_ptr(vc, "vc", torch.float32),
                             _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
            "kvc_am_fit")
@@ -514,16 +515,18 @@ class Compactor:
         kvc_lrfu_update(self.cache, self.segs, self.attn, frac, lam, self.scores, hits, stream)
 
     def am_fit(self, q: torch.Tensor, scale: float, sweeps: int = 8, keep: Optional[torch.Tensor] = None,
-               beta: Optional[torch.Tensor] = None, vc: Optional[torch.Tensor] = None, stream=None):
+               beta: Optional[torch.Tensor] = None, vc: Optional[torch.Tensor] = None, stream=None,
+               lse: Optional[torch.Tensor] = None):
         """Attention Matching on the kept entries: beta into the cache's aux values (when it has
-        them) and `beta`, V_C over the kept V rows and into `vc`."""
+        them) and `beta`, V_C over the kept V rows and into `vc`.  `lse`: the rows' LSE from
+        this compactor's scoring (self.lse after score(want_lse=True)), or None to recompute it."""
         if getattr(self, "am_ws", None) is None:
             nbytes = max(256, kvc_am_workspace_size(self.cache, self.segs, self.m, self.R))
             self.am_ws_raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.keep.device)
             off = (-self.am_ws_raw.data_ptr()) % 256
             self.am_ws = self.am_ws_raw[off:off + nbytes]
         kvc_am_fit(self.cache, self.segs, self.m, q, self.R, scale, self.keep if keep is None else keep,
-                   sweeps, beta, vc, self.am_ws, stream)
+                   sweeps, beta, vc, self.am_ws, stream, lse=lse)
 
     def select(self, stream=None):
         kvc_select_topm(self.cache, self.segs, self.scores, self.m, self.keep, None, stream)

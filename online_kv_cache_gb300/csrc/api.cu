@@ -1280,8 +1280,8 @@ kvc_status kvc_am_workspace_size(const kvc_cache* cache, const kvc_segments* seg
 }
 
 kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const int32_t* m, const uint16_t* q,
-                      int32_t R, float scale, const int32_t* keep, int32_t sweeps, float* beta, float* vc, void* ws,
-                      size_t ws_bytes, kvc_stream_t stream) {
+                      int32_t R, float scale, const float* lse, const int32_t* keep, int32_t sweeps, float* beta,
+                      float* vc, void* ws, size_t ws_bytes, kvc_stream_t stream) {
   const NvtxRange nvtx_range("kvc_am_fit");
   Plan p;
   kvc_status st = check_am_args(cache, segs, m, R, &p);
@@ -1291,6 +1291,8 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
   if (p.Mtot == 0) return ok();
   if (q == nullptr || !aligned16(q)) return fail(KVC_ERR_INVALID_ARG, "q is NULL or not 16-byte aligned");
   if (keep == nullptr) return fail(KVC_ERR_INVALID_ARG, "keep is NULL");
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(KVC_ERR_INVALID_ARG, "lse is not 4-byte aligned");
   const int64_t qrows = (int64_t)cache->batch * cache->num_layers * cache->num_kv_heads * R;
   if (qrows >= (int64_t(1) << 31)) return fail(KVC_ERR_UNSUPPORTED, "B*L*H*R >= 2^31");
   AmPlan ap;
@@ -1302,12 +1304,17 @@ kvc_status kvc_am_fit(const kvc_cache* cache, const kvc_segments* segs, const in
     return fail(KVC_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
   DeviceInfo di;
   if ((st = device_info(&di)) != KVC_OK) return st;
-  // the LSE of every proxy row over its segment's keys: the scoring LSE pass
+  // the LSE of every proxy row over its segment's keys: the caller's (the scoring
+  // LSE pass's own output for the same rows), else the scoring LSE pass here
   uint8_t* score_ws = static_cast<uint8_t*>(ws) + align256((size_t)ap.floats * sizeof(float));
-  float* lse_rows = reinterpret_cast<float*>(score_ws + align256(score_bytes));
-  if ((st = score_common("kvc_am_fit", kPhaseLse, 2.0f, cache, segs, q, R, scale, nullptr, lse_rows, nullptr,
-                         score_ws, align256(score_bytes), stream)) != KVC_OK)
-    return st;
+  const float* lse_rows = lse;
+  if (lse_rows == nullptr) {
+    float* own = reinterpret_cast<float*>(score_ws + align256(score_bytes));
+    if ((st = score_common("kvc_am_fit", kPhaseLse, 2.0f, cache, segs, q, R, scale, nullptr, own, nullptr,
+                           score_ws, align256(score_bytes), stream)) != KVC_OK)
+      return st;
+    lse_rows = own;
+  }
   const int64_t krows = (int64_t)cache->num_layers * cache->num_pages * cache->num_kv_heads * cache->page_size;
   CUtensorMap tmK, tmV, tmQ;
   if ((st = make_kmap(&tmK, cache->k_pool, krows, cache->head_dim, cache->page_size)) != KVC_OK) return st;

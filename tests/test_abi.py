@@ -263,15 +263,16 @@ def test_am_validation(lib):
     assert size(m, 4097)[0] == kvc.KVC_ERR_UNSUPPORTED
     assert size(m, 0)[0] == kvc.KVC_ERR_UNSUPPORTED
 
-    def fit(mm=m, R=16, scale=0.1, q=0x60000, keep=0x70000, sweeps=4, ws=0x80000, ws_bytes=1 << 30):
-        return lib.kvc_am_fit(ctypes.byref(c), ctypes.byref(s), mm.ctypes.data, q, R, scale, keep, sweeps, None,
-                              None, ws, ws_bytes, None)
+    def fit(mm=m, R=16, scale=0.1, q=0x60000, keep=0x70000, sweeps=4, ws=0x80000, ws_bytes=1 << 30, lse=None):
+        return lib.kvc_am_fit(ctypes.byref(c), ctypes.byref(s), mm.ctypes.data, q, R, scale, lse, keep, sweeps,
+                              None, None, ws, ws_bytes, None)
 
     assert fit(sweeps=-1) == kvc.KVC_ERR_INVALID_ARG
     assert fit(sweeps=1001) == kvc.KVC_ERR_INVALID_ARG
     assert fit(scale=float("inf")) == kvc.KVC_ERR_INVALID_ARG
     assert fit(q=0x60004) == kvc.KVC_ERR_INVALID_ARG
     assert fit(keep=None) == kvc.KVC_ERR_INVALID_ARG
+    assert fit(lse=0x90002) == kvc.KVC_ERR_INVALID_ARG  # a caller's LSE must be 4-byte aligned
     assert fit(ws_bytes=b16 - 256) == kvc.KVC_ERR_WORKSPACE
     assert fit(ws=0x80010) == kvc.KVC_ERR_WORKSPACE
     assert fit(np.array([20, -1], np.int32)) == kvc.KVC_ERR_BUDGET

@@ -269,3 +269,30 @@ def test_am_multi_turn_shape_sampled(qdist):
         units[(b, l, h)] = am.unit(am.bf16_to_f64(qb[b, l, h]), K, V, keep_np[l, h, :m[0]], sp.scale, 8)
     kinds = check_units(units, m, beta, vc, 8, sample=sample)
     assert kinds["concentrated" if qdist == "planted4" else "well"] == len(sample)
+
+
+def test_caller_lse_gives_the_same_fit():
+    """kvc_am_fit with the LSE kvc_score wrote for the same rows runs no LSE pass of its own and
+    gives bit-identical beta, V_C and V pool (the same pass computed the same numbers); the
+    proxy rows span two row ranges of the value fit's Gram product and a ragged last key tile."""
+    sp = workloads.custom(L=2, H=2, G=4, d=128, P=16, q=24, lengths=(700, 333), shuffle_pages=True,
+                          qdist="normal")
+    outs = []
+    for use_lse in (False, True):
+        case = workloads.build(sp, 11, DEV)
+        m = [oracle.budget_ratio(n, 0.2) for n in PT.seg_lengths(case)]
+        cp = kvc.Compactor(case.k_pool, case.v_pool, case.tags, case.block_table, case.nblocks, case.free_ids,
+                           case.free_top, case.seg_start, case.seg_end, case.seq_len, m, sp.R)
+        cp.score(case.q, sp.scale, want_lse=True)
+        cp.select()
+        beta = torch.full((sp.L, sp.H, max(1, cp.Mtot)), float("nan"), device=DEV)
+        vc = torch.full((sp.L, sp.H, max(1, cp.Mtot), sp.d), float("nan"), device=DEV)
+        cp.am_fit(case.q, sp.scale, 6, beta=beta, vc=vc, lse=cp.lse if use_lse else None)
+        torch.cuda.synchronize()
+        PT.device_status_clean()
+        outs.append((beta.cpu().numpy(), vc.cpu().numpy(), bits(case.v_pool), cp.keep.cpu().numpy()))
+    (b0, v0, p0, k0), (b1, v1, p1, k1) = outs
+    np.testing.assert_array_equal(k0, k1)
+    np.testing.assert_array_equal(b0.view(np.uint32), b1.view(np.uint32))
+    np.testing.assert_array_equal(v0.view(np.uint32), v1.view(np.uint32))
+    np.testing.assert_array_equal(p0, p1)
