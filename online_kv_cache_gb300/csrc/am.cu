@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sV = sK + kTcStages * kTile;           // V ring
   int32_t* sKeep = reinterpret_cast<int32_t*>(sV + kTcStages * kTile);  // the unit's kept positions
   float* sTr = reinterpret_cast<float*>(sKeep + kAmMaxM);  // [kTcEpi][32][33] turn-around
-  float* red = reinterpret_cast<float*>(tc_smem + 576);  // [one per warp] maxima of the rows' LSE
+  float* red = reinterpret_cast<float*>(tc_smem + 576);  // [kTcEpi] epilogue warps' maxima of the rows' LSE
 
   const int rb = (meta.R + kTcRows - 1) / kTcRows;
   const AmUnit u = am_unit(meta, blockIdx.x / rb, ws);
@@ -199,20 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // must hold finite values (their probabilities are 0)
   for (int i = threadIdx.x; i < kTcStages * 2 * kTile / 16; i += kTcThreads)
     reinterpret_cast<uint4*>(sK)[i] = make_uint4(0u, 0u, 0u, 0u);
-  // the unit's kept positions (ascending) and the shift c = max_i LSE_i of its rows
-  const int64_t krow0 = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
-  for (int k = threadIdx.x; k < u.m; k += kTcThreads) {
-    const int32_t pos = __ldg(keep + krow0 + k);
-    // the tile walk below needs the positions inside the segment and strictly ascending
-    if (pos < 0 || pos >= u.n || (k > 0 && pos <= __ldg(keep + krow0 + k - 1))) atomicOr(status, KVC_DEV_BAD_KEEP);
-    sKeep[k] = pos;
-  }
   const int64_t lrow = (((int64_t)u.b * meta.L + u.l) * meta.H + u.h) * meta.R;
-  float cmax = -INFINITY;
-  for (int k = threadIdx.x; k < meta.R; k += kTcThreads) cmax = fmaxf(cmax, __ldg(lse_rows + lrow + k));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cmax;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kTcStages; ++i) {
@@ -361,11 +348,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int i = r0 + r;                  // proxy row
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c2 = meta.scale * kLog2e;
+    // the unit's kept positions (ascending) and the shift c = max_i LSE_i of its
+    // rows, loaded by the epilogue warps alone while the producers already stream
+    const int et = threadIdx.x - 64;  // 0 .. 32 kTcEpi - 1
+    const int64_t krow0 = ((int64_t)u.l * meta.H + u.h) * meta.Mtot + u.moff;
+    for (int k = et; k < u.m; k += 32 * kTcEpi) {
+      const int32_t pos = __ldg(keep + krow0 + k);
+      // the tile walk below needs the positions inside the segment and strictly ascending
+      if (pos < 0 || pos >= u.n || (k > 0 && pos <= __ldg(keep + krow0 + k - 1))) atomicOr(status, KVC_DEV_BAD_KEEP);
+      sKeep[k] = pos;
+    }
+    float cmax = -INFINITY;
+    for (int k = et; k < meta.R; k += 32 * kTcEpi) cmax = fmaxf(cmax, __ldg(lse_rows + lrow + k));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    if (lane == 0) red[warp - 2] = cmax;
+    bar_sync_n(1, 32 * kTcEpi);  // sKeep and red complete
     const float lse = i < meta.R ? lse_rows[lrow + i] : INFINITY;
     const float lse2 = lse * kLog2e;
     float c = red[0];
 #pragma unroll
-    for (int w = 1; w < kTcThreads / 32; ++w) c = fmaxf(c, red[w]);
+    for (int w = 1; w < kTcEpi; ++w) c = fmaxf(c, red[w]);
     const float cc = c * kLog2e;
     // stores of E and Y go through the warp's 32 x 33 turn-around, so that each
     // runs along one row (lane = column) instead of down 32 rows (lane = row)
