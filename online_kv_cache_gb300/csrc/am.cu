@@ -34,7 +34,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -518,8 +517,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //           (range p > 0 into Bp part p - 1); it runs in the same launch as
 //           mode 1, whose blocks come first and never read B
 //   mode 3: A = H (m rows), B = X0 (the kept values), C = H X0 - Bm in Bm's
-//           place, Bm's row ranges added in order (the value fit's starting
-//           gradient; H is symmetric)
+//           place, Bm's first row range only (the value fit's starting
+//           gradient once the value fit subtracts the others; H is symmetric)
 // on tcgen05 with fp32-level accuracy: every fp32 value
 // x is split into three bf16 parts (x0 = bf16(x), x1 = bf16(x - x0),
 // x2 = bf16(x - x0 - x1): 8 + 8 + 8 significant bits, x0 + x1 + x2 = x to the
@@ -600,7 +599,7 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b) {
 __global__ void __launch_bounds__(kTbThreads, 1)
     am_atb_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const AmMeta meta, float* ws, int mode_lo, int bpu_lo, int64_t blocks_lo, int bpu2,
-                     int parts2, unsigned* status) {
+                     unsigned* status) {
   extern __shared__ __align__(16) uint8_t tb_smem[];
   uint64_t* done = reinterpret_cast<uint64_t*>(tb_smem);  // [kTbBufs] an operand buffer's MMAs are done
   uint64_t* ready = done + kTbBufs;                        // [kTbBufs] an operand buffer is split
@@ -613,16 +612,16 @@ __global__ void __launch_bounds__(kTbThreads, 1)
                                              ~uintptr_t(1023));
   float* ring = reinterpret_cast<float*>(bufs + kTbBufs * kTbBuf);
   // blocks [0, blocks_lo) run mode_lo over all K rows; the others (modes 1 and 2
-  // in one launch) run mode 2 over one of parts2 ranges of the rows
+  // in one launch) run mode 2 over one of meta.bm_parts ranges of the rows
   int mode = mode_lo, blocks_per_unit = bpu_lo, part = 0, nparts = 1;
   int64_t lb = blockIdx.x;
   if (lb >= blocks_lo) {
     lb -= blocks_lo;
     mode = 2;
     blocks_per_unit = bpu2;
-    nparts = parts2;
-    part = (int)(lb % parts2);
-    lb /= parts2;
+    nparts = meta.bm_parts;
+    part = (int)(lb % nparts);
+    lb /= nparts;
   }
   const int64_t unit = lb / blocks_per_unit;
   const AmUnit u = am_unit(meta, unit, ws);
@@ -815,10 +814,9 @@ __global__ void __launch_bounds__(kTbThreads, 1)
     // consecutive columns of one row.
     float* tr = reinterpret_cast<float*>(bufs) + warp * 32 * 33;
     // C: G or H (stride ldE), Bm (stride d), or (mode 2, row range p > 0) Bp part p - 1
-    const float* Bp = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, meta.d);
-    const int64_t bp_stride = (int64_t)meta.max_m * meta.d;
     float* C = mode >= 2 ? u.base + am_off_Bm(meta.R, meta.max_m, u.ldE, meta.d) : u.base + am_off_G(meta.R, u.ldE);
-    if (mode == 2 && part > 0) C = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, meta.d) + (part - 1) * bp_stride;
+    if (mode == 2 && part > 0)
+      C = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, meta.d) + (part - 1) * (int64_t)meta.max_m * meta.d;
     const int ldc = mode >= 2 ? meta.d : u.ldE;
 #pragma unroll 1
     for (int k = 0; k < ntiles && warp < 16; ++k) {
@@ -841,24 +839,15 @@ __global__ void __launch_bounds__(kTbThreads, 1)
       for (int t = 0; t < 32; ++t) tr[lane * 33 + t] = y[t];
       __syncwarp();
       const int q = qb + lane;  // this lane's column; rows p0w .. p0w + 31
-      if (mode == 3) {  // C = H X0 - Bm, 8 rows at a time: their Bm values first (its row ranges in order)
-        static_assert(kAmBmParts == 4, "the row ranges of Bm are added below one by one");
+      if (mode == 3) {  // C = H X0 - (Bm's first row range), 16 rows at a time: their Bm values first
 #pragma unroll
-        for (int r0 = 0; r0 < 32; r0 += 8) {
-          float bm[8];
+        for (int r0 = 0; r0 < 32; r0 += 16) {
+          float bm[16];
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int64_t o = (int64_t)(p0w + r0 + r) * ldc + q;
-            bm[r] = 0.0f;
-            if (p0w + r0 + r < M && q < N) {
-              bm[r] = C[o];
-              if (parts2 > 1) bm[r] += Bp[o];
-              if (parts2 > 2) bm[r] += Bp[bp_stride + o];
-              if (parts2 > 3) bm[r] += Bp[2 * bp_stride + o];
-            }
-          }
+          for (int r = 0; r < 16; ++r)
+            bm[r] = (p0w + r0 + r < M && q < N) ? C[(int64_t)(p0w + r0 + r) * ldc + q] : 0.0f;
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+          for (int r = 0; r < 16; ++r)
             if (p0w + r0 + r < M && q < N) C[(int64_t)(p0w + r0 + r) * ldc + q] = tr[(r0 + r) * 33 + lane] - bm[r];
         }
       } else {
@@ -1237,9 +1226,16 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
       thrb[i] = d > 0.0f ? kAmGuard * p : INFINITY;
     }
   }
-  for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {  // the starting gradient H X0 - Bm (Bm's place)
-    const int i = e / kVc, c = e % kVc;
-    Gs[c * ldv + i] = G0[(int64_t)i * D + col0 + c];
+  {  // the starting gradient: H X0 - (Bm's first row range) in Bm's place, minus its other ranges in order
+    const float* Bp = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, D);
+    const int64_t bp_stride = (int64_t)meta.max_m * D;
+    for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
+      const int i = e / kVc, c = e % kVc;
+      const int64_t o = (int64_t)i * D + col0 + c;
+      float g0 = G0[o];
+      for (int p = 1; p < meta.bm_parts; ++p) g0 -= Bp[(p - 1) * bp_stride + o];
+      Gs[c * ldv + i] = g0;
+    }
   }
   if (threadIdx.x < 2 * kVc) S[threadIdx.x] = 0.0f;  // S: max |Y| bits, Sx: max |X0| bits
   if (threadIdx.x < 2) moved[threadIdx.x] = 0;
@@ -1431,11 +1427,9 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     if ((e = check()) != cudaSuccess) return e;
     const int g0 = atb_blocks_per_unit(0, m.max_m, D), g1 = atb_blocks_per_unit(1, m.max_m, D);
     const int g2 = atb_blocks_per_unit(2, m.max_m, D), g3 = atb_blocks_per_unit(3, m.max_m, D);
-    // Bm's row ranges: as many as there are 16-row chunks, at most kAmBmParts
-    const int parts = std::min(kAmBmParts, (m.R + kTbRows - 1) / kTbRows);
-    const int64_t nb0 = m.units * g0, nb1 = m.units * g1, nb2 = m.units * g2 * parts, nb3 = m.units * g3;
+    const int64_t nb0 = m.units * g0, nb1 = m.units * g1, nb2 = m.units * g2 * m.bm_parts, nb3 = m.units * g3;
     am_atb_tc_kernel<<<(unsigned)nb0, kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmX[ci], m, al.ws, 0, g0, nb0,
-                                                                     0, 1, al.status);
+                                                                     0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_mass_kernel<<<(unsigned)m.units, kAmThreads, mass_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, al.ws, al.aux, al.beta, al.status);
@@ -1445,10 +1439,10 @@ cudaError_t launch_am_d(const AmLaunch& al, cudaStream_t stream) {
     // H = Ph^T Ph and Bm = Ph^T Y in one launch (mode 1 never reads B): Bm's
     // row-range blocks fill the SMs the blocks of H leave idle
     am_atb_tc_kernel<<<(unsigned)(nb1 + nb2), kTbThreads, kTbSmem, stream>>>(al.tmX[ci], al.tmY[ci], m, al.ws, 1,
-                                                                             g1, nb1, g2, parts, al.status);
+                                                                             g1, nb1, g2, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_atb_tc_kernel<<<(unsigned)nb3, kTbThreads, kTbSmem, stream>>>(al.tmH[ci], al.tmX0[ci], m, al.ws, 3, g3, nb3,
-                                                                     0, parts, al.status);
+                                                                     0, al.status);
     if ((e = check()) != cudaSuccess) return e;
     am_value_kernel<D><<<(unsigned)(m.units * (D / kVc)), kAmThreads, value_smem_bytes(m.max_m), stream>>>(
         m, al.block_table, al.keep, vp, al.ws, al.vc, al.status);

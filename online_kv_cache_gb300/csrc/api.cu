@@ -1203,6 +1203,7 @@ void build_am_plan(const kvc_cache* c, const Plan& p, int R, float scale, int sw
     am.R = R;
     am.sweeps = sweeps;
     am.scale = scale;
+    am.bm_parts = std::min(kAmBmParts, (R + 15) / 16);  // at most one range per 16-row chunk
     am.Mtot = p.Mtot;
     const size_t a1 = std::min(act.size(), a0 + (size_t)kMaxSeqPerLaunch);
     am.nseq = (int)(a1 - a0);

@@ -154,8 +154,8 @@ constexpr int kLrfuMaxSegment = 1 << 20;
 //                  overwritten by H = Ph^T Ph for the value fit
 //   Y   [R][d]     full attention output softmax(L) V
 //   lse [R]        natural-log row mass of the full attention
-//   Bm  [m][d]     Ph^T Y over the first of its row ranges (the value fit's
-//                  starting gradient H X0 - Bm replaces it)
+//   Bm  [m][d]     Ph^T Y over the first of its row ranges (H X0 minus it
+//                  replaces it; the value fit subtracts the other ranges)
 //   w   [m4]       fitted exp(beta)
 //   X   [m][d]     the value fit's unknowns (from the kept values X0)
 //   Bp  [kAmBmParts - 1][m][d]  Ph^T Y over the other row ranges
@@ -174,7 +174,7 @@ struct AmMeta {
   int32_t max_m;   // largest m of the launch (grid sizing)
   int32_t sweeps;  // coordinate-descent sweeps of each fit
   float scale;
-  int32_t pad;
+  int32_t bm_parts;  // row ranges Bm = Ph^T Y is summed over (1 .. kAmBmParts)
   int64_t Mtot;
   int64_t units;   // units of this launch
   AmSeq seq[kMaxSeqPerLaunch];
@@ -196,7 +196,8 @@ __host__ __device__ inline int64_t am_off_X(int R, int m, int ldE, int d) {
 }
 // Bm = Ph^T Y is summed over up to kAmBmParts row ranges by separate blocks
 // (they fill the SMs the blocks of H = Ph^T Ph leave idle); range p > 0 lands
-// in Bp part p - 1 and the starting-gradient product adds them to Bm in order.
+// in Bp part p - 1.  The starting-gradient product leaves H X0 - (range 0) in
+// Bm's place and the value fit subtracts ranges 1, 2, .. in order as it loads it.
 constexpr int kAmBmParts = 4;
 __host__ __device__ inline int64_t am_off_Bp(int R, int m, int ldE, int d) {
   return am_off_X(R, m, ldE, d) + (int64_t)m * d;
