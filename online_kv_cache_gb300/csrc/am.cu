@@ -1229,12 +1229,16 @@ __global__ void __launch_bounds__(kAmThreads, 3) am_value_kernel(const AmMeta me
   {  // the starting gradient: H X0 - (Bm's first row range) in Bm's place, minus its other ranges in order
     const float* Bp = u.base + am_off_Bp(meta.R, meta.max_m, u.ldE, D);
     const int64_t bp_stride = (int64_t)meta.max_m * D;
+    static_assert(kAmBmParts == 4, "three more row ranges at most, loaded side by side below");
+    const int np = meta.bm_parts;
     for (int e = threadIdx.x; e < m * kVc; e += kAmThreads) {
       const int i = e / kVc, c = e % kVc;
       const int64_t o = (int64_t)i * D + col0 + c;
-      float g0 = G0[o];
-      for (int p = 1; p < meta.bm_parts; ++p) g0 -= Bp[(p - 1) * bp_stride + o];
-      Gs[c * ldv + i] = g0;
+      const float g0 = G0[o];
+      const float b1 = np > 1 ? Bp[o] : 0.0f;
+      const float b2 = np > 2 ? Bp[bp_stride + o] : 0.0f;
+      const float b3 = np > 3 ? Bp[2 * bp_stride + o] : 0.0f;
+      Gs[c * ldv + i] = ((g0 - b1) - b2) - b3;
     }
   }
   if (threadIdx.x < 2 * kVc) S[threadIdx.x] = 0.0f;  // S: max |Y| bits, Sx: max |X0| bits
