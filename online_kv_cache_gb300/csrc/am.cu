@@ -19,16 +19,16 @@
 // probabilities split into two bf16 parts; the Gram products, which the
 // ill-conditioned fits need to fp32 accuracy (a single bf16 or tf32 rounding
 // would put ~1e-3 into them), with every fp32 operand split into three bf16
-// parts.  The coordinate descents are fp32 on the CUDA cores.  Per unit the
-// kernels run
-//   (scoring LSE pass) LSE_i over all n keys, the rows' log-sum-exp
+// parts.  The coordinate descents are fp32 on the CUDA cores.  Per unit, after
+// the rows' log-sum-exp LSE_i over all n keys (the scoring LSE pass, the
+// caller's or run by the entry point), the kernels run in launch order
 //   am_targets_tc_kernel  Y = softmax(L) V over all n keys on the tensor cores
 //                      and E = exp(L_C - c) over the kept keys, s = exp(LSE - c)
+//   am_x0_kernel       X0 = the kept values (fp32)
 //   am_atb_tc_kernel   G = E^T [E | s]              (mode 0, tensor cores)
 //   am_mass_kernel     w by projected coordinate descent; beta = ln w
 //   am_probs_kernel    Ph = rows of E diag(w), normalised (in place)
-//   am_atb_tc_kernel   H = Ph^T Ph, Bm = Ph^T Y     (modes 1, 2)
-//   am_x0_kernel       X0 = the kept values (fp32)
+//   am_atb_tc_kernel   H = Ph^T Ph, Bm = Ph^T Y     (modes 1 and 2, one launch)
 //   am_atb_tc_kernel   H X0 - Bm, the value fit's starting gradient (mode 3)
 //   am_value_kernel    V_C by coordinate descent; written to the pool (bf16)
 #include <cuda_bf16.h>

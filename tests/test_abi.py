@@ -258,6 +258,17 @@ def test_am_validation(lib):
 
     st, b16 = size(m, 16)
     assert st == kvc.KVC_OK and b16 > 0 and b16 % 256 == 0
+    # the header's count: per unit about 4 ((R + M)(M + 4) + R (d + 1) + M (5 d + 1)) bytes with M the
+    # largest m launched together, plus the LSE pass's workspace and 4 B L H R bytes of row LSE
+    for R in (16, 64, 200):
+        M, d = int(m.max()), c.head_dim
+        units = 2 * c.num_layers * c.num_kv_heads
+        floats = (R + M) * (M + 4) + R * (d + 1) + M * (5 * d + 1)
+        score = ctypes.c_size_t(0)
+        assert lib.kvc_score_workspace_size(ctypes.byref(c), ctypes.byref(s), R, ctypes.byref(score)) == kvc.KVC_OK
+        low = units * 4 * floats + score.value + 4 * c.batch * c.num_layers * c.num_kv_heads * R
+        got = size(m, R)[1]
+        assert low <= got <= low + units * (256 + 64) + 3 * 256, (R, got, low)
     assert size(m, 64)[1] > b16
     assert size(np.zeros(2, np.int32), 16) == (kvc.KVC_OK, 0)
     assert size(m, 4097)[0] == kvc.KVC_ERR_UNSUPPORTED
