@@ -94,21 +94,6 @@ __device__ __forceinline__ void bar_arrive_n(int id, int n) {
   asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Barrier `id` over `n` threads that also returns the AND of every
-// participant's `pred` (non-aligned form).
-__device__ __forceinline__ bool bar_red_and_n(int id, int n, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "r"(id), "r"(n)
-      : "memory");
-  return out != 0;
-}
-
 // ------------------------------------------------------------------ cp.async (4-byte)
 
 // Asynchronous 4-byte global -> shared copy (completion tracked per thread by
@@ -147,16 +132,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
-// 16-byte aligned), completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
